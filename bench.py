@@ -1,0 +1,467 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE expert-parallel dispatch / combine hot path on GB300.
+
+One step = routing layout + bf16 dispatch (rows and metadata) + combine over one
+batch of the DeepSeek-V3-shaped workload: T=4096 tokens, hidden 7168 bf16,
+top-8 of 256 experts, W=8 logical ranks.  Inputs are seeded synthetic data
+resident in HBM; combine reads a separate buffer of expert outputs (identity
+experts: a copy of the dispatched rows), as it would after the expert GEMMs.
+L2 (129 MB) is flushed by a 256 MiB write before every timed step.
+
+Prints ONE JSON line.  ``value`` is the step's algorithmic HBM GB/s (bytes the
+method must move, summed over ranks, over the max-over-ranks step time); the
+per-kernel microseconds and GB/s are in ``us`` and ``gbs``.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (single thread) on the same workload
+and metric, on bounded token slices per step.  For N > 1 (torchrun, one process
+per GPU) every rank runs an independent replica (weak scaling; the path has no
+exchange step on one device); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch & combine µs and achieved HBM GB/s (% of peak), T=4096 H=7168 top-8"
+WORKLOAD = "dsv3"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------- byte model
+
+def alg_bytes(T: int, H: int, E: int, k: int, W: int, R: int) -> dict:
+    """Minimum HBM bytes each kernel must move (x read once per token)."""
+    layout = T * k * 4 + T * W * 4 + (E + 2 * W + 1) * 4
+    dispatch = T * H * 2 + T * k * 8 + T * W * 4 + R * H * 2 + R * (8 * k + 4)
+    combine = R * H * 2 + T * W * 4 + T * H * 2
+    return {"layout": layout, "dispatch": dispatch, "combine": combine,
+            "step": layout + dispatch + combine}
+
+
+def expected_rows(T: int, E: int, k: int, W: int) -> float:
+    """E[R] for k distinct uniform experts: T * W * (1 - C(E - E/W, k) / C(E, k))."""
+    Er = E // W
+    p = 1.0
+    for i in range(k):
+        p *= (E - Er - i) / (E - i)
+    return T * W * (1.0 - p)
+
+
+def pages_convention_gbs(R: int, H: int, elem: int, seconds: float) -> float:
+    """GB/s as the mori pages count it: one side of the payload, R * H * elem bytes."""
+    return R * H * elem / seconds / 1e9
+
+
+# ----------------------------------------------------------------- helpers
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _kernel_source_hash(kernel_file: str) -> str:
+    h = hashlib.sha256()
+    for name in (kernel_file, "ep_device.cuh"):
+        with open(os.path.join(ROOT, "combine_ep_dispatch_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_from_profile(kernel: str, kernel_file: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (its 'source_sha256_16' line), else None."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{WORKLOAD}.txt")
+    try:
+        txt = open(p).read()
+    except OSError:
+        return None
+    m = re.search(r"^source_sha256_16:\s*(\S+)", txt, re.M)
+    b = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", txt, re.M)
+    if not m or not b or m.group(1) != _kernel_source_hash(kernel_file):
+        return None
+    return float(b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            if self.t_start and not (self.t_start - 0.15 <= ts <= (self.t_stop or ts) + 0.15):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in timed region"],
+                    "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": rows[0][1],
+                "reasons": reasons, "samples": len(rows)}
+
+
+def aggregate(stats, nbytes, world, device):
+    """Max over ranks of each timing entry, sum over ranks of the bytes moved."""
+    import torch
+
+    st = torch.tensor([float(v) for v in stats], dtype=torch.float64, device=device)
+    b = torch.tensor([float(nbytes)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.all_reduce(st, op=dist.ReduceOp.MAX)
+        dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return st.tolist(), b.item()
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args) -> dict | None:
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import combine_ep_dispatch_gb300 as ep
+    from combine_ep_dispatch_gb300.inputs import CONFIGS, make_inputs
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    __graft_entry__.build()
+    ep.load_library()
+
+    cfg = CONFIGS[WORKLOAD]
+    inp = make_inputs(cfg, seed=args.seed + rank)
+    T, H, E, k, W = cfg.T, cfg.H, cfg.E, cfg.k, cfg.W
+    stream = torch.cuda.Stream(device=dev)
+
+    x_h = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    idx_h = torch.from_numpy(inp["topk_idx"]).pin_memory()
+    w_h = torch.from_numpy(inp["topk_w"]).pin_memory()
+    x = x_h.to(dev)
+    idx = idx_h.to(dev)
+    w = w_h.to(dev)
+    dc = ep.DispatchCombine(T, H, E, k, W, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    # expert outputs of identity experts, in a buffer of their own
+    with torch.cuda.stream(stream):
+        dc.layout(idx, stream)
+        dc.dispatch(x, idx, w, stream)
+    stream.synchronize()
+    R = int(dc.rank_offset[W].item())
+    y = dc.recv_x.clone()
+    torch.cuda.synchronize()
+    nbytes = alg_bytes(T, H, E, k, W, R)
+
+    # correctness guard of the timed configuration: identity experts give d_t * x
+    with torch.cuda.stream(stream):
+        dc.combine(y, stream)
+    stream.synchronize()
+    d = (dc.slot >= 0).sum(dim=1, keepdim=True).to(torch.float32)
+    ok = torch.equal(dc.out, (x.float() * d).to(torch.bfloat16)) and int(dc.status.item()) == 0
+    if not ok:
+        raise RuntimeError("bench: combine(dispatch(x)) != d_t * x on the timed workload")
+
+    def step(events=None):
+        if events is not None:
+            events[0].record(stream)
+        dc.layout(idx, stream)
+        if events is not None and len(events) == 4:
+            events[1].record(stream)
+        dc.dispatch(x, idx, w, stream)
+        if events is not None and len(events) == 4:
+            events[2].record(stream)
+        dc.combine(y, stream)
+        if events is not None:
+            events[-1].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            flush.fill_(i & 0xFF)
+            step()
+        stream.synchronize()
+
+        # (1) the K timed steps: events at step boundaries only, so consecutive
+        # kernels of a step overlap their launch latency as they would in use.
+        # A 20 ms device sleep first lets the host queue launches ahead of the GPU.
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        sampler.mark_start()
+        torch.cuda._sleep(40_000_000)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            step(ev[i])
+        torch.cuda.synchronize()
+        barrier()
+        step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+
+        # (2) per-kernel breakdown: events between the kernels
+        evk = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(40_000_000)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            step(evk[i])
+        torch.cuda.synchronize()
+        sampler.mark_stop()
+    clocks = sampler.stop()
+    lay_ms = [e[0].elapsed_time(e[1]) for e in evk]
+    dis_ms = [e[1].elapsed_time(e[2]) for e in evk]
+    com_ms = [e[2].elapsed_time(e[3]) for e in evk]
+
+    # (3) end to end through the public API with host buffers: pinned host inputs
+    # in, result out, every step
+    out_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    n_e2e = max(3, min(args.steps, 100))
+    eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            flush.fill_(i & 0xFF)
+            eve[i][0].record(stream)
+            x.copy_(x_h, non_blocking=True)
+            idx.copy_(idx_h, non_blocking=True)
+            w.copy_(w_h, non_blocking=True)
+            dc.step(x, idx, w, None, stream)
+            out_h.copy_(dc.out, non_blocking=True)
+            eve[i][1].record(stream)
+        torch.cuda.synchronize()
+    e2e_ms = [e[0].elapsed_time(e[1]) for e in eve]
+
+    mean = statistics.fmean
+    (s_ms, l_ms, d_ms, c_ms, e_ms), total_bytes = aggregate(
+        [mean(step_ms), mean(lay_ms), mean(dis_ms), mean(com_ms), mean(e2e_ms)], nbytes["step"],
+        world, dev)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    peak, peak_kind = _peaks()
+    dom, dom_file, dom_ms = (("dispatch", "dispatch.cu", d_ms) if d_ms >= c_ms
+                             else ("combine", "combine.cu", c_ms))
+    achieved = nbytes[dom] / (dom_ms * 1e-3) / 1e9
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
+    h2d = x_h.numel() * 2 + idx_h.numel() * 4 + w_h.numel() * 4
+    d2h = out_h.numel() * 2
+    return {
+        "metric": METRIC,
+        "value": round(total_bytes / (s_ms * 1e-3) / 1e9, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(s_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "DeepSeek-V3 shape: T=4096 H=7168 E=256 top-8 W=8, uniform "
+                               "routing, bf16 dispatch + bf16 combine (layout+dispatch+combine)",
+                   "T": T, "H": H, "E": E, "k": k, "W": W, "R": R, "seed": args.seed,
+                   "l2": "flushed by a 256 MiB write before every step (outside the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "us": {"step": round(s_ms * 1e3, 2), "layout": round(l_ms * 1e3, 2),
+               "dispatch": round(d_ms * 1e3, 2), "combine": round(c_ms * 1e3, 2)},
+        "gbs": {"step": round(gbs(nbytes["step"], s_ms), 1),
+                "layout": round(gbs(nbytes["layout"], l_ms), 1),
+                "dispatch": round(gbs(nbytes["dispatch"], d_ms), 1),
+                "combine": round(gbs(nbytes["combine"], c_ms), 1),
+                "frac_of_peak": {"dispatch": round(gbs(nbytes["dispatch"], d_ms) / peak, 4),
+                                 "combine": round(gbs(nbytes["combine"], c_ms) / peak, 4)},
+                "pages_convention": {"dispatch": round(pages_convention_gbs(R, H, 2, d_ms * 1e-3), 1),
+                                     "combine": round(pages_convention_gbs(R, H, 2, c_ms * 1e-3), 1)}},
+        "alg_bytes": nbytes,
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": _traffic_from_profile(dom, dom_file)},
+        "cpu_baseline": cpu_baseline(args) if not args.no_cpu else None,
+        "e2e": {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def _oracle_run(inp, t0: int, t1: int) -> int:
+    """Layout + dispatch + combine of tokens [t0, t1) with the CPU oracle;
+    returns the algorithmic bytes of that slice."""
+    import oracle
+
+    cfg = inp["cfg"]
+    idx = inp["topk_idx"][t0:t1]
+    lay = oracle.layout(idx, cfg.E, cfg.W)
+    R = int(lay["rank_offset"][-1])
+    dis = oracle.dispatch(inp["x"][t0:t1], idx, inp["topk_w"][t0:t1], lay["slot"], R)
+    oracle.combine(dis["recv_x"], lay["slot"])
+    return alg_bytes(t1 - t0, cfg.H, cfg.E, cfg.k, cfg.W, R)["step"]
+
+
+def cpu_baseline(args, min_seconds: float = 10.0) -> dict:
+    """The oracle as it stands, single-threaded, on whole steps of the workload."""
+    from combine_ep_dispatch_gb300.inputs import make_inputs
+
+    inp = make_inputs(WORKLOAD, seed=args.seed)
+    T = inp["cfg"].T
+    total_b, total_s, n = 0, 0.0, 0
+    while total_s < min_seconds or n < 1:
+        t = time.perf_counter()
+        total_b += _oracle_run(inp, 0, T)
+        total_s += time.perf_counter() - t
+        n += 1
+    return {"value": round(total_b / total_s / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n} whole steps of the workload (T={T}), layout+dispatch+combine, "
+                      f"{total_s:.1f} s on one host thread"}
+
+
+def run_reference(args) -> dict | None:
+    world, rank, _ = _dist()
+    if rank != 0:
+        return None
+    from combine_ep_dispatch_gb300.inputs import make_inputs
+
+    inp = make_inputs(WORKLOAD, seed=args.seed)
+    cfg = inp["cfg"]
+    T = cfg.T
+    # calibrate the slice so that warmup + steps take about a minute
+    t = time.perf_counter()
+    _oracle_run(inp, 0, 256)
+    per_token = (time.perf_counter() - t) / 256
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    S = int(min(T, max(16, budget / per_token)))
+    pos = 0
+    for _ in range(args.warmup):
+        _oracle_run(inp, pos, pos + S)
+        pos = (pos + S) % (T - S + 1)
+    tb, ts, times = 0, 0.0, []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        tb += _oracle_run(inp, pos, pos + S)
+        dt = time.perf_counter() - t
+        ts += dt
+        times.append(dt)
+        pos = (pos + S) % (T - S + 1)
+    v = round(tb / ts / 1e9, 3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(statistics.fmean(times) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "DeepSeek-V3 shape: T=4096 H=7168 E=256 top-8 W=8, uniform "
+                               "routing, bf16 dispatch + bf16 combine (layout+dispatch+combine)",
+                   "T": T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "W": cfg.W, "seed": args.seed},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "kind": "oracle", "cores": 1,
+                         "sample": f"each step: tokens [p, p+{S}) of the workload (slices "
+                                   f"rotate), layout+dispatch+combine on one host thread"},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

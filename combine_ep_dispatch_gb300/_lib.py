@@ -1,0 +1,170 @@
+"""Thin ctypes binding of libep_gb300.so (the C ABI declared in include/ep_gb300.h).
+
+Argument marshalling only: every function takes torch CUDA tensors (and the
+caller's stream), passes raw device pointers and sizes to the library, and
+raises EPError on a non-zero return code.  All computation happens in the
+library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libep_gb300.so")
+
+EP_OK = 0
+EP_ERR_INVALID_ARG = 1
+EP_ERR_MISALIGNED = 2
+EP_ERR_UNSUPPORTED = 3
+EP_ERR_CUDA = 4
+EP_ERR_WORKSPACE = 5
+
+EP_STATUS_BAD_EXPERT = 1
+EP_STATUS_CAPACITY = 2
+
+EP_QUANT_BF16 = 0
+EP_QUANT_FP8_E4M3_B128 = 1
+
+EXPORTED = ("ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_dispatch_layout", "ep_dispatch",
+            "ep_combine", "ep_status_string")
+
+
+class EPError(RuntimeError):
+    def __init__(self, fn: str, code: int, text: str):
+        super().__init__(f"{fn} failed with code {code}: {text}")
+        self.code = code
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libep_gb300.so; raises ImportError when it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.ep_layout_workspace_bytes.argtypes = [_I64, _I, _I]
+    lib.ep_layout_workspace_bytes.restype = ctypes.c_size_t
+    lib.ep_max_recv_rows.argtypes = [_I64, _I, _I]
+    lib.ep_max_recv_rows.restype = _I64
+    lib.ep_dispatch_layout.argtypes = [_P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                       _P, _P]
+    lib.ep_dispatch_layout.restype = _I
+    lib.ep_dispatch.argtypes = [_P, _P, _P, _I64, _I, _I, _I, _P, _I64, _I, _P, _P, _P, _P, _P,
+                                _P, _P]
+    lib.ep_dispatch.restype = _I
+    lib.ep_combine.argtypes = [_P, _P, _I64, _I, _I, _I64, _P, _P, _P]
+    lib.ep_combine.restype = _I
+    lib.ep_status_string.argtypes = [_I]
+    lib.ep_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check_cuda(name: str, t: torch.Tensor | None, dtype=None, optional=False):
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _raise(fn: str, code: int):
+    if code != EP_OK:
+        raise EPError(fn, code, ep_status_string(code))
+
+
+def ep_status_string(code: int) -> str:
+    return load_library().ep_status_string(int(code)).decode()
+
+
+def ep_layout_workspace_bytes(T: int, W: int, E: int) -> int:
+    return int(load_library().ep_layout_workspace_bytes(T, W, E))
+
+
+def ep_max_recv_rows(T: int, k: int, W: int) -> int:
+    return int(load_library().ep_max_recv_rows(T, k, W))
+
+
+def ep_dispatch_layout(topk_idx: torch.Tensor, E: int, W: int,
+                       num_tokens_per_expert: torch.Tensor, num_tokens_per_rank: torch.Tensor,
+                       rank_offset: torch.Tensor, slot: torch.Tensor, workspace: torch.Tensor,
+                       status: torch.Tensor | None = None, stream=None) -> None:
+    for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
+                 ("num_tokens_per_rank", num_tokens_per_rank), ("rank_offset", rank_offset),
+                 ("slot", slot)):
+        _check_cuda(n, t, torch.int32)
+    _check_cuda("workspace", workspace)
+    _check_cuda("status", status, torch.int32, optional=True)
+    T, k = topk_idx.shape
+    rc = load_library().ep_dispatch_layout(
+        _ptr(topk_idx), T, k, E, W, _ptr(num_tokens_per_expert), _ptr(num_tokens_per_rank),
+        _ptr(rank_offset), _ptr(slot), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream))
+    _raise("ep_dispatch_layout", rc)
+
+
+def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor, W: int,
+                slot: torch.Tensor, recv_x: torch.Tensor, recv_topk_idx: torch.Tensor | None = None,
+                recv_topk_w: torch.Tensor | None = None, recv_src: torch.Tensor | None = None,
+                recv_scale: torch.Tensor | None = None, quant: int = EP_QUANT_BF16,
+                status: torch.Tensor | None = None, stream=None) -> None:
+    _check_cuda("x", x, torch.bfloat16)
+    _check_cuda("topk_idx", topk_idx, torch.int32)
+    _check_cuda("topk_w", topk_w, torch.float32)
+    _check_cuda("slot", slot, torch.int32)
+    _check_cuda("recv_x", recv_x, torch.bfloat16 if quant == EP_QUANT_BF16 else torch.uint8)
+    _check_cuda("recv_topk_idx", recv_topk_idx, torch.int32, optional=True)
+    _check_cuda("recv_topk_w", recv_topk_w, torch.float32, optional=True)
+    _check_cuda("recv_src", recv_src, torch.int32, optional=True)
+    _check_cuda("recv_scale", recv_scale, torch.float32, optional=quant == EP_QUANT_BF16)
+    _check_cuda("status", status, torch.int32, optional=True)
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    rc = load_library().ep_dispatch(
+        _ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, W, _ptr(slot), recv_x.shape[0], quant,
+        _ptr(recv_x), _ptr(recv_scale), _ptr(recv_topk_idx), _ptr(recv_topk_w), _ptr(recv_src),
+        _ptr(status), _stream(stream))
+    _raise("ep_dispatch", rc)
+
+
+def ep_combine(y: torch.Tensor, slot: torch.Tensor, out: torch.Tensor,
+               status: torch.Tensor | None = None, stream=None) -> None:
+    _check_cuda("y", y, torch.bfloat16)
+    _check_cuda("slot", slot, torch.int32)
+    _check_cuda("out", out, torch.bfloat16)
+    _check_cuda("status", status, torch.int32, optional=True)
+    T, W = slot.shape
+    H = out.shape[1]
+    if y.dim() != 2 or y.shape[1] != H:
+        raise ValueError("y must be [capacity_rows, H] with the same H as out")
+    rc = load_library().ep_combine(_ptr(y), _ptr(slot), T, H, W, y.shape[0], _ptr(out),
+                                   _ptr(status), _stream(stream))
+    _raise("ep_combine", rc)

@@ -1,0 +1,124 @@
+// C ABI of the library: argument checks on the host, then kernel launches.
+// Nothing here allocates, synchronises or keeps per-call state.
+#include <stdint.h>
+
+#include "ep_device.cuh"
+
+namespace ep {
+
+int device_sm_count() {
+  static int cache[128];  // per device ordinal; 0 = not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 128) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+}  // namespace ep
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int64_t kMaxRows = 0x7fffffffLL;  // receive rows are int32
+
+inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t ep_layout_workspace_bytes(int64_t T, int W, int E) {
+  if (T < 0 || W < 1 || W > 32 || E < 1) return 0;
+  return ep::layout_workspace_bytes(T, W, E);
+}
+
+int64_t ep_max_recv_rows(int64_t T, int k, int W) {
+  if (T < 0 || k < 1 || W < 1) return -1;
+  return T * min64(k, W);
+}
+
+int ep_dispatch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int W,
+                       int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                       int32_t* rank_offset, int32_t* slot, void* workspace,
+                       size_t workspace_bytes, int32_t* status, ep_stream_t stream) {
+  if (T < 0 || k < 1 || W < 1 || W > 32 || E < 1 || E > 8192 || E % W != 0)
+    return EP_ERR_INVALID_ARG;
+  if (T * min64(k, W) > kMaxRows || T > kMaxRows / W) return EP_ERR_UNSUPPORTED;
+  if (!num_tokens_per_expert || !num_tokens_per_rank || !rank_offset || !workspace)
+    return EP_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !slot)) return EP_ERR_INVALID_ARG;
+  if (workspace_bytes < ep::layout_workspace_bytes(T, W, E)) return EP_ERR_WORKSPACE;
+  if (!aligned(topk_idx, 4) || !aligned(num_tokens_per_expert, 4) ||
+      !aligned(num_tokens_per_rank, 4) || !aligned(rank_offset, 4) || !aligned(slot, 4) ||
+      !aligned(workspace, 16) || !aligned(status, 4))
+    return EP_ERR_MISALIGNED;
+  return from_cuda(ep::launch_layout(topk_idx, T, k, E, W, num_tokens_per_expert,
+                                     num_tokens_per_rank, rank_offset, slot, workspace, status,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T, int H,
+                int k, int W, const int32_t* slot, int64_t capacity_rows, int quant, void* recv_x,
+                float* recv_scale, int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
+                int32_t* status, ep_stream_t stream) {
+  if (T < 0 || H < 1 || k < 1 || W < 1 || W > 32 || capacity_rows < 0 || capacity_rows > kMaxRows)
+    return EP_ERR_INVALID_ARG;
+  if (quant != EP_QUANT_BF16 && quant != EP_QUANT_FP8_E4M3_B128) return EP_ERR_INVALID_ARG;
+  if (quant == EP_QUANT_BF16 && H % 8 != 0) return EP_ERR_UNSUPPORTED;
+  if (quant == EP_QUANT_FP8_E4M3_B128 && H % 128 != 0) return EP_ERR_UNSUPPORTED;
+  if (T > kMaxRows / W) return EP_ERR_UNSUPPORTED;
+  if (T > 0 && (!x || !topk_idx || !topk_w || !slot)) return EP_ERR_INVALID_ARG;
+  if (capacity_rows > 0 && !recv_x) return EP_ERR_INVALID_ARG;
+  if (capacity_rows > 0 && quant == EP_QUANT_FP8_E4M3_B128 && !recv_scale)
+    return EP_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(recv_x, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+      !aligned(slot, 4) || !aligned(recv_scale, 4) || !aligned(recv_topk_idx, 4) ||
+      !aligned(recv_topk_w, 4) || !aligned(recv_src, 4) || !aligned(status, 4))
+    return EP_ERR_MISALIGNED;
+  return from_cuda(ep::launch_dispatch(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, quant,
+                                       recv_x, recv_scale, recv_topk_idx, recv_topk_w, recv_src,
+                                       status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ep_combine(const void* y, const int32_t* slot, int64_t T, int H, int W, int64_t capacity_rows,
+               void* out, int32_t* status, ep_stream_t stream) {
+  if (T < 0 || H < 1 || W < 1 || W > 32 || capacity_rows < 0 || capacity_rows > kMaxRows)
+    return EP_ERR_INVALID_ARG;
+  if (H % 8 != 0) return EP_ERR_UNSUPPORTED;
+  if (T > kMaxRows / W) return EP_ERR_UNSUPPORTED;
+  if (T > 0 && (!slot || !out)) return EP_ERR_INVALID_ARG;
+  if (T > 0 && capacity_rows > 0 && !y) return EP_ERR_INVALID_ARG;
+  if (!aligned(y, 16) || !aligned(out, 16) || !aligned(slot, 4) || !aligned(status, 4))
+    return EP_ERR_MISALIGNED;
+  return from_cuda(ep::launch_combine(y, slot, T, H, W, capacity_rows, out, status,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* ep_status_string(int code) {
+  switch (code) {
+    case EP_OK:
+      return "EP_OK";
+    case EP_ERR_INVALID_ARG:
+      return "EP_ERR_INVALID_ARG: a size or pointer argument is out of range or NULL";
+    case EP_ERR_MISALIGNED:
+      return "EP_ERR_MISALIGNED: payload pointers need 16-byte, index pointers 4-byte alignment";
+    case EP_ERR_UNSUPPORTED:
+      return "EP_ERR_UNSUPPORTED: shape outside the supported set";
+    case EP_ERR_CUDA:
+      return "EP_ERR_CUDA: the CUDA runtime refused a launch";
+    case EP_ERR_WORKSPACE:
+      return "EP_ERR_WORKSPACE: workspace smaller than ep_layout_workspace_bytes()";
+    default:
+      return "unknown ep status code";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,246 @@
+// Dispatch: one warp per token reads the token's row once and writes it to the
+// receive row of every destination rank (bf16 bit copy, or FP8 e4m3 with one
+// fp32 scale per 1x128 block), and carries the top-k ids, weights and the
+// source index along.
+#include "ep_device.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kDThreads = 256;
+
+// Destinations of token t in ascending rank order: lane i < nd holds the i-th
+// destination's receive row.  Rows at or beyond the capacity are dropped and
+// reported.  (The cached (token, rank) -> row map of "perf(ep): optimize
+// IntraNode dispatch kernel for MI350X", Technical Details 1, is `slot`.)
+struct Dests {
+  int nd;
+  int my_row;
+  bool cap_err;
+};
+
+__device__ __forceinline__ Dests token_dests(const int32_t* __restrict__ slot, int64_t t, int W,
+                                             int64_t cap, int lane) {
+  int s = -1;
+  if (lane < W) s = __ldg(slot + t * W + lane);
+  const bool keep = s >= 0 && (int64_t)s < cap;
+  const bool over = s >= 0 && (int64_t)s >= cap;
+  const unsigned dmask = __ballot_sync(kFull, keep);
+  const int r = nth_set_bit_of_lane(dmask, lane);
+  const int row = __shfl_sync(kFull, s, r & 31);
+  Dests d;
+  d.nd = __popc(dmask);
+  d.my_row = r >= 0 ? row : -1;
+  d.cap_err = __any_sync(kFull, over);
+  return d;
+}
+
+// Metadata of one token for all its destinations: per destination row, k ids,
+// k weights and the source index (2k+1 words), written by the whole warp at
+// once ("perf(ep): optimize IntraNode dispatch kernel for MI350X", Technical
+// Details 4).
+__device__ __forceinline__ void carry_metadata(const int32_t* __restrict__ topk_idx,
+                                               const float* __restrict__ topk_w, int64_t t, int k,
+                                               const Dests& d, int32_t* __restrict__ recv_topk_idx,
+                                               float* __restrict__ recv_topk_w,
+                                               int32_t* __restrict__ recv_src, int lane) {
+  const int per = 2 * k + 1;
+  const int total = d.nd * per;
+  for (int base = 0; base < total; base += 32) {
+    const int i = base + lane;
+    const int dd = i / per;
+    const int j = i - dd * per;
+    const int row = __shfl_sync(kFull, d.my_row, dd & 31);
+    if (i < total) {
+      if (j < k) {
+        if (recv_topk_idx) recv_topk_idx[(int64_t)row * k + j] = __ldg(topk_idx + t * k + j);
+      } else if (j < 2 * k) {
+        if (recv_topk_w) recv_topk_w[(int64_t)row * k + (j - k)] = __ldg(topk_w + t * k + (j - k));
+      } else if (recv_src) {
+        recv_src[row] = (int32_t)t;
+      }
+    }
+  }
+}
+
+// bf16 payload: lane l moves 16-byte chunks l, l+32, ... of the row; U chunks
+// are loaded before the stores of a round so that each lane keeps U loads in
+// flight.  The row is read once whatever the number of destinations.
+template <int U>
+__global__ void __launch_bounds__(kDThreads)
+    dispatch_bf16_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ topk_idx,
+                         const float* __restrict__ topk_w, int64_t T, int n16, int k, int W,
+                         const int32_t* __restrict__ slot, int64_t cap, uint4* __restrict__ recv_x,
+                         int32_t* __restrict__ recv_topk_idx, float* __restrict__ recv_topk_w,
+                         int32_t* __restrict__ recv_src, int32_t* __restrict__ status) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = ((int64_t)blockIdx.x * kDThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kDThreads) >> 5;
+  bool cap_err = false;
+  for (int64_t t = gwarp; t < T; t += nwarps) {
+    const Dests d = token_dests(slot, t, W, cap, lane);
+    cap_err |= d.cap_err;
+    carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
+    const uint4* src = x + t * n16;
+    for (int c0 = 0; c0 < n16; c0 += 32 * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < n16) v[u] = ld_stream_v4(src + c);
+      }
+      for (int dg = 0; dg < d.nd; dg += 8) {
+        int rows[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) rows[q] = __shfl_sync(kFull, d.my_row, (dg + q) & 31);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (dg + q < d.nd) {
+            uint4* dst = recv_x + (int64_t)rows[q] * n16;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const int c = c0 + u * 32 + lane;
+              if (c < n16) st_v4(dst + c, v[u]);
+            }
+          }
+        }
+      }
+    }
+  }
+  pdl_launch_dependents();
+  if (cap_err && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_CAPACITY);
+}
+
+// Two fp32 values to two e4m3 codes, round to nearest even, saturating to
+// +-448: `lo` goes to the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// FP8 payload.  A 128-column block is 256 bytes of bf16 = 16 lanes x 16 bytes,
+// so a warp covers two blocks per round (lanes 0-15 and 16-31).  Per block:
+// amax over the block (a 16-lane max reduction), scale = amax / 448, codes =
+// e4m3(x / scale); both divisions are IEEE round-to-nearest.  The token is
+// quantised once and the codes and scales are stored to every destination.
+template <int U>
+__global__ void __launch_bounds__(kDThreads)
+    dispatch_fp8_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ topk_idx,
+                        const float* __restrict__ topk_w, int64_t T, int H, int k, int W,
+                        const int32_t* __restrict__ slot, int64_t cap, uint8_t* __restrict__ recv_x,
+                        float* __restrict__ recv_scale, int32_t* __restrict__ recv_topk_idx,
+                        float* __restrict__ recv_topk_w, int32_t* __restrict__ recv_src,
+                        int32_t* __restrict__ status) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
+  const int nb = H >> 7;
+  const int n16 = H >> 3;
+  const int64_t gwarp = ((int64_t)blockIdx.x * kDThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kDThreads) >> 5;
+  bool cap_err = false;
+  for (int64_t t = gwarp; t < T; t += nwarps) {
+    const Dests d = token_dests(slot, t, W, cap, lane);
+    cap_err |= d.cap_err;
+    carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
+    const uint4* src = x + t * n16;
+    for (int b0 = 0; b0 < nb; b0 += 2 * U) {
+      uint2 q[U];
+      float sc[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int b = b0 + 2 * u + half;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (b < nb) v = ld_stream_v4(src + b * 16 + hl);
+        const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(f[i]));
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(kFull, a, o));
+        const float s = __fdiv_rn(a, 448.0f);
+        sc[u] = s;
+        if (s == 0.0f) {
+          q[u] = make_uint2(0u, 0u);
+        } else {
+          uint32_t c[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            c[i] = e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+          q[u] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+        }
+      }
+      for (int dg = 0; dg < d.nd; dg += 8) {
+        int rows[8];
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) rows[qq] = __shfl_sync(kFull, d.my_row, (dg + qq) & 31);
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) {
+          if (dg + qq < d.nd) {
+            uint8_t* dst = recv_x + (int64_t)rows[qq] * H;
+            float* dsc = recv_scale + (int64_t)rows[qq] * nb;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const int b = b0 + 2 * u + half;
+              if (b < nb) {
+                st_v2(reinterpret_cast<uint2*>(dst + b * 128 + hl * 8), q[u]);
+                if (hl == 0) dsc[b] = sc[u];
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  pdl_launch_dependents();
+  if (cap_err && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_CAPACITY);
+}
+
+template <typename K>
+int grid_for(K kernel, int64_t T, int threads) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t want = (T * 32 + threads - 1) / threads;  // one warp per token
+  const int64_t cap = (int64_t)device_sm_count() * per_sm;
+  int64_t g = want < cap ? want : cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w,
+                            int64_t T, int H, int k, int W, const int32_t* slot,
+                            int64_t capacity_rows, int quant, void* recv_x, float* recv_scale,
+                            int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
+                            int32_t* status, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const uint4* x4 = static_cast<const uint4*>(x);
+  if (quant == EP_QUANT_BF16) {
+    const int n16 = H / 8;
+    if (n16 % (32 * 7) == 0) {
+      auto kern = dispatch_bf16_kernel<7>;
+      return launch_pdl(kern, dim3(grid_for(kern, T, kDThreads)), dim3(kDThreads), 0, stream, x4,
+                        topk_idx, topk_w, T, n16, k, W, slot, capacity_rows,
+                        static_cast<uint4*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status);
+    }
+    auto kern = dispatch_bf16_kernel<8>;
+    return launch_pdl(kern, dim3(grid_for(kern, T, kDThreads)), dim3(kDThreads), 0, stream, x4,
+                      topk_idx, topk_w, T, n16, k, W, slot, capacity_rows,
+                      static_cast<uint4*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status);
+  }
+  auto kern = dispatch_fp8_kernel<2>;
+  return launch_pdl(kern, dim3(grid_for(kern, T, kDThreads)), dim3(kDThreads), 0, stream, x4,
+                    topk_idx, topk_w, T, H, k, W, slot, capacity_rows,
+                    static_cast<uint8_t*>(recv_x), recv_scale, recv_topk_idx, recv_topk_w, recv_src,
+                    status);
+}
+
+}  // namespace ep

@@ -1,0 +1,100 @@
+// Device helpers and kernel launchers shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ep_gb300.h"
+
+namespace ep {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ------------------------------------------------------------ dependent launch
+// Every kernel of the library is launched with programmatic stream
+// serialization and begins with pdl_wait(): the grid may become resident while
+// the previous kernel on the stream drains, but touches no memory until that
+// kernel has completed and its writes are visible.  Every CTA executes the wait
+// before it can exit, so completion stays transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------ memory access
+// Read-once streaming load of 16 bytes: no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// 16-byte store of data that is not read again by this kernel.
+__device__ __forceinline__ void st_v4(uint4* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_v2(uint2* p, const uint2& v) {
+  asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// ------------------------------------------------------------ warp helpers
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Position of the (lane+1)-th set bit of `mask`, counting from bit 0 upwards:
+// lane i < popc(mask) receives the rank of its i-th destination; the other
+// lanes receive -1.
+__device__ __forceinline__ int nth_set_bit_of_lane(unsigned mask, int lane) {
+  return (int)__fns(mask, 0, lane + 1);
+}
+
+// ------------------------------------------------------------ launchers
+int device_sm_count();  // cached per device; 0 on error
+
+cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int W,
+                          int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                          int32_t* rank_offset, int32_t* slot, void* workspace, int32_t* status,
+                          cudaStream_t stream);
+size_t layout_workspace_bytes(int64_t T, int W, int E);
+
+cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w,
+                            int64_t T, int H, int k, int W, const int32_t* slot,
+                            int64_t capacity_rows, int quant, void* recv_x, float* recv_scale,
+                            int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
+                            int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H, int W,
+                           int64_t capacity_rows, void* out, int32_t* status, cudaStream_t stream);
+
+// cudaLaunchKernelEx with the programmatic-stream-serialization attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+}  // namespace ep

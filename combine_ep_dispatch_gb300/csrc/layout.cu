@@ -1,0 +1,192 @@
+// Routing layout: per-expert and per-rank counts, a stable exclusive scan over
+// the per-rank counts, and the receive slot of every (token, rank) pair.
+//
+// Two kernels, both over chunks of kLT tokens (one token per thread):
+//   count: decode each token's expert ids into its destination-rank bit set
+//          (deduplication by construction), tally the chunk's per-rank and
+//          per-expert counts into the workspace;
+//   scan:  every CTA reduces the per-chunk rank counts (all chunks, and those
+//          before its own), derives rank_offset and its chunk's base row per
+//          rank, then numbers its tokens in ascending order with warp ballots.
+// Integer counts only, no atomics whose order could leak into a result: the
+// layout is a pure function of topk_idx.
+#include "ep_device.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kLT = 256;  // tokens per CTA
+constexpr int kLWarps = kLT / 32;
+
+inline size_t a256(size_t b) { return (b + 255) & ~size_t(255); }
+
+struct LayoutWs {
+  uint32_t* mask;       // [T]     bit r set iff r in D(t)
+  int32_t* chunk_rank;  // [C][W]  tokens of chunk c with r in D(t)
+  int32_t* chunk_exp;   // [C][E]  (t, j) entries of chunk c with expert e
+};
+
+inline int64_t num_chunks(int64_t T) { return T <= 0 ? 1 : (T + kLT - 1) / kLT; }
+
+LayoutWs carve(void* ws, int64_t T, int W) {
+  char* p = static_cast<char*>(ws);
+  const int64_t C = num_chunks(T);
+  LayoutWs w;
+  w.mask = reinterpret_cast<uint32_t*>(p);
+  p += a256(sizeof(uint32_t) * (size_t)T);
+  w.chunk_rank = reinterpret_cast<int32_t*>(p);
+  p += a256(sizeof(int32_t) * (size_t)(C * W));
+  w.chunk_exp = reinterpret_cast<int32_t*>(p);
+  return w;
+}
+
+// Destination ranks of a token: rank = expert / experts-per-rank, one entry per
+// distinct rank ("perf(ep): optimize IntraNode dispatch kernel for MI350X",
+// Technical Details 1).  The bit set is the cached routing of that section: it
+// is computed here once and consumed by the scan.
+__global__ void __launch_bounds__(kLT)
+    layout_count_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k, int E, int W,
+                        int Er, LayoutWs ws, int32_t* __restrict__ status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  extern __shared__ int32_t s_hist[];  // [E]
+  __shared__ int32_t s_warp_rank[kLWarps][32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += kLT) s_hist[e] = 0;
+  __syncthreads();
+
+  const int64_t t = (int64_t)blockIdx.x * kLT + tid;
+  const bool live = t < T;
+  const int32_t* row = topk_idx + (live ? t * k : 0);
+  uint32_t m = 0;
+  bool bad = false;
+  for (int j = 0; j < k; ++j) {
+    const int e = live ? __ldg(row + j) : -1;
+    const bool ok = (unsigned)e < (unsigned)E;
+    bad |= live && !ok;
+    if (ok) m |= 1u << (e / Er);
+    // lanes holding the same expert add once, with their number
+    const unsigned peers = __match_any_sync(kFull, ok ? e : -1);
+    if (ok && lane == __ffs(peers) - 1) atomicAdd(&s_hist[e], __popc(peers));
+  }
+  if (live) ws.mask[t] = m;
+
+  int cnt = 0;
+  for (int r = 0; r < W; ++r) {
+    const unsigned b = __ballot_sync(kFull, (m >> r) & 1u);
+    if (lane == r) cnt = __popc(b);
+  }
+  if (lane < W) s_warp_rank[warp][lane] = cnt;
+  if (__any_sync(kFull, bad) && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_BAD_EXPERT);
+  __syncthreads();
+
+  if (tid < W) {
+    int s = 0;
+    for (int w = 0; w < kLWarps; ++w) s += s_warp_rank[w][tid];
+    ws.chunk_rank[(int64_t)blockIdx.x * W + tid] = s;
+  }
+  for (int e = tid; e < E; e += kLT) ws.chunk_exp[(int64_t)blockIdx.x * E + e] = s_hist[e];
+}
+
+// Stable exclusive scan and slots.  The receive rows of rank r are
+// [rank_offset[r], rank_offset[r+1]) in ascending token order; the slot of
+// (t, r) is rank_offset[r] + (rows of r in earlier chunks) + (rows of r in
+// earlier warps of this chunk) + (rows of r in earlier lanes of this warp).
+__global__ void __launch_bounds__(kLT)
+    layout_scan_kernel(int64_t T, int E, int W, int64_t C, LayoutWs ws,
+                       int32_t* __restrict__ num_tokens_per_expert,
+                       int32_t* __restrict__ num_tokens_per_rank, int32_t* __restrict__ rank_offset,
+                       int32_t* __restrict__ slot) {
+  pdl_wait();
+  __shared__ int32_t s_total[32], s_before[32], s_base[32];
+  __shared__ int32_t s_warp_cnt[kLWarps][32];
+  __shared__ int32_t s_warp_pre[kLWarps][32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t c = blockIdx.x;
+
+  for (int r = warp; r < W; r += kLWarps) {
+    int tot = 0, bef = 0;
+    for (int64_t q = lane; q < C; q += 32) {
+      const int v = ws.chunk_rank[q * W + r];
+      tot += v;
+      if (q < c) bef += v;
+    }
+    tot = warp_sum(tot);
+    bef = warp_sum(bef);
+    if (lane == 0) {
+      s_total[r] = tot;
+      s_before[r] = bef;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int r = 0; r < W; ++r) {
+      s_base[r] = acc + s_before[r];
+      if (c == 0) {
+        rank_offset[r] = acc;
+        num_tokens_per_rank[r] = s_total[r];
+      }
+      acc += s_total[r];
+    }
+    if (c == 0) rank_offset[W] = acc;
+  }
+
+  const int64_t t = c * kLT + tid;
+  const bool live = t < T;
+  const uint32_t m = live ? ws.mask[t] : 0u;
+  int cnt = 0;
+  for (int r = 0; r < W; ++r) {
+    const unsigned b = __ballot_sync(kFull, (m >> r) & 1u);
+    if (lane == r) cnt = __popc(b);
+  }
+  if (lane < W) s_warp_cnt[warp][lane] = cnt;
+  __syncthreads();
+  if (tid < W) {
+    int acc = s_base[tid];
+    for (int w = 0; w < kLWarps; ++w) {
+      s_warp_pre[w][tid] = acc;
+      acc += s_warp_cnt[w][tid];
+    }
+  }
+  __syncthreads();
+
+  const unsigned lt = lanemask_lt();
+  int32_t* srow = slot + (live ? t * W : 0);
+  for (int r = 0; r < W; ++r) {
+    const unsigned in_r = (m >> r) & 1u;
+    const unsigned b = __ballot_sync(kFull, in_r);
+    if (live) srow[r] = in_r ? s_warp_pre[warp][r] + __popc(b & lt) : -1;
+  }
+
+  for (int64_t e = c * kLT + tid; e < E; e += (int64_t)gridDim.x * kLT) {
+    int s = 0;
+    for (int64_t q = 0; q < C; ++q) s += ws.chunk_exp[q * E + e];
+    num_tokens_per_expert[e] = s;
+  }
+  pdl_launch_dependents();
+}
+
+}  // namespace
+
+size_t layout_workspace_bytes(int64_t T, int W, int E) {
+  const int64_t C = num_chunks(T);
+  return a256(sizeof(uint32_t) * (size_t)T) + a256(sizeof(int32_t) * (size_t)(C * W)) +
+         a256(sizeof(int32_t) * (size_t)(C * E));
+}
+
+cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int W,
+                          int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                          int32_t* rank_offset, int32_t* slot, void* workspace, int32_t* status,
+                          cudaStream_t stream) {
+  const int64_t C = num_chunks(T);
+  const LayoutWs ws = carve(workspace, T, W);
+  cudaError_t err = launch_pdl(layout_count_kernel, dim3((unsigned)C), dim3(kLT),
+                               sizeof(int32_t) * (size_t)E, stream, topk_idx, T, k, E, W, E / W, ws,
+                               status);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(layout_scan_kernel, dim3((unsigned)C), dim3(kLT), 0, stream, T, E, W, C, ws,
+                    num_tokens_per_expert, num_tokens_per_rank, rank_offset, slot);
+}
+
+}  // namespace ep

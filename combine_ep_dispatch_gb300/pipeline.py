@@ -1,0 +1,70 @@
+"""Preallocated buffers for one dispatch/combine shape, and the three calls on them.
+
+PyTorch allocates the device memory once; every step then only enqueues the
+library's kernels (layout -> dispatch -> [experts] -> combine) on one stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+
+class DispatchCombine:
+    """Buffers for T tokens of hidden size H routed top-k over E experts on W ranks.
+
+    ``capacity_rows`` defaults to the worst case T * min(k, W), so dispatch can
+    never overflow.  ``quant`` selects the dispatch payload (bf16 or FP8 e4m3
+    with 1x128 block scales); combine always reads bf16 expert outputs.
+    """
+
+    def __init__(self, T: int, H: int, E: int, k: int, W: int, capacity_rows: int | None = None,
+                 quant: int = _lib.EP_QUANT_BF16, device: str | torch.device = "cuda"):
+        self.T, self.H, self.E, self.k, self.W, self.quant = T, H, E, k, W, quant
+        dev = torch.device(device)
+        cap = _lib.ep_max_recv_rows(T, k, W) if capacity_rows is None else capacity_rows
+        self.capacity_rows = cap
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.num_tokens_per_expert = torch.empty(E, **i32)
+        self.num_tokens_per_rank = torch.empty(W, **i32)
+        self.rank_offset = torch.empty(W + 1, **i32)
+        self.slot = torch.empty(T, W, **i32)
+        self.workspace = torch.empty(max(_lib.ep_layout_workspace_bytes(T, W, E), 16),
+                                     dtype=torch.uint8, device=dev)
+        if quant == _lib.EP_QUANT_BF16:
+            self.recv_x = torch.empty(cap, H, dtype=torch.bfloat16, device=dev)
+            self.recv_scale = None
+        else:
+            self.recv_x = torch.empty(cap, H, dtype=torch.uint8, device=dev)
+            self.recv_scale = torch.empty(cap, H // 128, dtype=torch.float32, device=dev)
+        self.recv_topk_idx = torch.empty(cap, k, **i32)
+        self.recv_topk_w = torch.empty(cap, k, dtype=torch.float32, device=dev)
+        self.recv_src = torch.empty(cap, **i32)
+        self.out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        self.status = torch.zeros(1, **i32)
+
+    def layout(self, topk_idx: torch.Tensor, stream=None) -> None:
+        _lib.ep_dispatch_layout(topk_idx, self.E, self.W, self.num_tokens_per_expert,
+                                self.num_tokens_per_rank, self.rank_offset, self.slot,
+                                self.workspace, self.status, stream)
+
+    def dispatch(self, x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                 stream=None) -> None:
+        _lib.ep_dispatch(x, topk_idx, topk_w, self.W, self.slot, self.recv_x, self.recv_topk_idx,
+                         self.recv_topk_w, self.recv_src, self.recv_scale, self.quant, self.status,
+                         stream)
+
+    def combine(self, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Sum each token's expert outputs ``y`` (default: the dispatched rows,
+        i.e. identity experts; bf16 dispatch only) into ``self.out``."""
+        if y is None:
+            if self.quant != _lib.EP_QUANT_BF16:
+                raise ValueError("identity experts need a bf16 dispatch")
+            y = self.recv_x
+        _lib.ep_combine(y, self.slot, self.out, self.status, stream)
+        return self.out
+
+    def step(self, x, topk_idx, topk_w, y=None, stream=None) -> torch.Tensor:
+        self.layout(topk_idx, stream)
+        self.dispatch(x, topk_idx, topk_w, stream)
+        return self.combine(y, stream)

@@ -1,0 +1,171 @@
+/*
+ * ep_gb300.h -- C ABI of the MoE expert-parallel dispatch / combine library
+ * (libep_gb300.so, CUDA, sm_103a).
+ *
+ * The W expert-parallel ranks are W logical partitions of one receive buffer in
+ * one GPU's memory: the "send" of a row to rank r is a store into rank r's
+ * region.  There is no collective and no second device.
+ *
+ * Conventions shared by every entry point
+ *  - Every pointer argument is a DEVICE pointer owned by the caller.  Tensors
+ *    are dense and row-major.  The library allocates nothing, keeps no state
+ *    between calls (apart from a per-device cache of the SM count) and never
+ *    synchronises: each call enqueues its kernels on `stream` and returns.
+ *  - Return value: EP_OK, or an EP_ERR_* code found on the host before anything
+ *    was enqueued (bad argument, misaligned pointer, unsupported shape), or
+ *    EP_ERR_CUDA when a launch was refused.
+ *  - Data-dependent problems are reported on the device: the kernels OR
+ *    EP_STATUS_* bits into the caller's int32 `*status` (may be NULL).  The
+ *    caller zeroes it and reads it whenever it likes; nothing traps.
+ *  - Payload pointers (x, recv_x, y, out) must be 16-byte aligned; index,
+ *    weight, count and slot pointers 4-byte aligned.
+ *  - Kernels are launched with programmatic dependent launch: each one waits
+ *    for the previous kernel on the stream to finish before it touches memory,
+ *    so consecutive calls overlap only their launch latency.
+ *
+ * Notation: T tokens, H hidden size, E experts, k experts per token, W ranks,
+ * Er = E / W experts per rank, rank(e) = e / Er, D(t) = the distinct ranks of
+ * token t's valid expert ids, R = sum over t of |D(t)| receive rows.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define EP_API __attribute__((visibility("default")))
+#else
+#define EP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st* ep_stream_t;
+
+/* Host-side return codes. */
+enum {
+  EP_OK = 0,
+  EP_ERR_INVALID_ARG = 1,  /* a size or pointer argument is out of range / NULL */
+  EP_ERR_MISALIGNED = 2,   /* a pointer violates the alignment rule above */
+  EP_ERR_UNSUPPORTED = 3,  /* shape outside the supported set (see each call) */
+  EP_ERR_CUDA = 4,         /* the CUDA runtime refused a launch */
+  EP_ERR_WORKSPACE = 5     /* workspace smaller than ep_layout_workspace_bytes() */
+};
+
+/* Device-side status bits, OR-ed into *status. */
+enum {
+  EP_STATUS_BAD_EXPERT = 1, /* an expert id outside [0, E): the entry was ignored */
+  EP_STATUS_CAPACITY = 2    /* a receive row >= capacity_rows: it was not read / written */
+};
+
+/* Dispatch payload formats. */
+enum {
+  EP_QUANT_BF16 = 0,         /* rows copied as bf16 */
+  EP_QUANT_FP8_E4M3_B128 = 1 /* rows quantised to FP8 e4m3 with one fp32 scale per 1x128 block */
+};
+
+/*
+ * Bytes of device workspace that ep_dispatch_layout needs for T tokens, W
+ * ranks and E experts.  The contents need no initialisation.
+ */
+EP_API size_t ep_layout_workspace_bytes(int64_t T, int W, int E);
+
+/*
+ * Worst-case number of receive rows, T * min(k, W): a receive buffer of this
+ * many rows can never overflow.  (Sizing the receive side for the worst case
+ * follows the size hint of "Feature/sm free normal kernel", deepseek-ai/DeepEP
+ * pull 347, section 3.3.1.)  Returns -1 for invalid arguments.
+ */
+EP_API int64_t ep_max_recv_rows(int64_t T, int k, int W);
+
+/*
+ * Routing layout.  Follows "perf(ep): optimize IntraNode dispatch kernel for
+ * MI350X" (ROCm/mori pull 586), Technical Details 1: the destination rank of
+ * expert e is e / Er, a token is sent once per destination rank, and the
+ * destination of every kept (token, rank) pair is computed once and cached for
+ * the copy and for combine.  The pages reserve receive slots with atomics; here
+ * they come from a stable prefix scan, so the layout is deterministic.
+ *
+ *  topk_idx              int32 [T, k]   expert ids; ids outside [0, E) are
+ *                                       ignored and set EP_STATUS_BAD_EXPERT
+ *  num_tokens_per_expert int32 [E]      out: #(t, j) with topk_idx[t][j] == e
+ *                                       (before deduplication)
+ *  num_tokens_per_rank   int32 [W]      out: #t with r in D(t)
+ *  rank_offset           int32 [W + 1]  out: exclusive prefix sum of
+ *                                       num_tokens_per_rank; rank_offset[W] = R
+ *  slot                  int32 [T, W]   out: receive row of (t, r):
+ *                                       rank_offset[r] + #{t' < t : r in D(t')}
+ *                                       if r in D(t), else -1
+ *  workspace             ep_layout_workspace_bytes(T, W, E) bytes, 16-byte aligned
+ * Limits: 0 <= T, T * min(k, W) < 2^31; 1 <= k; 1 <= W <= 32; E % W == 0;
+ * 1 <= E <= 8192.
+ */
+EP_API int ep_dispatch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int W,
+                       int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                       int32_t* rank_offset, int32_t* slot, void* workspace,
+                       size_t workspace_bytes, int32_t* status, ep_stream_t stream);
+
+/*
+ * Dispatch: scatter each token's row to the receive row of every rank in D(t),
+ * reading x[t] once, and carry the routing metadata with it.  Follows "perf(ep):
+ * optimize IntraNode dispatch kernel for MI350X", Technical Details 1, 3 and 4
+ * (cached destinations, warp-wide row copy, metadata copied by the whole warp)
+ * and "Optimizing Distributed Inference Kernels for AMD DEVELOPER CHALLENGE
+ * 2025", section 3.1 (16-byte vector copies of a token row).
+ *
+ *  x              bf16 [T, H]
+ *  topk_idx       int32 [T, k], topk_w fp32 [T, k]
+ *  slot           int32 [T, W] from ep_dispatch_layout
+ *  capacity_rows  rows of every receive buffer; rows >= capacity_rows are
+ *                 skipped and set EP_STATUS_CAPACITY
+ *  quant          EP_QUANT_BF16: recv_x is bf16 [capacity_rows, H], a bit copy.
+ *                 EP_QUANT_FP8_E4M3_B128: recv_x is uint8 [capacity_rows, H];
+ *                 per row and 128-column block b: scale = amax / 448 (fp32,
+ *                 IEEE division), recv_scale[s][b] = scale, code =
+ *                 e4m3 round-to-nearest-even with saturation of x / scale (fp32
+ *                 IEEE division); scale 0 gives all-zero codes.  The FP8 e4m3
+ *                 dispatch of the same page (Test Plan) is the model; the block
+ *                 scale rule is this library's.
+ *  recv_scale     fp32 [capacity_rows, H / 128] for FP8, else ignored (may be NULL)
+ *  recv_topk_idx  int32 [capacity_rows, k]  copy of topk_idx[t]  (NULL: skipped)
+ *  recv_topk_w    fp32  [capacity_rows, k]  copy of topk_w[t]    (NULL: skipped)
+ *  recv_src       int32 [capacity_rows]     source token t       (NULL: skipped)
+ * Rows of the receive buffers that no (t, r) maps to are left untouched.
+ * Limits: H % 8 == 0 (bf16) or H % 128 == 0 (FP8); 1 <= W <= 32; 1 <= k.
+ */
+EP_API int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T, int H,
+                int k, int W, const int32_t* slot, int64_t capacity_rows, int quant, void* recv_x,
+                float* recv_scale, int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
+                int32_t* status, ep_stream_t stream);
+
+/*
+ * Combine: out[t] = bf16_rne( ((+0 + y[s_0]) + y[s_1]) + ... ) with the fp32
+ * sum taken over the ranks r in D(t) in ascending order, s_r = slot[t][r]; a
+ * token with no rows gives +0.  Follows "perf(ep): optimize IntraNode dispatch
+ * kernel for MI350X", "Remaining gap" (combine reads the pre-routed rows of each
+ * token and accumulates them) and "Optimizing Distributed Inference Kernels for
+ * AMD DEVELOPER CHALLENGE 2025", section 3.1 (combine brings the expert outputs
+ * back to token order).  The sum is unweighted: the expert side applies the
+ * gate weights.
+ *
+ *  y              bf16 [capacity_rows, H]  expert outputs, one per receive row
+ *  slot           int32 [T, W] from ep_dispatch_layout
+ *  out            bf16 [T, H]
+ * Rows >= capacity_rows are skipped and set EP_STATUS_CAPACITY.
+ * Limits: H % 8 == 0; 1 <= W <= 32.
+ */
+EP_API int ep_combine(const void* y, const int32_t* slot, int64_t T, int H, int W, int64_t capacity_rows,
+               void* out, int32_t* status, ep_stream_t stream);
+
+/* Human-readable name of an EP_* return code (static string). */
+EP_API const char* ep_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_H */

@@ -1,0 +1,95 @@
+"""Helpers of the GPU parity tests: run the CUDA path through the C ABI binding on
+the same seeded inputs as the oracle, and bring results back as numpy."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import combine_ep_dispatch_gb300 as ep
+
+SENT_BF16 = 0x7FAB          # a NaN pattern no kernel writes: untouched rows keep it
+SENT_U8 = 0xA5
+SENT_I32 = -123456789
+
+
+def to_dev_bf16(a_u16: np.ndarray, dev="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a_u16).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def run_layout(topk_idx: np.ndarray, E: int, W: int, dev="cuda") -> dict:
+    T = topk_idx.shape[0]
+    idx = torch.from_numpy(np.ascontiguousarray(topk_idx, dtype=np.int32)).to(dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    ne = torch.full((E,), SENT_I32, **i32)
+    nr = torch.full((W,), SENT_I32, **i32)
+    off = torch.full((W + 1,), SENT_I32, **i32)
+    slot = torch.full((T, W), SENT_I32, **i32)
+    ws = torch.full((max(ep.ep_layout_workspace_bytes(T, W, E), 16),), 0x5A, dtype=torch.uint8,
+                    device=dev)
+    st = torch.zeros(1, **i32)
+    ep.ep_dispatch_layout(idx, E, W, ne, nr, off, slot, ws, st)
+    torch.cuda.synchronize()
+    return {"num_tokens_per_expert": ne.cpu().numpy(), "num_tokens_per_rank": nr.cpu().numpy(),
+            "rank_offset": off.cpu().numpy(), "slot": slot.cpu().numpy(), "status": int(st.item())}
+
+
+def run_dispatch(x: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, slot: np.ndarray,
+                 cap: int, quant: int, dev="cuda", with_meta=True) -> dict:
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    W = slot.shape[1]
+    i32 = dict(dtype=torch.int32, device=dev)
+    xd = to_dev_bf16(x, dev)
+    idx = torch.from_numpy(np.ascontiguousarray(topk_idx, np.int32)).to(dev)
+    w = torch.from_numpy(np.ascontiguousarray(topk_w, np.float32)).to(dev)
+    sl = torch.from_numpy(np.ascontiguousarray(slot, np.int32)).to(dev)
+    if quant == ep.EP_QUANT_BF16:
+        rx = torch.full((cap, H), SENT_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+        rs = None
+    else:
+        rx = torch.full((cap, H), SENT_U8, dtype=torch.uint8, device=dev)
+        rs = torch.full((cap, H // 128), -7.0, dtype=torch.float32, device=dev)
+    ri = torch.full((cap, k), SENT_I32, **i32) if with_meta else None
+    rw = torch.full((cap, k), -3.0, dtype=torch.float32, device=dev) if with_meta else None
+    rsrc = torch.full((cap,), SENT_I32, **i32) if with_meta else None
+    st = torch.zeros(1, **i32)
+    ep.ep_dispatch(xd, idx, w, W, sl, rx, ri, rw, rsrc, rs, quant, st)
+    torch.cuda.synchronize()
+    out = {"recv_x": u16(rx) if quant == ep.EP_QUANT_BF16 else rx.cpu().numpy(),
+           "status": int(st.item())}
+    if rs is not None:
+        out["recv_scale"] = rs.cpu().numpy()
+    if with_meta:
+        out.update(recv_topk_idx=ri.cpu().numpy(), recv_topk_w=rw.cpu().numpy(),
+                   recv_src=rsrc.cpu().numpy())
+    return out
+
+
+def run_combine(y: np.ndarray, slot: np.ndarray, H: int, cap: int | None = None, dev="cuda") -> dict:
+    T, W = slot.shape
+    yd = to_dev_bf16(y, dev)
+    if cap is not None and cap < yd.shape[0]:
+        yd = yd[:cap].contiguous()
+    sl = torch.from_numpy(np.ascontiguousarray(slot, np.int32)).to(dev)
+    out = torch.full((T, H), SENT_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ep.ep_combine(yd, sl, out, st)
+    torch.cuda.synchronize()
+    return {"out": u16(out), "status": int(st.item())}
+
+
+def assert_rows_equal(got: np.ndarray, want: np.ndarray, what: str):
+    if got.shape != want.shape:
+        raise AssertionError(f"{what}: shape {got.shape} != {want.shape}")
+    g = got.reshape(got.shape[0], -1) if got.ndim > 1 else got.reshape(-1, 1)
+    w = want.reshape(want.shape[0], -1) if want.ndim > 1 else want.reshape(-1, 1)
+    bad = np.nonzero(np.any(g != w, axis=1))[0]
+    if bad.size:
+        i = bad[0]
+        j = np.nonzero(g[i] != w[i])[0][:8]
+        raise AssertionError(f"{what}: {bad.size} rows differ, first row {i} cols {j}: "
+                             f"got {g[i][j]} want {w[i][j]}")

@@ -1,0 +1,131 @@
+"""The C ABI library builds, loads and exports every entry point that
+include/ep_gb300.h declares; host-side argument checks reject bad calls before
+anything reaches a GPU.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import combine_ep_dispatch_gb300 as ep
+from combine_ep_dispatch_gb300 import _build, _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ep_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build_library()
+    return _lib.load_library()
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"^EP_API\s+[\w\s\*]+?\b(ep_\w+)\s*\(", txt, re.M)))
+
+
+def test_header_declares_the_calls():
+    assert _declared() == sorted(_lib.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_enum_values_match_header():
+    txt = open(HEADER).read()
+    for name in ("EP_OK", "EP_ERR_INVALID_ARG", "EP_ERR_MISALIGNED", "EP_ERR_UNSUPPORTED",
+                 "EP_ERR_CUDA", "EP_ERR_WORKSPACE", "EP_STATUS_BAD_EXPERT", "EP_STATUS_CAPACITY",
+                 "EP_QUANT_BF16", "EP_QUANT_FP8_E4M3_B128"):
+        m = re.search(rf"\b{name}\s*=\s*(\d+)", txt)
+        assert m and int(m.group(1)) == getattr(_lib, name), name
+
+
+def test_size_queries(lib):
+    assert ep.ep_max_recv_rows(4096, 8, 8) == 32768
+    assert ep.ep_max_recv_rows(100, 2, 8) == 200
+    assert ep.ep_max_recv_rows(-1, 8, 8) == -1
+    assert ep.ep_layout_workspace_bytes(4096, 8, 256) >= 4096 * 4
+    assert ep.ep_layout_workspace_bytes(0, 8, 256) > 0
+    assert ep.ep_layout_workspace_bytes(10, 33, 66) == 0
+    for code in range(6):
+        assert ep.ep_status_string(code).startswith("EP_")
+
+
+# The calls below pass made-up device addresses that each violate one rule, so
+# they must return before any CUDA call.  They are skipped where a GPU exists:
+# there the same paths are covered with real tensors by the GPU tests.
+cpu_only = pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers: CPU machines only")
+
+A = 0x10000  # a 64 KiB-aligned fake address (never dereferenced)
+
+
+@cpu_only
+@pytest.mark.parametrize("args,code", [
+    # (T, k, E, W, workspace_bytes, ptr offsets)
+    ((100, 8, 256, 3, 1 << 20, 0), _lib.EP_ERR_INVALID_ARG),       # E % W != 0
+    ((100, 8, 256, 33, 1 << 20, 0), _lib.EP_ERR_INVALID_ARG),      # W > 32
+    ((100, 0, 256, 8, 1 << 20, 0), _lib.EP_ERR_INVALID_ARG),       # k < 1
+    ((-1, 8, 256, 8, 1 << 20, 0), _lib.EP_ERR_INVALID_ARG),        # T < 0
+    ((100, 8, 16384, 8, 1 << 20, 0), _lib.EP_ERR_INVALID_ARG),     # E > 8192
+    ((100, 8, 256, 8, 16, 0), _lib.EP_ERR_WORKSPACE),              # workspace too small
+    ((100, 8, 256, 8, 1 << 20, 2), _lib.EP_ERR_MISALIGNED),        # slot 2-byte aligned
+    ((1 << 29, 8, 256, 8, 1 << 40, 0), _lib.EP_ERR_UNSUPPORTED),   # rows overflow int32
+])
+def test_layout_rejects(lib, args, code):
+    T, k, E, W, wsb, off = args
+    rc = lib.ep_dispatch_layout(A, T, k, E, W, A, A, A, A + off, A, wsb, None, None)
+    assert rc == code
+
+
+@cpu_only
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=7), _lib.EP_ERR_UNSUPPORTED),                       # H % 8 for bf16
+    (dict(H=136, quant=1), _lib.EP_ERR_UNSUPPORTED),            # H % 128 for FP8
+    (dict(quant=7), _lib.EP_ERR_INVALID_ARG),
+    (dict(x_off=8), _lib.EP_ERR_MISALIGNED),                    # x 8-byte aligned
+    (dict(recv_off=4), _lib.EP_ERR_MISALIGNED),
+    (dict(cap=-1), _lib.EP_ERR_INVALID_ARG),
+    (dict(W=0), _lib.EP_ERR_INVALID_ARG),
+    (dict(quant=1, H=256, scale_null=True), _lib.EP_ERR_INVALID_ARG),
+    (dict(x_null=True), _lib.EP_ERR_INVALID_ARG),
+])
+def test_dispatch_rejects(lib, kw, code):
+    H = kw.get("H", 256)
+    quant = kw.get("quant", 0)
+    x = None if kw.get("x_null") else A + kw.get("x_off", 0)
+    scale = None if kw.get("scale_null") else A
+    rc = lib.ep_dispatch(x, A, A, 100, H, 8, kw.get("W", 8), A, kw.get("cap", 800), quant,
+                         A + kw.get("recv_off", 0), scale, A, A, A, None, None)
+    assert rc == code
+
+
+@cpu_only
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=12), _lib.EP_ERR_UNSUPPORTED),
+    (dict(y_off=2), _lib.EP_ERR_MISALIGNED),
+    (dict(out_off=8), _lib.EP_ERR_MISALIGNED),
+    (dict(W=40), _lib.EP_ERR_INVALID_ARG),
+    (dict(out_null=True), _lib.EP_ERR_INVALID_ARG),
+])
+def test_combine_rejects(lib, kw, code):
+    out = None if kw.get("out_null") else A + kw.get("out_off", 0)
+    rc = lib.ep_combine(A + kw.get("y_off", 0), A, 100, kw.get("H", 256), kw.get("W", 8), 800, out,
+                        None, None)
+    assert rc == code
+
+
+def test_binding_rejects_host_tensors(lib):
+    idx = torch.zeros(4, 2, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        ep.ep_dispatch_layout(idx, 4, 2, idx, idx, idx, idx, idx)
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        _lib.load_library()

@@ -1,0 +1,300 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element
+by element, on the same seeded inputs.  Integer, index and byte outputs and the
+bf16 combine (fixed ascending-rank fp32 order) must be bit-exact."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import combine_ep_dispatch_gb300 as ep
+import oracle
+from combine_ep_dispatch_gb300.inputs import (CONFIGS, f32_from_bf16_bits, make_bf16, make_inputs,
+                                              make_routing)
+from gpu_util import (SENT_BF16, SENT_I32, SENT_U8, assert_rows_equal, run_combine, run_dispatch,
+                      run_layout)
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _check_layout(idx, E, W):
+    want = oracle.layout(idx, E, W)
+    got = run_layout(idx, E, W)
+    for key in ("num_tokens_per_expert", "num_tokens_per_rank", "rank_offset", "slot"):
+        assert_rows_equal(got[key], want[key], key)
+    assert got["status"] == want["status"]
+    return want
+
+
+def _check_dispatch(inp, lay, cap, quant, with_meta=True):
+    want = oracle.dispatch(inp["x"], inp["topk_idx"], inp["topk_w"], lay["slot"], cap, quant)
+    got = run_dispatch(inp["x"], inp["topk_idx"], inp["topk_w"], lay["slot"], cap, quant,
+                       with_meta=with_meta)
+    R = min(int(lay["rank_offset"][-1]), cap)
+    assert got["status"] == want["status"]
+    assert_rows_equal(got["recv_x"][:R], want["recv_x"][:R], "recv_x")
+    if quant == ep.EP_QUANT_FP8_E4M3_B128:
+        assert_rows_equal(got["recv_scale"][:R].view(np.uint32), want["recv_scale"][:R].view(np.uint32),
+                          "recv_scale")
+    if with_meta:
+        assert_rows_equal(got["recv_topk_idx"][:R], want["recv_topk_idx"][:R], "recv_topk_idx")
+        assert_rows_equal(got["recv_topk_w"][:R].view(np.uint32), want["recv_topk_w"][:R].view(np.uint32),
+                          "recv_topk_w")
+        assert_rows_equal(got["recv_src"][:R], want["recv_src"][:R], "recv_src")
+    # rows beyond R are never written
+    sent = SENT_BF16 if quant == ep.EP_QUANT_BF16 else SENT_U8
+    assert np.all(got["recv_x"][R:] == sent)
+    if with_meta:
+        assert np.all(got["recv_src"][R:] == SENT_I32)
+    return want, got
+
+
+def _inputs_dev(inp):
+    return inp
+
+
+# ------------------------------------------------------------ all workloads
+
+@pytest.mark.parametrize("name", list(CONFIGS))
+def test_workload_parity_full(name):
+    """Every output of layout, dispatch and combine, bit for bit, at full size."""
+    inp = make_inputs(name, seed=0)
+    cfg = inp["cfg"]
+    quant = ep.EP_QUANT_FP8_E4M3_B128 if cfg.quant == "fp8" else ep.EP_QUANT_BF16
+    lay = _check_layout(inp["topk_idx"], cfg.E, cfg.W)
+    R = int(lay["rank_offset"][-1])
+    cap = ep.ep_max_recv_rows(cfg.T, cfg.k, cfg.W)
+    _check_dispatch(inp, lay, cap, quant)
+    # combine: random expert outputs (bf16) for every receive row
+    y = make_bf16(np.random.default_rng(100), (R, cfg.H))
+    want = oracle.combine(y, lay["slot"])
+    got = run_combine(y, lay["slot"], cfg.H)
+    assert got["status"] == want["status"] == 0
+    assert_rows_equal(got["out"], want["out"], "combine out")
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "qwen"])
+def test_identity_experts_end_to_end(name):
+    """combine(dispatch(x)) with identity experts = bf16(d_t * x), exactly."""
+    inp = make_inputs(name, seed=1)
+    cfg = inp["cfg"]
+    xd = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).cuda()
+    idx = torch.from_numpy(inp["topk_idx"]).cuda()
+    w = torch.from_numpy(inp["topk_w"]).cuda()
+    dc = ep.DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W)
+    out = dc.step(xd, idx, w)
+    torch.cuda.synchronize()
+    d = np.array([len({int(e) // cfg.Er for e in row}) for row in inp["topk_idx"]])
+    want = torch.from_numpy(f32_from_bf16_bits(inp["x"]) * d[:, None].astype(np.float32)).to(
+        torch.bfloat16)
+    got = out.cpu()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    assert dc.status.item() == 0
+
+
+def test_rank_tagged_experts():
+    """y = 2^r * row for rows of rank r: out = bf16(M_t * x), M_t = sum of 2^r."""
+    inp = make_inputs("decode", seed=2)
+    cfg = inp["cfg"]
+    lay = _check_layout(inp["topk_idx"], cfg.E, cfg.W)
+    R = int(lay["rank_offset"][-1])
+    dis = run_dispatch(inp["x"], inp["topk_idx"], inp["topk_w"], lay["slot"], R, ep.EP_QUANT_BF16)
+    rank_of_row = np.searchsorted(lay["rank_offset"], np.arange(R), side="right") - 1
+    yf = f32_from_bf16_bits(dis["recv_x"]) * (2.0 ** rank_of_row)[:, None].astype(np.float32)
+    y = torch.from_numpy(yf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = run_combine(y, lay["slot"], cfg.H)
+    m = np.array([sum(2 ** r for r in {int(e) // cfg.Er for e in row}) for row in inp["topk_idx"]])
+    want = torch.from_numpy(f32_from_bf16_bits(inp["x"]) * m[:, None].astype(np.float32)).to(
+        torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert_rows_equal(got["out"], want, "rank-tagged combine")
+
+
+def test_combine_golden_order():
+    with open(os.path.join(GOLDEN, "combine_order.json")) as f:
+        g = json.load(f)
+    lay = _check_layout(np.array(g["topk_idx"], np.int32), g["E"], g["W"])
+    y = torch.tensor(g["y_by_rank"], dtype=torch.float32)[:, None].expand(-1, 64).to(torch.bfloat16)
+    y = y.contiguous().view(torch.int16).numpy().view(np.uint16)
+    got = run_combine(y, lay["slot"], 64)
+    assert np.all(f32_from_bf16_bits(got["out"]) == np.float32(g["out"]))
+
+
+def test_golden_hand_example():
+    with open(os.path.join(GOLDEN, "layout_combine_tiny.json")) as f:
+        g = json.load(f)
+    idx = np.array(g["topk_idx"], np.int32)
+    got = run_layout(idx, g["E"], g["W"])
+    np.testing.assert_array_equal(got["slot"], g["expect"]["slot"])
+    np.testing.assert_array_equal(got["rank_offset"], g["expect"]["rank_offset"])
+    np.testing.assert_array_equal(got["num_tokens_per_expert"], g["expect"]["num_tokens_per_expert"])
+    assert got["status"] & ep.EP_STATUS_BAD_EXPERT
+    # combine needs H % 8 == 0: pad the 2-column rows with zeros
+    y = np.zeros((6, 8), np.float32)
+    y[:, :2] = np.array(g["combine"]["y"], np.float32)
+    yb = torch.from_numpy(y).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    out = run_combine(yb, got["slot"], 8)["out"]
+    outf = f32_from_bf16_bits(out)[:, :2]
+    np.testing.assert_array_equal(outf, np.array(g["combine"]["out"], np.float32))
+    np.testing.assert_array_equal(np.signbit(outf), np.array(g["combine"]["out_sign_bits_negative"]))
+
+
+# ------------------------------------------------------------ shapes and edges
+
+@pytest.mark.parametrize("T,H,E,k,W", [
+    (0, 256, 16, 4, 4),        # empty
+    (1, 8, 4, 2, 2),           # one token, one 16-byte chunk per row
+    (257, 264, 64, 6, 8),      # ragged tokens (one past a chunk) and ragged columns
+    (1000, 7168, 256, 8, 8),   # several layout chunks, not a multiple of anything
+    (333, 4096, 128, 8, 8),
+    (300, 512, 64, 16, 32),    # W = 32: up to 16 destinations (two groups of 8)
+    (200, 136, 7, 3, 1),       # W = 1, odd E
+    (513, 1024, 96, 5, 3),     # W not a power of two
+])
+def test_shapes_bf16(T, H, E, k, W):
+    rng = np.random.default_rng(T * 7 + H)
+    x = make_bf16(rng, (T, H))
+    idx = make_routing(rng, T, E, k) if T else np.zeros((0, k), np.int32)
+    w = rng.random((T, k), dtype=np.float32)
+    inp = {"x": x, "topk_idx": idx, "topk_w": w}
+    lay = _check_layout(idx, E, W)
+    R = int(lay["rank_offset"][-1])
+    cap = max(R, 1)
+    _check_dispatch(inp, lay, cap, ep.EP_QUANT_BF16)
+    y = make_bf16(rng, (cap, H))
+    want = oracle.combine(y, lay["slot"])["out"]
+    got = run_combine(y, lay["slot"], H)["out"]
+    assert_rows_equal(got, want, "combine")
+
+
+@pytest.mark.parametrize("T,H,E,k,W", [(1, 128, 8, 2, 2), (257, 384, 64, 6, 8), (64, 7168, 256, 8, 8),
+                                       (100, 1024, 64, 16, 32)])
+def test_shapes_fp8(T, H, E, k, W):
+    rng = np.random.default_rng(T + H)
+    x = make_bf16(rng, (T, H), scale=5.0)
+    idx = make_routing(rng, T, E, k)
+    w = rng.random((T, k), dtype=np.float32)
+    lay = _check_layout(idx, E, W)
+    _check_dispatch({"x": x, "topk_idx": idx, "topk_w": w}, lay, int(lay["rank_offset"][-1]),
+                    ep.EP_QUANT_FP8_E4M3_B128)
+
+
+def test_fp8_special_blocks():
+    """Zero and -0 blocks, the smallest bf16 subnormal (subnormal fp32 scale),
+    the largest bf16 values, exact +-448*2^j values, exact e4m3 ties."""
+    rng = np.random.default_rng(21)
+    T, H = 8, 1024
+    xs = rng.standard_normal((T, H)).astype(np.float32)
+    xs[0, :128] = 0.0
+    xs[0, 128:256] = -0.0
+    xs[1, :128] = 0.0
+    xs[1, 7] = 2.0 ** -133
+    xs[1, 128:256] = 2.0 ** -133 * rng.integers(-1, 2, 128)
+    xs[2, :] = 3.3e38 * np.sign(rng.standard_normal(H))
+    xs[3, :128] = 448.0 * 2.0 ** rng.integers(-20, 20, 128)
+    # ties of e4m3 after scaling: amax 56 -> scale 0.125, codes of 8*x
+    xs[4, :128] = 0.0
+    xs[4, 0] = 56.0
+    xs[4, 1:9] = [1.0625, 1.1875, -1.0625, 0.0029296875, 1.5 * 2 ** -10, 2.0 ** -12, 2.0 ** -13, 3 * 2.0 ** -13]
+    xs[5, :] = rng.standard_normal(H).astype(np.float32) * 1e-30
+    xs[6, :] = rng.standard_normal(H).astype(np.float32) * 2.0 ** rng.integers(-60, 60, H)
+    x = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    idx = np.tile(np.array([[0, 5]], np.int32), (T, 1))
+    w = np.ones((T, 2), np.float32)
+    lay = _check_layout(idx, 8, 4)
+    _check_dispatch({"x": x, "topk_idx": idx, "topk_w": w}, lay, int(lay["rank_offset"][-1]),
+                    ep.EP_QUANT_FP8_E4M3_B128)
+
+
+def test_fp8_many_values_match_oracle_encoder():
+    """Codes for 8M random normal values across many binades."""
+    rng = np.random.default_rng(22)
+    T, H = 1024, 8192
+    xs = (rng.standard_normal((T, H)) * 2.0 ** rng.integers(-30, 30, (T, 1))).astype(np.float32)
+    x = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    idx = np.zeros((T, 1), np.int32)
+    w = np.ones((T, 1), np.float32)
+    lay = _check_layout(idx, 1, 1)
+    _check_dispatch({"x": x, "topk_idx": idx, "topk_w": w}, lay, T, ep.EP_QUANT_FP8_E4M3_B128)
+
+
+def test_invalid_expert_ids_are_ignored_and_flagged():
+    rng = np.random.default_rng(31)
+    T, E, k, W, H = 500, 64, 6, 8, 256
+    idx = make_routing(rng, T, E, k)
+    idx[rng.random(idx.shape) < 0.1] = -5
+    idx[rng.random(idx.shape) < 0.05] = E
+    idx[7, :] = 1000                      # a token with no valid id
+    lay = _check_layout(idx, E, W)
+    assert lay["status"] & oracle.STATUS_BAD_EXPERT
+    x = make_bf16(rng, (T, H))
+    _check_dispatch({"x": x, "topk_idx": idx, "topk_w": rng.random((T, k), dtype=np.float32)}, lay,
+                    max(int(lay["rank_offset"][-1]), 1), ep.EP_QUANT_BF16)
+    y = make_bf16(rng, (int(lay["rank_offset"][-1]), H))
+    got = run_combine(y, lay["slot"], H)["out"]
+    assert_rows_equal(got, oracle.combine(y, lay["slot"])["out"], "combine")
+    assert np.all(got[7] == 0)            # no rows: +0
+
+
+def test_capacity_overflow_flags_and_skips():
+    inp = make_inputs("tiny", seed=41)
+    cfg = inp["cfg"]
+    lay = _check_layout(inp["topk_idx"], cfg.E, cfg.W)
+    R = int(lay["rank_offset"][-1])
+    cap = R - 50
+    want, got = _check_dispatch(inp, lay, cap, ep.EP_QUANT_BF16)
+    assert got["status"] & ep.EP_STATUS_CAPACITY
+    y = make_bf16(np.random.default_rng(42), (R, cfg.H))
+    g = run_combine(y, lay["slot"], cfg.H, cap=cap)
+    w = oracle.combine(y[:cap], lay["slot"], cap=cap)
+    assert g["status"] == w["status"] == ep.EP_STATUS_CAPACITY
+    assert_rows_equal(g["out"], w["out"], "combine under capacity")
+
+
+def test_dispatch_without_metadata_outputs():
+    inp = make_inputs("tiny", seed=43)
+    cfg = inp["cfg"]
+    lay = oracle.layout(inp["topk_idx"], cfg.E, cfg.W)
+    _check_dispatch(inp, lay, int(lay["rank_offset"][-1]), ep.EP_QUANT_BF16, with_meta=False)
+
+
+def test_deterministic_bytes():
+    inp = make_inputs("decode", seed=44)
+    cfg = inp["cfg"]
+    a = run_layout(inp["topk_idx"], cfg.E, cfg.W)
+    b = run_layout(inp["topk_idx"], cfg.E, cfg.W)
+    np.testing.assert_array_equal(a["slot"], b["slot"])
+    R = int(a["rank_offset"][-1])
+    y = make_bf16(np.random.default_rng(45), (R, cfg.H))
+    o1 = run_combine(y, a["slot"], cfg.H)["out"]
+    o2 = run_combine(y, a["slot"], cfg.H)["out"]
+    np.testing.assert_array_equal(o1, o2)
+
+
+def test_host_errors_through_binding():
+    inp = make_inputs("tiny", seed=46)
+    cfg = inp["cfg"]
+    dc = ep.DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W)
+    idx = torch.from_numpy(inp["topk_idx"]).cuda()
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_dispatch_layout(idx, cfg.E, 3, dc.num_tokens_per_expert, dc.num_tokens_per_rank,
+                              dc.rank_offset, dc.slot, dc.workspace, dc.status)   # E % W != 0
+    assert e.value.code == ep.EP_ERR_INVALID_ARG
+    small = torch.empty(8, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_dispatch_layout(idx, cfg.E, cfg.W, dc.num_tokens_per_expert, dc.num_tokens_per_rank,
+                              dc.rank_offset, dc.slot, small, dc.status)
+    assert e.value.code == ep.EP_ERR_WORKSPACE
+    x = torch.zeros(cfg.T, cfg.H + 8, dtype=torch.bfloat16, device="cuda")[:, 1:cfg.H + 1]
+    with pytest.raises(ValueError):
+        ep.ep_dispatch(x, idx, idx.float(), cfg.W, dc.slot, dc.recv_x)      # not contiguous

@@ -85,8 +85,10 @@ def run_combine(y: np.ndarray, slot: np.ndarray, H: int, cap: int | None = None,
 def assert_rows_equal(got: np.ndarray, want: np.ndarray, what: str):
     if got.shape != want.shape:
         raise AssertionError(f"{what}: shape {got.shape} != {want.shape}")
-    g = got.reshape(got.shape[0], -1) if got.ndim > 1 else got.reshape(-1, 1)
-    w = want.reshape(want.shape[0], -1) if want.ndim > 1 else want.reshape(-1, 1)
+    n = got.shape[0]
+    cols = int(np.prod(got.shape[1:])) if got.ndim > 1 else 1
+    g = got.reshape(n, cols)
+    w = want.reshape(n, cols)
     bad = np.nonzero(np.any(g != w, axis=1))[0]
     if bad.size:
         i = bad[0]

@@ -28,7 +28,10 @@ EP_QUANT_BF16 = 0
 EP_QUANT_FP8_E4M3_B128 = 1
 
 EXPORTED = ("ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_dispatch_layout", "ep_dispatch",
-            "ep_combine", "ep_status_string")
+            "ep_combine", "ep_status_string", "ep_dispatch_layout_noalloc")
+
+# Size of the library's built-in layout workspace (ep_dispatch_layout_noalloc).
+EP_LAYOUT_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 class EPError(RuntimeError):
@@ -65,6 +68,8 @@ def load_library() -> ctypes.CDLL:
     lib.ep_dispatch.restype = _I
     lib.ep_combine.argtypes = [_P, _P, _I64, _I, _I, _I64, _P, _P, _P]
     lib.ep_combine.restype = _I
+    lib.ep_dispatch_layout_noalloc.argtypes = [_P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, _P]
+    lib.ep_dispatch_layout_noalloc.restype = _I
     lib.ep_status_string.argtypes = [_I]
     lib.ep_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -168,3 +173,23 @@ def ep_combine(y: torch.Tensor, slot: torch.Tensor, out: torch.Tensor,
     rc = load_library().ep_combine(_ptr(y), _ptr(slot), T, H, W, y.shape[0], _ptr(out),
                                    _ptr(status), _stream(stream))
     _raise("ep_combine", rc)
+
+
+def ep_dispatch_layout_noalloc(topk_idx: torch.Tensor, E: int, W: int,
+                               num_tokens_per_expert: torch.Tensor,
+                               num_tokens_per_rank: torch.Tensor, rank_offset: torch.Tensor,
+                               slot: torch.Tensor, status: torch.Tensor | None = None,
+                               stream=None) -> None:
+    """ep_dispatch_layout for callers that cannot allocate device memory: the
+    workspace is the library's built-in EP_LAYOUT_NOALLOC_SCRATCH_BYTES array,
+    shared by every call (calls that overlap on the GPU race on it)."""
+    for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
+                 ("num_tokens_per_rank", num_tokens_per_rank), ("rank_offset", rank_offset),
+                 ("slot", slot)):
+        _check_cuda(n, t, torch.int32)
+    _check_cuda("status", status, torch.int32, optional=True)
+    T, k = topk_idx.shape
+    rc = load_library().ep_dispatch_layout_noalloc(
+        _ptr(topk_idx), T, k, E, W, _ptr(num_tokens_per_expert), _ptr(num_tokens_per_rank),
+        _ptr(rank_offset), _ptr(slot), _ptr(status), _stream(stream))
+    _raise("ep_dispatch_layout_noalloc", rc)

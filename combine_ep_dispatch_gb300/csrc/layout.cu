@@ -10,6 +10,8 @@
 //          rank, then numbers its tokens in ascending order with warp ballots.
 // Integer counts only, no atomics whose order could leak into a result: the
 // layout is a pure function of topk_idx.
+#include <atomic>
+
 #include "ep_device.cuh"
 
 namespace ep {
@@ -190,3 +192,64 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
 }
 
 }  // namespace ep
+
+// ---------------------------------------------------------------------------
+// Layout without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory where they need the layout: C or
+// embedded hosts with no device allocator of their own, and latency-critical
+// paths where cudaMalloc is off limits because it blocks the host and
+// synchronises the device.  For them the library keeps the layout workspace in
+// a fixed device array of EP_LAYOUT_NOALLOC_SCRATCH_BYTES, reserved on every
+// GPU that loads the library until the process exits.
+//
+// Host code cannot use the array's name as a device address (on the host it
+// names a stand-in), so the first call on each device asks the runtime for
+// the address with cudaGetSymbolAddress, with that device current, and caches
+// it; later calls reuse the cached address.  Every call uses the same array:
+// calls whose kernels overlap on the GPU (different streams, or different
+// host threads) race on it.  Nothing in it needs clearing between calls: each
+// call writes every word it reads before reading it.
+static __device__ __align__(256) unsigned char
+    g_layout_noalloc_scratch[EP_LAYOUT_NOALLOC_SCRATCH_BYTES];
+
+namespace ep {
+namespace {
+
+constexpr int kMaxDevices = 128;
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+cudaError_t noalloc_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    e = cudaGetSymbolAddress(&p, g_layout_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_addr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace ep
+
+extern "C" EP_API int ep_dispatch_layout_noalloc(const int32_t* topk_idx, int64_t T, int k, int E,
+                                                 int W, int32_t* num_tokens_per_expert,
+                                                 int32_t* num_tokens_per_rank, int32_t* rank_offset,
+                                                 int32_t* slot, int32_t* status, ep_stream_t stream) {
+  if (T < 0 || k < 1 || W < 1 || W > 32 || E < 1 || E > 8192 || E % W != 0)
+    return EP_ERR_INVALID_ARG;
+  if (T * (k < W ? k : W) > 0x7fffffffLL || T > 0x7fffffffLL / W) return EP_ERR_UNSUPPORTED;
+  if (ep::layout_workspace_bytes(T, W, E) > (size_t)EP_LAYOUT_NOALLOC_SCRATCH_BYTES)
+    return EP_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (ep::noalloc_scratch_address(&scratch) != cudaSuccess) return EP_ERR_CUDA;
+  return ep_dispatch_layout(topk_idx, T, k, E, W, num_tokens_per_expert, num_tokens_per_rank,
+                            rank_offset, slot, scratch, (size_t)EP_LAYOUT_NOALLOC_SCRATCH_BYTES,
+                            status, stream);
+}
+

@@ -161,6 +161,32 @@ EP_API int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk
 EP_API int ep_combine(const void* y, const int32_t* slot, int64_t T, int H, int W, int64_t capacity_rows,
                void* out, int32_t* status, ep_stream_t stream);
 
+/*
+ * ep_dispatch_layout without a workspace argument, for callers that cannot
+ * allocate device memory: C or embedded hosts without a device allocator, and
+ * latency-critical paths that must not call cudaMalloc (it blocks the host and
+ * synchronises the device).  The pages have no counterpart; this is an entry
+ * point of this library only.
+ *
+ * The workspace is a device array of EP_LAYOUT_NOALLOC_SCRATCH_BYTES built into
+ * the library; every GPU that loads the library holds it until the process
+ * exits.  Arguments, outputs and status bits are those of ep_dispatch_layout;
+ * the call allocates nothing.
+ *  - Returns EP_ERR_WORKSPACE when ep_layout_workspace_bytes(T, W, E) exceeds
+ *    EP_LAYOUT_NOALLOC_SCRATCH_BYTES (up to 129024 tokens at W = 8, E = 256).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture on that device.
+ *  - All calls share the one array: calls whose kernels overlap on the GPU
+ *    (other streams, other host threads) race and must be serialised by the
+ *    caller.  The array needs no clearing: each call writes what it reads.
+ */
+#define EP_LAYOUT_NOALLOC_SCRATCH_BYTES (1u << 20)
+EP_API int ep_dispatch_layout_noalloc(const int32_t* topk_idx, int64_t T, int k, int E, int W,
+                                      int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                                      int32_t* rank_offset, int32_t* slot, int32_t* status,
+                                      ep_stream_t stream);
+
 /* Human-readable name of an EP_* return code (static string). */
 EP_API const char* ep_status_string(int code);
 

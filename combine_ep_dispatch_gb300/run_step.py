@@ -1,0 +1,57 @@
+"""Run layout -> dispatch -> combine on one seeded workload a few times.
+
+A minimal driver, e.g. for a profiler, that allocates only what the step
+needs:
+
+  python -m combine_ep_dispatch_gb300.run_step --workload dsv3 --iters 3
+
+Combine reads the dispatched rows (identity experts; for the FP8 workload a
+bf16 dispatch of the same routing provides them).
+"""
+from __future__ import annotations
+
+import argparse
+
+import numpy as np
+import torch
+
+from . import _lib
+from .inputs import CONFIGS, make_inputs
+from .pipeline import DispatchCombine
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--workload", default="dsv3", choices=sorted(CONFIGS))
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--seed", type=int, default=0)
+    args = ap.parse_args(argv)
+
+    inp = make_inputs(args.workload, seed=args.seed)
+    cfg = inp["cfg"]
+    dev = torch.device("cuda")
+    x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+    idx = torch.from_numpy(inp["topk_idx"]).to(dev)
+    w = torch.from_numpy(inp["topk_w"]).to(dev)
+    quant = _lib.EP_QUANT_FP8_E4M3_B128 if cfg.quant == "fp8" else _lib.EP_QUANT_BF16
+    probe = DispatchCombine(cfg.T, 8, cfg.E, cfg.k, cfg.W, capacity_rows=0, device=dev)
+    probe.layout(idx)
+    R = int(probe.rank_offset[cfg.W].item())
+    dc = DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, capacity_rows=R, quant=quant,
+                         device=dev)
+    ident = dc if quant == _lib.EP_QUANT_BF16 else DispatchCombine(
+        cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, capacity_rows=R, device=dev)
+    for _ in range(args.iters):
+        dc.layout(idx)
+        dc.dispatch(x, idx, w)
+        if ident is not dc:
+            ident.layout(idx)
+            ident.dispatch(x, idx, w)
+        dc.combine(ident.recv_x)
+    torch.cuda.synchronize()
+    print(f"{args.workload}: T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} W={cfg.W} R={R} "
+          f"iters={args.iters} status={int(dc.status.item())}")
+
+
+if __name__ == "__main__":
+    main()

@@ -23,6 +23,7 @@ EP_ERR_WORKSPACE = 5
 
 EP_STATUS_BAD_EXPERT = 1
 EP_STATUS_CAPACITY = 2
+EP_STATUS_TIMEOUT = 4
 
 EP_QUANT_BF16 = 0
 EP_QUANT_FP8_E4M3_B128 = 1

@@ -202,6 +202,135 @@ __global__ void __launch_bounds__(kDThreads)
   if (cap_err && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_CAPACITY);
 }
 
+// bf16 payload through the bulk-copy (TMA) engine.  Each warp runs its own
+// pipeline over its tokens with kTmaStages private row buffers in shared
+// memory: lane 0 brings the token's row in with one bulk copy (global ->
+// shared) and, once it has landed, sends it out with one bulk copy (shared ->
+// global) per destination row; a buffer is refilled with a later token once
+// the copies out of it have finished reading it.  A row copy is then one
+// instruction instead of H/256 warp-wide 16-byte stores, which keeps the
+// load/store pipe free; the other lanes fetch the next token's slots early and
+// carry the metadata.
+constexpr int kTmaStages = 3;
+constexpr int kTmaBarBytes = 1024;         // barrier area ahead of the row buffers
+constexpr int kTmaSmemBudget = 200 * 1024; // row buffers per CTA (one CTA per SM)
+constexpr uint32_t kTmaMinRowBytes = 1024;  // smaller rows: 16-byte stores from registers
+
+__device__ __forceinline__ int load_slot(const int32_t* __restrict__ slot, int64_t t, int W,
+                                         int lane, int64_t T) {
+  return (t < T && lane < W) ? __ldg(slot + t * W + lane) : -1;
+}
+
+__global__ void __launch_bounds__(256, 1)
+    dispatch_bf16_tma_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
+                             const float* __restrict__ topk_w, int64_t T, uint32_t row_bytes,
+                             uint32_t stage_bytes, int k, int W, const int32_t* __restrict__ slot,
+                             int64_t cap, uint8_t* __restrict__ recv_x,
+                             int32_t* __restrict__ recv_topk_idx, float* __restrict__ recv_topk_w,
+                             int32_t* __restrict__ recv_src, int32_t* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta_warps = blockDim.x >> 5;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem) + warp * kTmaStages;
+  uint8_t* buf = smem + kTmaBarBytes + (size_t)warp * kTmaStages * stage_bytes;
+  if (lane == 0) {
+    for (int s = 0; s < kTmaStages; ++s) mbar_init(&full[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  pdl_wait();
+
+  const int64_t gw = (int64_t)blockIdx.x * cta_warps + warp;
+  const int64_t NW = (int64_t)gridDim.x * cta_warps;
+  const int64_t n = gw < T ? (T - 1 - gw) / NW + 1 : 0;  // tokens gw, gw+NW, ...
+  int64_t issued = 0;                                      // tokens whose row load was issued
+  if (lane == 0) {
+    for (; issued < n && issued < kTmaStages; ++issued) {
+      mbar_arrive_expect_tx(&full[issued], row_bytes);
+      bulk_load(buf + issued * stage_bytes, x + (gw + issued * NW) * row_bytes, row_bytes,
+                &full[issued]);
+    }
+  }
+  const bool meta_lanes = 2 * k + 1 <= 32;
+  bool cap_err = false, timed_out = false;
+  int s_cur = load_slot(slot, gw, W, lane, T);
+  int64_t j = 0;
+  for (; j < n; ++j) {
+    const int64_t t = gw + j * NW;
+    const int st = (int)(j % kTmaStages);
+    const uint32_t parity = (uint32_t)((j / kTmaStages) & 1);
+    // one metadata word per lane: k ids, k weights, the source index
+    int32_t mv = 0;
+    if (meta_lanes && lane <= 2 * k) {
+      if (lane < k)
+        mv = __ldg(topk_idx + t * k + lane);
+      else if (lane < 2 * k)
+        mv = __float_as_int(__ldg(topk_w + t * k + (lane - k)));
+      else
+        mv = (int32_t)t;
+    }
+    const int s_next = load_slot(slot, t + NW, W, lane, T);
+    const bool keep = s_cur >= 0 && (int64_t)s_cur < cap;
+    cap_err |= __any_sync(kFull, s_cur >= 0 && (int64_t)s_cur >= cap);
+    const unsigned dmask = __ballot_sync(kFull, keep);
+    const int nd = __popc(dmask);
+    const int r = nth_set_bit_of_lane(dmask, lane);
+    const int my_row = __shfl_sync(kFull, s_cur, r & 31);
+
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_bounded(&full[st], parity);
+    if (!__shfl_sync(kFull, ok, 0)) {
+      timed_out = true;
+      break;
+    }
+    for (int q = 0; q < nd; ++q) {
+      const int row = __shfl_sync(kFull, my_row, q);
+      if (lane == 0) bulk_store(recv_x + (int64_t)row * row_bytes, buf + st * stage_bytes, row_bytes);
+    }
+    if (lane == 0) bulk_commit();
+    if (meta_lanes) {
+      for (int q = 0; q < nd; ++q) {
+        const int64_t row = __shfl_sync(kFull, my_row, q);
+        if (lane < k) {
+          if (recv_topk_idx) recv_topk_idx[row * k + lane] = mv;
+        } else if (lane < 2 * k) {
+          if (recv_topk_w) recv_topk_w[row * k + (lane - k)] = __int_as_float(mv);
+        } else if (lane == 2 * k) {
+          if (recv_src) recv_src[row] = mv;
+        }
+      }
+    } else {
+      Dests d;
+      d.nd = nd;
+      d.my_row = r >= 0 ? my_row : -1;
+      d.cap_err = false;
+      carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
+    }
+    // refill the previous token's buffer once the copies out of it have read it
+    if (lane == 0 && j >= 1 && issued < n) {
+      bulk_wait_read<1>();
+      const int sp = (int)((j - 1) % kTmaStages);
+      mbar_arrive_expect_tx(&full[sp], row_bytes);
+      bulk_load(buf + sp * stage_bytes, x + (gw + issued * NW) * row_bytes, row_bytes, &full[sp]);
+      ++issued;
+    }
+    issued = __shfl_sync(kFull, issued, 0);
+    s_cur = s_next;
+  }
+  if (lane == 0) {
+    // never leave with a bulk copy still using this CTA's shared memory
+    for (int64_t q = j; q < issued; ++q)
+      (void)mbar_wait_bounded(&full[q % kTmaStages], (uint32_t)((q / kTmaStages) & 1));
+    bulk_wait_all();
+  }
+  __syncwarp();
+  pdl_launch_dependents();
+  if (lane == 0 && status != nullptr) {
+    if (cap_err) atomicOr(status, EP_STATUS_CAPACITY);
+    if (timed_out) atomicOr(status, EP_STATUS_TIMEOUT);
+  }
+}
+
 template <typename K>
 int grid_for(K kernel, int64_t T, int threads) {
   int per_sm = 0;
@@ -224,6 +353,31 @@ cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float*
   if (T == 0) return cudaSuccess;
   const uint4* x4 = static_cast<const uint4*>(x);
   if (quant == EP_QUANT_BF16) {
+    const uint32_t row_bytes = (uint32_t)H * 2u;
+    const uint32_t stage_bytes = (row_bytes + 127u) & ~127u;
+    const int cta_warps_fit = (int)(kTmaSmemBudget / ((size_t)kTmaStages * stage_bytes));
+    if (row_bytes >= kTmaMinRowBytes && cta_warps_fit >= 1) {
+      const int cta_warps = cta_warps_fit < 8 ? cta_warps_fit : 8;
+      const size_t smem = kTmaBarBytes + (size_t)cta_warps * kTmaStages * stage_bytes;
+      static bool attr_set[128];
+      int dev = 0;
+      cudaGetDevice(&dev);
+      if (dev >= 0 && dev < 128 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(dispatch_bf16_tma_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kTmaBarBytes + kTmaSmemBudget);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+      }
+      const int64_t want = (T + cta_warps - 1) / cta_warps;
+      const int64_t sms = device_sm_count();
+      const int grid = (int)(want < sms ? want : sms);
+      return launch_pdl(dispatch_bf16_tma_kernel, dim3(grid < 1 ? 1 : grid), dim3(cta_warps * 32),
+                        smem, stream, static_cast<const uint8_t*>(x), topk_idx, topk_w, T,
+                        row_bytes, stage_bytes, k, W, slot, capacity_rows,
+                        static_cast<uint8_t*>(recv_x), recv_topk_idx, recv_topk_w, recv_src,
+                        status);
+    }
     const int n16 = H / 8;
     if (n16 % (32 * 7) == 0) {
       auto kern = dispatch_bf16_kernel<7>;

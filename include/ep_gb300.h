@@ -59,7 +59,8 @@ enum {
 /* Device-side status bits, OR-ed into *status. */
 enum {
   EP_STATUS_BAD_EXPERT = 1, /* an expert id outside [0, E): the entry was ignored */
-  EP_STATUS_CAPACITY = 2    /* a receive row >= capacity_rows: it was not read / written */
+  EP_STATUS_CAPACITY = 2,   /* a receive row >= capacity_rows: it was not read / written */
+  EP_STATUS_TIMEOUT = 4     /* a bounded on-chip wait gave up (about 1 s); outputs incomplete */
 };
 
 /* Dispatch payload formats. */

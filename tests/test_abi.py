@@ -39,6 +39,7 @@ def test_enum_values_match_header():
     txt = open(HEADER).read()
     for name in ("EP_OK", "EP_ERR_INVALID_ARG", "EP_ERR_MISALIGNED", "EP_ERR_UNSUPPORTED",
                  "EP_ERR_CUDA", "EP_ERR_WORKSPACE", "EP_STATUS_BAD_EXPERT", "EP_STATUS_CAPACITY",
+                 "EP_STATUS_TIMEOUT",
                  "EP_QUANT_BF16", "EP_QUANT_FP8_E4M3_B128"):
         m = re.search(rf"\b{name}\s*=\s*(\d+)", txt)
         assert m and int(m.group(1)) == getattr(_lib, name), name

@@ -48,18 +48,26 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build_library(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
+def build_library(force: bool = False, verbose: bool = False, defines=(), out: str | None = None,
+                  build_dir: str | None = None) -> str:
+    """Compile and link the library.  ``defines`` (e.g. ["EP_TMA_STAGES=4"])
+    override compile-time tuning constants; with ``out`` the result goes to that
+    path instead of the package's libep_gb300.so."""
+    if not force and not defines and out is None and up_to_date():
         return LIB
+    lib_path = out or LIB
+    build = build_dir or BUILD
     nvcc = os.path.join(cuda_home(), "bin", "nvcc")
     if not os.path.exists(nvcc):
         nvcc = "nvcc"
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build, exist_ok=True)
     srcs = _sources()
+    dflags = [f"-D{d}" for d in defines]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
+        obj = os.path.join(build, os.path.basename(src) + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *dflags, "-I", os.path.join(ROOT, "include"), "-c", src,
+               "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -67,21 +75,21 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         results = list(ex.map(compile_one, srcs))
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+    with open(os.path.join(build, "ptxas.log"), "w") as f:
         for (obj, log) in results:
             f.write(f"== {os.path.basename(obj)}\n{log}\n")
     if verbose:
         for _, log in results:
             print(log)
     lib64 = os.path.join(cuda_home(), "lib64")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for o, _ in results],
            "-Xlinker", f"-rpath,{lib64}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -5,6 +5,9 @@
 namespace ep {
 namespace {
 
+#ifndef EP_COMBINE_U
+#define EP_COMBINE_U 2
+#endif
 constexpr int kCThreads = 256;
 
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
@@ -90,12 +93,164 @@ __global__ void __launch_bounds__(kCThreads)
   if (cap_err && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_CAPACITY);
 }
 
+// Combine through the bulk-copy (TMA) engine, for W <= 8.  The work unit of a
+// warp is (token, column chunk of kCChunk bytes).  Lane 0 loads the chunk of
+// each of the token's rows into a private shared-memory stage with one bulk
+// copy per row, kCStages units ahead of the one being summed; the warp then
+// sums the stage's rows in ascending rank order (each lane 16-byte pieces of
+// the chunk) and stores the bf16 result.  Deep look-ahead with few threads
+// keeps enough bytes in flight to stream the rows at full bandwidth.
+#ifndef EP_COMBINE_STAGES
+#define EP_COMBINE_STAGES 3
+#endif
+#ifndef EP_COMBINE_CHUNK_BYTES
+#define EP_COMBINE_CHUNK_BYTES 2048
+#endif
+#ifndef EP_COMBINE_SMEM_BUDGET
+#define EP_COMBINE_SMEM_BUDGET (200 * 1024)
+#endif
+#ifndef EP_COMBINE_MAX_WARPS
+#define EP_COMBINE_MAX_WARPS 8
+#endif
+constexpr int kCStages = EP_COMBINE_STAGES;
+constexpr uint32_t kCChunk = EP_COMBINE_CHUNK_BYTES;
+constexpr int kCMaxRows = 8;
+constexpr uint32_t kCStageBytes = kCMaxRows * kCChunk;
+constexpr int kCBarBytes = 1024;
+constexpr int kCSmemBudget = EP_COMBINE_SMEM_BUDGET;
+constexpr int kCMaxWarps = EP_COMBINE_MAX_WARPS;
+
+__global__ void __launch_bounds__(kCMaxWarps * 32, 1)
+    combine_tma_kernel(const uint8_t* __restrict__ y, const int32_t* __restrict__ slot, int64_t T,
+                       uint32_t row_bytes, int W, int64_t cap, uint8_t* __restrict__ out,
+                       int32_t* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta_warps = blockDim.x >> 5;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem) + warp * kCStages;  // < 256 bytes
+  int* nd_ring = reinterpret_cast<int*>(smem + 256) + warp * kCStages;    // < 128 bytes
+  int* rows = reinterpret_cast<int*>(smem + 512) + warp * kCMaxRows;       // < 256 bytes
+  uint8_t* buf = smem + kCBarBytes + (size_t)warp * kCStages * kCStageBytes;
+  if (lane == 0) {
+    for (int s = 0; s < kCStages; ++s) mbar_init(&full[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  pdl_wait();
+
+  const int64_t gw = (int64_t)blockIdx.x * cta_warps + warp;
+  const int64_t NW = (int64_t)gridDim.x * cta_warps;
+  const int64_t n_tok = gw < T ? (T - 1 - gw) / NW + 1 : 0;
+  const int nch = (int)((row_bytes + kCChunk - 1) / kCChunk);
+  const int64_t n_units = n_tok * nch;
+
+  // issue side (lane 0 only): the next unit to load and its token's rows
+  int64_t issued = 0;
+  int nd_issue = 0;
+  bool cap_err = false, timed_out = false;
+  auto issue_next = [&]() {
+    const int64_t jt = issued / nch;
+    const int c = (int)(issued - jt * nch);
+    if (c == 0) {
+      const int64_t t = gw + jt * NW;
+      nd_issue = 0;
+#pragma unroll
+      for (int r = 0; r < kCMaxRows; ++r) {
+        const int s = r < W ? __ldg(slot + t * W + r) : -1;
+        if (s >= 0 && (int64_t)s < cap) rows[nd_issue++] = s;
+        cap_err |= s >= 0 && (int64_t)s >= cap;
+      }
+    }
+    const int st = (int)(issued % kCStages);
+    const uint32_t off = (uint32_t)c * kCChunk;
+    const uint32_t bytes = row_bytes - off < kCChunk ? row_bytes - off : kCChunk;
+    nd_ring[st] = nd_issue;
+    mbar_arrive_expect_tx(&full[st], (uint32_t)nd_issue * bytes);
+    for (int q = 0; q < nd_issue; ++q)
+      bulk_load(buf + st * kCStageBytes + q * kCChunk, y + (int64_t)rows[q] * row_bytes + off,
+                bytes, &full[st]);
+    ++issued;
+  };
+  if (lane == 0)
+    while (issued < n_units && issued < kCStages) issue_next();
+
+  int64_t u = 0;
+  for (; u < n_units; ++u) {
+    const int st = (int)(u % kCStages);
+    const uint32_t parity = (uint32_t)((u / kCStages) & 1);
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_bounded(&full[st], parity);
+    if (!__shfl_sync(kFull, ok, 0)) {
+      timed_out = true;
+      break;
+    }
+    const int nd = nd_ring[st];
+    const int64_t jt = u / nch;
+    const int c = (int)(u - jt * nch);
+    const int64_t t = gw + jt * NW;
+    const uint32_t off = (uint32_t)c * kCChunk;
+    const uint32_t bytes = row_bytes - off < kCChunk ? row_bytes - off : kCChunk;
+    const uint8_t* sb = buf + st * kCStageBytes;
+    uint4* dst = reinterpret_cast<uint4*>(out + t * row_bytes + off);
+#pragma unroll 4
+    for (uint32_t p = lane; p < bytes / 16; p += 32) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      uint4 v[kCMaxRows];
+#pragma unroll
+      for (int q = 0; q < kCMaxRows; ++q)
+        if (q < nd) v[q] = *reinterpret_cast<const uint4*>(sb + q * kCChunk + p * 16);
+#pragma unroll
+      for (int q = 0; q < kCMaxRows; ++q)
+        if (q < nd) add_bf16x8(acc, v[q]);
+      st_v4(dst + p, make_uint4(bf16x2_rn(acc[0], acc[1]), bf16x2_rn(acc[2], acc[3]),
+                                bf16x2_rn(acc[4], acc[5]), bf16x2_rn(acc[6], acc[7])));
+    }
+    __syncwarp();  // every lane has read the stage: it may be refilled
+    if (lane == 0 && issued < n_units) issue_next();
+  }
+  if (lane == 0) {
+    // loads still landing in shared memory must finish before the CTA exits
+    for (int64_t q = u; q < issued; ++q)
+      (void)mbar_wait_bounded(&full[q % kCStages], (uint32_t)((q / kCStages) & 1));
+  }
+  __syncwarp();
+  pdl_launch_dependents();
+  if (lane == 0 && status != nullptr) {
+    if (cap_err) atomicOr(status, EP_STATUS_CAPACITY);
+    if (timed_out) atomicOr(status, EP_STATUS_TIMEOUT);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H, int W,
                            int64_t capacity_rows, void* out, int32_t* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  auto kern = combine_kernel<2>;
+  const uint32_t row_bytes = (uint32_t)H * 2u;
+  const int cta_warps_fit = (int)(kCSmemBudget / ((size_t)kCStages * kCStageBytes));
+  if (!EP_FORCE_LSU && W <= kCMaxRows && row_bytes >= 1024 && cta_warps_fit >= 1) {
+    const int cta_warps = cta_warps_fit < kCMaxWarps ? cta_warps_fit : kCMaxWarps;
+    const size_t smem = kCBarBytes + (size_t)cta_warps * kCStages * kCStageBytes;
+    static bool attr_set[128];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 128 && !attr_set[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(combine_tma_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kCBarBytes + kCSmemBudget);
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
+    const int64_t want = (T + cta_warps - 1) / cta_warps;
+    const int64_t sms = device_sm_count();
+    const int grid = (int)(want < sms ? want : sms);
+    return launch_pdl(combine_tma_kernel, dim3(grid < 1 ? 1 : grid), dim3(cta_warps * 32), smem,
+                      stream, static_cast<const uint8_t*>(y), slot, T, row_bytes, W,
+                      capacity_rows, static_cast<uint8_t*>(out), status);
+  }
+  auto kern = combine_kernel<EP_COMBINE_U>;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCThreads, 0) != cudaSuccess ||
       per_sm < 1)

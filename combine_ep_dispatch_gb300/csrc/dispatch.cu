@@ -211,9 +211,23 @@ __global__ void __launch_bounds__(kDThreads)
 // instruction instead of H/256 warp-wide 16-byte stores, which keeps the
 // load/store pipe free; the other lanes fetch the next token's slots early and
 // carry the metadata.
-constexpr int kTmaStages = 3;
-constexpr int kTmaBarBytes = 1024;         // barrier area ahead of the row buffers
-constexpr int kTmaSmemBudget = 200 * 1024; // row buffers per CTA (one CTA per SM)
+#ifndef EP_TMA_STAGES
+#define EP_TMA_STAGES 3
+#endif
+#ifndef EP_TMA_SMEM_BUDGET
+#define EP_TMA_SMEM_BUDGET (200 * 1024)
+#endif
+#ifndef EP_TMA_MAX_WARPS
+#define EP_TMA_MAX_WARPS 8
+#endif
+#ifndef EP_TMA_CTAS_PER_SM
+#define EP_TMA_CTAS_PER_SM 1
+#endif
+constexpr int kTmaStages = EP_TMA_STAGES;            // row buffers per warp
+constexpr int kTmaBarBytes = 1024;                   // barrier area ahead of the row buffers
+constexpr int kTmaSmemBudget = EP_TMA_SMEM_BUDGET;   // row buffers per CTA
+constexpr int kTmaMaxWarps = EP_TMA_MAX_WARPS;
+constexpr int kTmaCtasPerSm = EP_TMA_CTAS_PER_SM;
 constexpr uint32_t kTmaMinRowBytes = 1024;  // smaller rows: 16-byte stores from registers
 
 __device__ __forceinline__ int load_slot(const int32_t* __restrict__ slot, int64_t t, int W,
@@ -221,7 +235,7 @@ __device__ __forceinline__ int load_slot(const int32_t* __restrict__ slot, int64
   return (t < T && lane < W) ? __ldg(slot + t * W + lane) : -1;
 }
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kTmaMaxWarps * 32, 1)
     dispatch_bf16_tma_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
                              const float* __restrict__ topk_w, int64_t T, uint32_t row_bytes,
                              uint32_t stage_bytes, int k, int W, const int32_t* __restrict__ slot,
@@ -356,8 +370,8 @@ cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float*
     const uint32_t row_bytes = (uint32_t)H * 2u;
     const uint32_t stage_bytes = (row_bytes + 127u) & ~127u;
     const int cta_warps_fit = (int)(kTmaSmemBudget / ((size_t)kTmaStages * stage_bytes));
-    if (row_bytes >= kTmaMinRowBytes && cta_warps_fit >= 1) {
-      const int cta_warps = cta_warps_fit < 8 ? cta_warps_fit : 8;
+    if (!EP_FORCE_LSU && row_bytes >= kTmaMinRowBytes && cta_warps_fit >= 1) {
+      const int cta_warps = cta_warps_fit < kTmaMaxWarps ? cta_warps_fit : kTmaMaxWarps;
       const size_t smem = kTmaBarBytes + (size_t)cta_warps * kTmaStages * stage_bytes;
       static bool attr_set[128];
       int dev = 0;
@@ -370,7 +384,7 @@ cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float*
         attr_set[dev] = true;
       }
       const int64_t want = (T + cta_warps - 1) / cta_warps;
-      const int64_t sms = device_sm_count();
+      const int64_t sms = (int64_t)device_sm_count() * kTmaCtasPerSm;
       const int grid = (int)(want < sms ? want : sms);
       return launch_pdl(dispatch_bf16_tma_kernel, dim3(grid < 1 ? 1 : grid), dim3(cta_warps * 32),
                         smem, stream, static_cast<const uint8_t*>(x), topk_idx, topk_w, T,

@@ -10,6 +10,13 @@ namespace ep {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// Build-time switch used when comparing kernel variants: 1 routes the bf16
+// copies through the register (16-byte load/store) kernels even where the
+// bulk-copy kernels apply.
+#ifndef EP_FORCE_LSU
+#define EP_FORCE_LSU 0
+#endif
+
 // ------------------------------------------------------------ dependent launch
 // Every kernel of the library is launched with programmatic stream
 // serialization and begins with pdl_wait(): the grid may become resident while

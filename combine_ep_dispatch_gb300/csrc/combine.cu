@@ -93,134 +93,171 @@ __global__ void __launch_bounds__(kCThreads)
   if (cap_err && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_CAPACITY);
 }
 
-// Combine through the bulk-copy (TMA) engine, for W <= 8.  The work unit of a
-// warp is (token, column chunk of kCChunk bytes).  Lane 0 loads the chunk of
-// each of the token's rows into a private shared-memory stage with one bulk
-// copy per row, kCStages units ahead of the one being summed; the warp then
-// sums the stage's rows in ascending rank order (each lane 16-byte pieces of
-// the chunk) and stores the bf16 result.  Deep look-ahead with few threads
-// keeps enough bytes in flight to stream the rows at full bandwidth.
-#ifndef EP_COMBINE_STAGES
-#define EP_COMBINE_STAGES 3
+// Combine through the bulk-copy (TMA) engine.  A ring of kCStages stages in
+// shared memory holds one row chunk each (a whole row for H <= 8192).  Warp 0
+// produces: for each of the CTA's tokens and each chunk, lane q loads the
+// chunk of the token's q-th destination row (ascending rank) into the next
+// stage with one bulk copy, once that stage is free, and writes the stage's
+// descriptor (token, chunk, last-row flag).  Warps 1..kCWarps consume the
+// stages strictly in ring order: each thread adds its 16-byte pieces of the
+// stage to fp32 running sums in registers and, at the token's last row,
+// rounds them to bf16 and stores them.  So the sum runs in ascending rank
+// order, a stage is handed back as soon as it has been added, and no token has
+// to sit in shared memory whole: the ring only holds bytes in flight.
+// Whole-row copies and several issuing lanes keep the copy engine streaming.
+#ifndef EP_COMBINE_TMA
+#define EP_COMBINE_TMA 1
 #endif
-#ifndef EP_COMBINE_CHUNK_BYTES
-#define EP_COMBINE_CHUNK_BYTES 2048
+#ifndef EP_COMBINE_WARPS
+#define EP_COMBINE_WARPS 8
+#endif
+#ifndef EP_COMBINE_STAGE
+#define EP_COMBINE_STAGE 16384
 #endif
 #ifndef EP_COMBINE_SMEM_BUDGET
-#define EP_COMBINE_SMEM_BUDGET (200 * 1024)
+#define EP_COMBINE_SMEM_BUDGET (208 * 1024)
 #endif
-#ifndef EP_COMBINE_MAX_WARPS
-#define EP_COMBINE_MAX_WARPS 8
-#endif
-constexpr int kCStages = EP_COMBINE_STAGES;
-constexpr uint32_t kCChunk = EP_COMBINE_CHUNK_BYTES;
-constexpr int kCMaxRows = 8;
-constexpr uint32_t kCStageBytes = kCMaxRows * kCChunk;
-constexpr int kCBarBytes = 1024;
-constexpr int kCSmemBudget = EP_COMBINE_SMEM_BUDGET;
-constexpr int kCMaxWarps = EP_COMBINE_MAX_WARPS;
+constexpr int kCWarps = EP_COMBINE_WARPS;                        // consumer warps
+constexpr uint32_t kCStage = EP_COMBINE_STAGE;                   // bytes per stage
+constexpr int kCStages = EP_COMBINE_SMEM_BUDGET / kCStage;       // ring length
+constexpr int kCPieces = kCStage / (16 * 32 * kCWarps);          // pieces per thread per stage
+constexpr int kCHead = 1024;                                     // barriers + descriptors
+constexpr uint32_t kDescLast = 1u, kDescNone = 2u, kDescDone = 4u;
+static_assert(kCStage % (16 * 32 * kCWarps) == 0, "stage must split evenly over consumers");
+static_assert(kCStages * (16 + 16) <= kCHead, "header too small");
+static_assert(kCStages <= 32, "one producer lane per stage of a token at most");
 
-__global__ void __launch_bounds__(kCMaxWarps * 32, 1)
+__global__ void __launch_bounds__((kCWarps + 1) * 32, 1)
     combine_tma_kernel(const uint8_t* __restrict__ y, const int32_t* __restrict__ slot, int64_t T,
-                       uint32_t row_bytes, int W, int64_t cap, uint8_t* __restrict__ out,
-                       int32_t* __restrict__ status) {
+                       uint32_t row_bytes, uint32_t chunk_bytes, int W, int64_t cap,
+                       uint8_t* __restrict__ out, int32_t* __restrict__ status) {
   extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kCStages;
+  int64_t* desc_tok = reinterpret_cast<int64_t*>(empty + kCStages);
+  uint32_t* desc_info = reinterpret_cast<uint32_t*>(desc_tok + kCStages);  // chunk << 8 | flags
+  uint8_t* ring = smem + kCHead;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cta_warps = blockDim.x >> 5;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem) + warp * kCStages;  // < 256 bytes
-  int* nd_ring = reinterpret_cast<int*>(smem + 256) + warp * kCStages;    // < 128 bytes
-  int* rows = reinterpret_cast<int*>(smem + 512) + warp * kCMaxRows;       // < 256 bytes
-  uint8_t* buf = smem + kCBarBytes + (size_t)warp * kCStages * kCStageBytes;
-  if (lane == 0) {
-    for (int s = 0; s < kCStages; ++s) mbar_init(&full[s], 1);
-    fence_barrier_init();
+  if (threadIdx.x < kCStages) {
+    mbar_init(&full[threadIdx.x], 1);
+    mbar_init(&empty[threadIdx.x], kCWarps);
   }
-  __syncwarp();
+  fence_barrier_init();
+  __syncthreads();
   pdl_wait();
 
-  const int64_t gw = (int64_t)blockIdx.x * cta_warps + warp;
-  const int64_t NW = (int64_t)gridDim.x * cta_warps;
-  const int64_t n_tok = gw < T ? (T - 1 - gw) / NW + 1 : 0;
-  const int nch = (int)((row_bytes + kCChunk - 1) / kCChunk);
-  const int64_t n_units = n_tok * nch;
+  const int64_t G = gridDim.x;
+  const int64_t n_tok = (int64_t)blockIdx.x < T ? (T - 1 - blockIdx.x) / G + 1 : 0;
+  const int nch = (int)((row_bytes + chunk_bytes - 1) / chunk_bytes);
+  bool timed_out = false;
 
-  // issue side (lane 0 only): the next unit to load and its token's rows
-  int64_t issued = 0;
-  int nd_issue = 0;
-  bool cap_err = false, timed_out = false;
-  auto issue_next = [&]() {
-    const int64_t jt = issued / nch;
-    const int c = (int)(issued - jt * nch);
-    if (c == 0) {
-      const int64_t t = gw + jt * NW;
-      nd_issue = 0;
-#pragma unroll
-      for (int r = 0; r < kCMaxRows; ++r) {
-        const int s = r < W ? __ldg(slot + t * W + r) : -1;
-        if (s >= 0 && (int64_t)s < cap) rows[nd_issue++] = s;
-        cap_err |= s >= 0 && (int64_t)s >= cap;
+  if (warp == 0) {
+    // ---------------- producer
+    bool cap_err = false;
+    int64_t g = 0;  // stages issued
+    int s_next = (n_tok > 0 && lane < W) ? __ldg(slot + (int64_t)blockIdx.x * W + lane) : -1;
+    for (int64_t i = 0; i < n_tok && !timed_out; ++i) {
+      const int64_t t = blockIdx.x + i * G;
+      const int s_cur = s_next;
+      s_next = (i + 1 < n_tok && lane < W) ? __ldg(slot + (t + G) * W + lane) : -1;
+      const bool keep = s_cur >= 0 && (int64_t)s_cur < cap;
+      cap_err |= __any_sync(kFull, s_cur >= 0 && (int64_t)s_cur >= cap);
+      const unsigned dmask = __ballot_sync(kFull, keep);
+      const int nd = __popc(dmask);
+      const int r = nth_set_bit_of_lane(dmask, lane);
+      const int my_row = __shfl_sync(kFull, s_cur, r & 31);  // lane q: row of the q-th destination
+      const int need = nd > 0 ? nd : 1;
+      for (int c = 0; c < nch && !timed_out; ++c) {
+        const uint32_t off = (uint32_t)c * chunk_bytes;
+        const uint32_t bytes = row_bytes - off < chunk_bytes ? row_bytes - off : chunk_bytes;
+        bool ok = true;
+        if (lane < need) {
+          const int64_t gq = g + lane;
+          const int st = (int)(gq % kCStages);
+          if (gq >= kCStages)
+            ok = mbar_wait_bounded(&empty[st], (uint32_t)(((gq / kCStages) - 1) & 1));
+          if (ok) {
+            desc_tok[st] = t;
+            desc_info[st] = ((uint32_t)c << 8) | (lane == need - 1 ? kDescLast : 0u) |
+                            (nd == 0 ? kDescNone : 0u);
+            if (nd > 0) {
+              mbar_arrive_expect_tx(&full[st], bytes);
+              bulk_load(ring + (size_t)st * kCStage, y + (int64_t)my_row * row_bytes + off, bytes,
+                        &full[st]);
+            } else {
+              mbar_arrive_expect_tx(&full[st], 0);
+            }
+          }
+        }
+        timed_out = !__all_sync(kFull, ok);
+        g += need;
       }
     }
-    const int st = (int)(issued % kCStages);
-    const uint32_t off = (uint32_t)c * kCChunk;
-    const uint32_t bytes = row_bytes - off < kCChunk ? row_bytes - off : kCChunk;
-    nd_ring[st] = nd_issue;
-    mbar_arrive_expect_tx(&full[st], (uint32_t)nd_issue * bytes);
-    for (int q = 0; q < nd_issue; ++q)
-      bulk_load(buf + st * kCStageBytes + q * kCChunk, y + (int64_t)rows[q] * row_bytes + off,
-                bytes, &full[st]);
-    ++issued;
-  };
-  if (lane == 0)
-    while (issued < n_units && issued < kCStages) issue_next();
-
-  int64_t u = 0;
-  for (; u < n_units; ++u) {
-    const int st = (int)(u % kCStages);
-    const uint32_t parity = (uint32_t)((u / kCStages) & 1);
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait_bounded(&full[st], parity);
-    if (!__shfl_sync(kFull, ok, 0)) {
-      timed_out = true;
-      break;
+    if (!timed_out && lane == 0) {  // end marker
+      const int st = (int)(g % kCStages);
+      if (g < kCStages || mbar_wait_bounded(&empty[st], (uint32_t)(((g / kCStages) - 1) & 1))) {
+        desc_info[st] = kDescDone;
+        mbar_arrive_expect_tx(&full[st], 0);
+      } else {
+        timed_out = true;
+      }
+      ++g;
     }
-    const int nd = nd_ring[st];
-    const int64_t jt = u / nch;
-    const int c = (int)(u - jt * nch);
-    const int64_t t = gw + jt * NW;
-    const uint32_t off = (uint32_t)c * kCChunk;
-    const uint32_t bytes = row_bytes - off < kCChunk ? row_bytes - off : kCChunk;
-    const uint8_t* sb = buf + st * kCStageBytes;
-    uint4* dst = reinterpret_cast<uint4*>(out + t * row_bytes + off);
-#pragma unroll 4
-    for (uint32_t p = lane; p < bytes / 16; p += 32) {
-      float acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-      uint4 v[kCMaxRows];
-#pragma unroll
-      for (int q = 0; q < kCMaxRows; ++q)
-        if (q < nd) v[q] = *reinterpret_cast<const uint4*>(sb + q * kCChunk + p * 16);
-#pragma unroll
-      for (int q = 0; q < kCMaxRows; ++q)
-        if (q < nd) add_bf16x8(acc, v[q]);
-      st_v4(dst + p, make_uint4(bf16x2_rn(acc[0], acc[1]), bf16x2_rn(acc[2], acc[3]),
-                                bf16x2_rn(acc[4], acc[5]), bf16x2_rn(acc[6], acc[7])));
-    }
-    __syncwarp();  // every lane has read the stage: it may be refilled
-    if (lane == 0 && issued < n_units) issue_next();
-  }
-  if (lane == 0) {
-    // loads still landing in shared memory must finish before the CTA exits
-    for (int64_t q = u; q < issued; ++q)
+    // copies still landing in shared memory must finish before the CTA exits
+    for (int64_t q = (g > kCStages ? g - kCStages : 0) + lane; q < g; q += 32)
       (void)mbar_wait_bounded(&full[q % kCStages], (uint32_t)((q / kCStages) & 1));
+    if (lane == 0 && status != nullptr) {
+      if (cap_err) atomicOr(status, EP_STATUS_CAPACITY);
+      if (timed_out) atomicOr(status, EP_STATUS_TIMEOUT);
+    }
+  } else if (n_tok > 0) {
+    // ---------------- consumers
+    const int ct = threadIdx.x - 32;
+    float acc[kCPieces][8];
+#pragma unroll
+    for (int pc = 0; pc < kCPieces; ++pc)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[pc][e] = 0.0f;
+    for (int64_t g = 0;; ++g) {
+      const int st = (int)(g % kCStages);
+      if (!mbar_wait_bounded(&full[st], (uint32_t)((g / kCStages) & 1))) {
+        timed_out = true;
+        break;
+      }
+      const uint32_t info = desc_info[st];
+      if (info & kDescDone) break;
+      const int64_t t = desc_tok[st];
+      const uint32_t off = (info >> 8) * chunk_bytes;
+      const uint32_t bytes = row_bytes - off < chunk_bytes ? row_bytes - off : chunk_bytes;
+      const uint8_t* sb = ring + (size_t)st * kCStage;
+      if (!(info & kDescNone)) {
+#pragma unroll
+        for (int pc = 0; pc < kCPieces; ++pc) {
+          const uint32_t p = (uint32_t)(pc * 32 * kCWarps + ct);
+          if (p * 16 < bytes) add_bf16x8(acc[pc], *reinterpret_cast<const uint4*>(sb + p * 16));
+        }
+      }
+      if (info & kDescLast) {
+        uint4* dst = reinterpret_cast<uint4*>(out + t * row_bytes + off);
+#pragma unroll
+        for (int pc = 0; pc < kCPieces; ++pc) {
+          const uint32_t p = (uint32_t)(pc * 32 * kCWarps + ct);
+          if (p * 16 < bytes)
+            st_v4(dst + p, make_uint4(bf16x2_rn(acc[pc][0], acc[pc][1]),
+                                      bf16x2_rn(acc[pc][2], acc[pc][3]),
+                                      bf16x2_rn(acc[pc][4], acc[pc][5]),
+                                      bf16x2_rn(acc[pc][6], acc[pc][7])));
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[pc][e] = 0.0f;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    if (timed_out && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_TIMEOUT);
   }
-  __syncwarp();
+  __syncthreads();
   pdl_launch_dependents();
-  if (lane == 0 && status != nullptr) {
-    if (cap_err) atomicOr(status, EP_STATUS_CAPACITY);
-    if (timed_out) atomicOr(status, EP_STATUS_TIMEOUT);
-  }
 }
 
 }  // namespace
@@ -229,25 +266,25 @@ cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H,
                            int64_t capacity_rows, void* out, int32_t* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const uint32_t row_bytes = (uint32_t)H * 2u;
-  const int cta_warps_fit = (int)(kCSmemBudget / ((size_t)kCStages * kCStageBytes));
-  if (!EP_FORCE_LSU && W <= kCMaxRows && row_bytes >= 1024 && cta_warps_fit >= 1) {
-    const int cta_warps = cta_warps_fit < kCMaxWarps ? cta_warps_fit : kCMaxWarps;
-    const size_t smem = kCBarBytes + (size_t)cta_warps * kCStages * kCStageBytes;
+  // (a token's rows must fit the ring at once: W <= kCStages)
+  if (EP_COMBINE_TMA && !EP_FORCE_LSU && row_bytes >= 1024 && W <= kCStages) {
+    // chunks of at most one stage, equal up to 16 bytes
+    const uint32_t nch = (row_bytes + kCStage - 1) / kCStage;
+    const uint32_t chunk = ((row_bytes / nch + 15u) & ~15u);
+    const size_t smem = kCHead + (size_t)kCStages * kCStage;
     static bool attr_set[128];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 128 && !attr_set[dev]) {
       cudaError_t e = cudaFuncSetAttribute(combine_tma_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kCBarBytes + kCSmemBudget);
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       attr_set[dev] = true;
     }
-    const int64_t want = (T + cta_warps - 1) / cta_warps;
     const int64_t sms = device_sm_count();
-    const int grid = (int)(want < sms ? want : sms);
-    return launch_pdl(combine_tma_kernel, dim3(grid < 1 ? 1 : grid), dim3(cta_warps * 32), smem,
-                      stream, static_cast<const uint8_t*>(y), slot, T, row_bytes, W,
+    const int grid = (int)(T < sms ? T : sms);
+    return launch_pdl(combine_tma_kernel, dim3(grid < 1 ? 1 : grid), dim3((kCWarps + 1) * 32),
+                      smem, stream, static_cast<const uint8_t*>(y), slot, T, row_bytes, chunk, W,
                       capacity_rows, static_cast<uint8_t*>(out), status);
   }
   auto kern = combine_kernel<EP_COMBINE_U>;

@@ -72,8 +72,36 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+#ifndef EP_MBAR_MODE
+#define EP_MBAR_MODE 0
+#endif
+// Test for completion of the barrier phase of the given parity.
+//  mode 0: mbarrier.try_wait (may suspend the thread for a while)
+//  mode 1: mbarrier.test_wait (never suspends)
+//  mode 2: mbarrier.try_wait with a 100 ns suspend-time hint
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
+#if EP_MBAR_MODE == 1
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+#elif EP_MBAR_MODE == 2
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(100)
+      : "memory");
+#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -81,6 +109,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
+#endif
   return ok != 0;
 }
 
@@ -93,13 +122,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Waits for the barrier phase of the given parity to complete, for at most
 // about one second; returns false when the limit ran out.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+#ifndef EP_WAIT_CHECK_EVERY
+#define EP_WAIT_CHECK_EVERY 512
+#endif
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (it % EP_WAIT_CHECK_EVERY == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
-  return true;
 }
 
 // global -> shared, completion counted in bytes on `bar`.

@@ -17,7 +17,7 @@
 namespace ep {
 namespace {
 
-constexpr int kLT = 256;  // tokens per CTA
+constexpr int kLT = 128;  // tokens per CTA, one per thread
 constexpr int kLWarps = kLT / 32;
 
 inline size_t a256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -42,10 +42,33 @@ LayoutWs carve(void* ws, int64_t T, int W) {
   return w;
 }
 
+// The k expert ids of a token row, loaded into registers before any is used:
+// VEC reads the row as int4 (k == KV, KV % 4 == 0, 16-byte aligned rows),
+// otherwise KV guarded scalar loads (k <= KV; missing entries read as -1).
+template <int KV, bool VEC>
+__device__ __forceinline__ void load_row(const int32_t* __restrict__ row, int k, bool live,
+                                         int (&e)[KV]) {
+  if constexpr (VEC) {
+#pragma unroll
+    for (int v = 0; v < KV / 4; ++v) {
+      const int4 q = live ? __ldg(reinterpret_cast<const int4*>(row) + v) : make_int4(-1, -1, -1, -1);
+      e[4 * v + 0] = q.x;
+      e[4 * v + 1] = q.y;
+      e[4 * v + 2] = q.z;
+      e[4 * v + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < KV; ++j) e[j] = (live && j < k) ? __ldg(row + j) : -1;
+  }
+}
+
 // Destination ranks of a token: rank = expert / experts-per-rank, one entry per
 // distinct rank ("perf(ep): optimize IntraNode dispatch kernel for MI350X",
 // Technical Details 1).  The bit set is the cached routing of that section: it
-// is computed here once and consumed by the scan.
+// is computed here once and consumed by the scan.  All k ids of a token are
+// loaded before any is used, so the chunk costs one memory round trip.
+template <int KV, bool VEC>
 __global__ void __launch_bounds__(kLT)
     layout_count_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k, int E, int W,
                         int Er, LayoutWs ws, int32_t* __restrict__ status) {
@@ -54,22 +77,31 @@ __global__ void __launch_bounds__(kLT)
   extern __shared__ int32_t s_hist[];  // [E]
   __shared__ int32_t s_warp_rank[kLWarps][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < E; e += kLT) s_hist[e] = 0;
-  __syncthreads();
-
   const int64_t t = (int64_t)blockIdx.x * kLT + tid;
   const bool live = t < T;
   const int32_t* row = topk_idx + (live ? t * k : 0);
   uint32_t m = 0;
   bool bad = false;
-  for (int j = 0; j < k; ++j) {
-    const int e = live ? __ldg(row + j) : -1;
-    const bool ok = (unsigned)e < (unsigned)E;
-    bad |= live && !ok;
-    if (ok) m |= 1u << (e / Er);
-    // lanes holding the same expert add once, with their number
-    const unsigned peers = __match_any_sync(kFull, ok ? e : -1);
-    if (ok && lane == __ffs(peers) - 1) atomicAdd(&s_hist[e], __popc(peers));
+  int ids[KV > 0 ? KV : 1];
+  if constexpr (KV > 0) load_row<KV, VEC>(row, k, live, ids);
+  for (int e = tid; e < E; e += kLT) s_hist[e] = 0;
+  __syncthreads();
+
+  const int kk = KV > 0 ? KV : k;
+#pragma unroll
+  for (int j = 0; j < kk; ++j) {
+    int e;
+    if constexpr (KV > 0)
+      e = ids[j];
+    else
+      e = live ? __ldg(row + j) : -1;
+    const bool in_row = KV == 0 || VEC || j < k;
+    const bool ok = in_row && (unsigned)e < (unsigned)E;
+    bad |= live && in_row && !ok;
+    if (ok) {
+      m |= 1u << (e / Er);
+      atomicAdd(&s_hist[e], 1);
+    }
   }
   if (live) ws.mask[t] = m;
 
@@ -84,6 +116,7 @@ __global__ void __launch_bounds__(kLT)
 
   if (tid < W) {
     int s = 0;
+#pragma unroll
     for (int w = 0; w < kLWarps; ++w) s += s_warp_rank[w][tid];
     ws.chunk_rank[(int64_t)blockIdx.x * W + tid] = s;
   }
@@ -94,17 +127,22 @@ __global__ void __launch_bounds__(kLT)
 // [rank_offset[r], rank_offset[r+1]) in ascending token order; the slot of
 // (t, r) is rank_offset[r] + (rows of r in earlier chunks) + (rows of r in
 // earlier warps of this chunk) + (rows of r in earlier lanes of this warp).
+// Per-expert totals are spread over the grid: CTA c sums experts c, c+C, ...
+// with one warp per expert and the chunks spread over the lanes.
 __global__ void __launch_bounds__(kLT)
     layout_scan_kernel(int64_t T, int E, int W, int64_t C, LayoutWs ws,
                        int32_t* __restrict__ num_tokens_per_expert,
                        int32_t* __restrict__ num_tokens_per_rank, int32_t* __restrict__ rank_offset,
                        int32_t* __restrict__ slot) {
   pdl_wait();
-  __shared__ int32_t s_total[32], s_before[32], s_base[32];
+  __shared__ int32_t s_total[32], s_before[32];
   __shared__ int32_t s_warp_cnt[kLWarps][32];
-  __shared__ int32_t s_warp_pre[kLWarps][32];
+  __shared__ int32_t s_base[kLWarps][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t c = blockIdx.x;
+  const int64_t t = c * kLT + tid;
+  const bool live = t < T;
+  const uint32_t m = live ? ws.mask[t] : 0u;
 
   for (int r = warp; r < W; r += kLWarps) {
     int tot = 0, bef = 0;
@@ -120,23 +158,6 @@ __global__ void __launch_bounds__(kLT)
       s_before[r] = bef;
     }
   }
-  __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int r = 0; r < W; ++r) {
-      s_base[r] = acc + s_before[r];
-      if (c == 0) {
-        rank_offset[r] = acc;
-        num_tokens_per_rank[r] = s_total[r];
-      }
-      acc += s_total[r];
-    }
-    if (c == 0) rank_offset[W] = acc;
-  }
-
-  const int64_t t = c * kLT + tid;
-  const bool live = t < T;
-  const uint32_t m = live ? ws.mask[t] : 0u;
   int cnt = 0;
   for (int r = 0; r < W; ++r) {
     const unsigned b = __ballot_sync(kFull, (m >> r) & 1u);
@@ -145,9 +166,17 @@ __global__ void __launch_bounds__(kLT)
   if (lane < W) s_warp_cnt[warp][lane] = cnt;
   __syncthreads();
   if (tid < W) {
-    int acc = s_base[tid];
+    int off = 0;
+    for (int r = 0; r < tid; ++r) off += s_total[r];
+    if (c == 0) {
+      rank_offset[tid] = off;
+      num_tokens_per_rank[tid] = s_total[tid];
+      if (tid == W - 1) rank_offset[W] = off + s_total[tid];
+    }
+    int acc = off + s_before[tid];
+#pragma unroll
     for (int w = 0; w < kLWarps; ++w) {
-      s_warp_pre[w][tid] = acc;
+      s_base[w][tid] = acc;
       acc += s_warp_cnt[w][tid];
     }
   }
@@ -155,16 +184,41 @@ __global__ void __launch_bounds__(kLT)
 
   const unsigned lt = lanemask_lt();
   int32_t* srow = slot + (live ? t * W : 0);
-  for (int r = 0; r < W; ++r) {
-    const unsigned in_r = (m >> r) & 1u;
-    const unsigned b = __ballot_sync(kFull, in_r);
-    if (live) srow[r] = in_r ? s_warp_pre[warp][r] + __popc(b & lt) : -1;
+  if ((W & 3) == 0 && (reinterpret_cast<uintptr_t>(slot) & 15) == 0) {
+    for (int r0 = 0; r0 < W; r0 += 4) {
+      int v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const unsigned in_r = (m >> (r0 + i)) & 1u;
+        const unsigned b = __ballot_sync(kFull, in_r);
+        v[i] = in_r ? s_base[warp][r0 + i] + __popc(b & lt) : -1;
+      }
+      if (live) reinterpret_cast<int4*>(srow)[r0 >> 2] = make_int4(v[0], v[1], v[2], v[3]);
+    }
+  } else {
+    for (int r = 0; r < W; ++r) {
+      const unsigned in_r = (m >> r) & 1u;
+      const unsigned b = __ballot_sync(kFull, in_r);
+      if (live) srow[r] = in_r ? s_base[warp][r] + __popc(b & lt) : -1;
+    }
   }
 
-  for (int64_t e = c * kLT + tid; e < E; e += (int64_t)gridDim.x * kLT) {
-    int s = 0;
-    for (int64_t q = 0; q < C; ++q) s += ws.chunk_exp[q * E + e];
-    num_tokens_per_expert[e] = s;
+  // per-expert totals over the chunks: with many chunks a warp per expert
+  // (chunks over the lanes), with few a thread per expert
+  if (C >= 16) {
+    for (int64_t e = c + (int64_t)warp * gridDim.x; e < E; e += (int64_t)kLWarps * gridDim.x) {
+      int s = 0;
+      for (int64_t q = lane; q < C; q += 32) s += ws.chunk_exp[q * E + e];
+      s = warp_sum(s);
+      if (lane == 0) num_tokens_per_expert[e] = s;
+    }
+  } else {
+    for (int64_t e = c * kLT + tid; e < E; e += (int64_t)gridDim.x * kLT) {
+      int s = 0;
+#pragma unroll 16
+      for (int64_t q = 0; q < C; ++q) s += ws.chunk_exp[q * E + e];
+      num_tokens_per_expert[e] = s;
+    }
   }
   pdl_launch_dependents();
 }
@@ -183,9 +237,21 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
                           cudaStream_t stream) {
   const int64_t C = num_chunks(T);
   const LayoutWs ws = carve(workspace, T, W);
-  cudaError_t err = launch_pdl(layout_count_kernel, dim3((unsigned)C), dim3(kLT),
-                               sizeof(int32_t) * (size_t)E, stream, topk_idx, T, k, E, W, E / W, ws,
-                               status);
+  const size_t smem = sizeof(int32_t) * (size_t)E;
+  const bool vec = (reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0;
+  cudaError_t err;
+  if (k == 8 && vec)
+    err = launch_pdl(layout_count_kernel<8, true>, dim3((unsigned)C), dim3(kLT), smem, stream,
+                     topk_idx, T, k, E, W, E / W, ws, status);
+  else if (k == 4 && vec)
+    err = launch_pdl(layout_count_kernel<4, true>, dim3((unsigned)C), dim3(kLT), smem, stream,
+                     topk_idx, T, k, E, W, E / W, ws, status);
+  else if (k <= 16)
+    err = launch_pdl(layout_count_kernel<16, false>, dim3((unsigned)C), dim3(kLT), smem, stream,
+                     topk_idx, T, k, E, W, E / W, ws, status);
+  else
+    err = launch_pdl(layout_count_kernel<0, false>, dim3((unsigned)C), dim3(kLT), smem, stream,
+                     topk_idx, T, k, E, W, E / W, ws, status);
   if (err != cudaSuccess) return err;
   return launch_pdl(layout_scan_kernel, dim3((unsigned)C), dim3(kLT), 0, stream, T, E, W, C, ws,
                     num_tokens_per_expert, num_tokens_per_rank, rank_offset, slot);

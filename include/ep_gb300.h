@@ -174,7 +174,7 @@ EP_API int ep_combine(const void* y, const int32_t* slot, int64_t T, int H, int 
  * exits.  Arguments, outputs and status bits are those of ep_dispatch_layout;
  * the call allocates nothing.
  *  - Returns EP_ERR_WORKSPACE when ep_layout_workspace_bytes(T, W, E) exceeds
- *    EP_LAYOUT_NOALLOC_SCRATCH_BYTES (up to 129024 tokens at W = 8, E = 256).
+ *    EP_LAYOUT_NOALLOC_SCRATCH_BYTES (up to 85504 tokens at W = 8, E = 256).
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) and caches it; make that first call before any
  *    stream capture on that device.

@@ -266,6 +266,28 @@ def test_dispatch_without_metadata_outputs():
     _check_dispatch(inp, lay, int(lay["rank_offset"][-1]), ep.EP_QUANT_BF16, with_meta=False)
 
 
+@pytest.mark.parametrize("k,E,W", [(20, 64, 8), (8, 256, 8), (3, 48, 6)])
+def test_layout_unaligned_and_wide_rows(k, E, W):
+    """topk_idx rows that are not 16-byte aligned, and k > 16 (scalar id loads)."""
+    rng = np.random.default_rng(k * 100 + E)
+    T = 777
+    idx = make_routing(rng, T, E, k)
+    flat = torch.zeros(T * k + 1, dtype=torch.int32, device="cuda")
+    flat[1:] = torch.from_numpy(idx.ravel()).cuda()
+    dev_idx = flat[1:].view(T, k)               # 4-byte aligned only
+    assert dev_idx.data_ptr() % 16 != 0
+    want = oracle.layout(idx, E, W)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    ne, nr = torch.empty(E, **i32), torch.empty(W, **i32)
+    off, slot = torch.empty(W + 1, **i32), torch.empty(T, W, **i32)
+    ws = torch.empty(ep.ep_layout_workspace_bytes(T, W, E), dtype=torch.uint8, device="cuda")
+    ep.ep_dispatch_layout(dev_idx, E, W, ne, nr, off, slot, ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(slot.cpu().numpy(), want["slot"])
+    np.testing.assert_array_equal(ne.cpu().numpy(), want["num_tokens_per_expert"])
+    np.testing.assert_array_equal(off.cpu().numpy(), want["rank_offset"])
+
+
 def test_deterministic_bytes():
     inp = make_inputs("decode", seed=44)
     cfg = inp["cfg"]

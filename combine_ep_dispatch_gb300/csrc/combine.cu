@@ -8,6 +8,7 @@ namespace {
 #ifndef EP_COMBINE_U
 #define EP_COMBINE_U 2
 #endif
+
 constexpr int kCThreads = 256;
 
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
@@ -40,9 +41,11 @@ __global__ void __launch_bounds__(kCThreads)
   const int64_t gwarp = ((int64_t)blockIdx.x * kCThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kCThreads) >> 5;
   bool cap_err = false;
+  int s_next = (gwarp < T && lane < W) ? __ldg(slot + gwarp * W + lane) : -1;
   for (int64_t t = gwarp; t < T; t += nwarps) {
-    int s = -1;
-    if (lane < W) s = __ldg(slot + t * W + lane);
+    int s = s_next;
+    s_next = (t + nwarps < T && lane < W) ? __ldg(slot + (t + nwarps) * W + lane) : -1;
+
     const bool keep = s >= 0 && (int64_t)s < cap;
     cap_err |= __any_sync(kFull, s >= 0 && (int64_t)s >= cap);
     const unsigned dmask = __ballot_sync(kFull, keep);
@@ -105,8 +108,15 @@ __global__ void __launch_bounds__(kCThreads)
 // order, a stage is handed back as soon as it has been added, and no token has
 // to sit in shared memory whole: the ring only holds bytes in flight.
 // Whole-row copies and several issuing lanes keep the copy engine streaming.
+// Used for T <= EP_COMBINE_TMA_MAX_T: measured on GB300 (H=7168, top-8, W=8)
+// it wins where the register kernel has too few warps to keep loads in flight
+// (T=256: 14 us against 23 us), ties at T=1024 and loses from T=2048 on
+// (T=4096: 71 us against 66 us), where the register kernel takes over.
 #ifndef EP_COMBINE_TMA
 #define EP_COMBINE_TMA 1
+#endif
+#ifndef EP_COMBINE_TMA_MAX_T
+#define EP_COMBINE_TMA_MAX_T 1024
 #endif
 #ifndef EP_COMBINE_WARPS
 #define EP_COMBINE_WARPS 8
@@ -267,7 +277,8 @@ cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H,
   if (T == 0) return cudaSuccess;
   const uint32_t row_bytes = (uint32_t)H * 2u;
   // (a token's rows must fit the ring at once: W <= kCStages)
-  if (EP_COMBINE_TMA && !EP_FORCE_LSU && row_bytes >= 1024 && W <= kCStages) {
+  if (EP_COMBINE_TMA && !EP_FORCE_LSU && row_bytes >= 1024 && W <= kCStages &&
+      T <= EP_COMBINE_TMA_MAX_T) {
     // chunks of at most one stage, equal up to 16 bytes
     const uint32_t nch = (row_bytes + kCStage - 1) / kCStage;
     const uint32_t chunk = ((row_bytes / nch + 15u) & ~15u);

@@ -123,11 +123,42 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// FP8 payload.  A 128-column block is 256 bytes of bf16 = 16 lanes x 16 bytes,
-// so a warp covers two blocks per round (lanes 0-15 and 16-31).  Per block:
-// amax over the block (a 16-lane max reduction), scale = amax / 448, codes =
-// e4m3(x / scale); both divisions are IEEE round-to-nearest.  The token is
-// quantised once and the codes and scales are stored to every destination.
+// One e4m3 code per value, of v / s with s > 0, exactly as if v / s were first
+// rounded to fp32 by IEEE division and that quotient then rounded to e4m3
+// (nearest, ties to even, saturating to +-448).  The e4m3 code is a
+// monotonic function of the quotient, so it is decided by a cheap quotient
+// q = v * (1/s) whenever the fp32 values 16 bit patterns below and above q
+// (in magnitude) map to the same code: |q - fl(v/s)| is only a few ulps
+// (rcp.approx has at most 1 ulp error, the product adds half an ulp), so the
+// correctly rounded quotient lies between them.  Otherwise (q near a rounding
+// boundary of e4m3, which happens for a few values in 10^5) the code comes from
+// the IEEE division itself.  `r` is 1/s from rcp.approx; r_ok is false when s
+// is subnormal or 1/s not finite, in which case every value takes the division.
+__device__ __forceinline__ uint32_t e4m3_of_quotient(float v, float s, float r, bool r_ok) {
+  if (r_ok) {
+    const float q = v * r;
+    const uint32_t m = __float_as_uint(q) & 0x7fffffffu;
+    const float lo = __uint_as_float(m > 16u ? m - 16u : 0u);
+    const float hi = __uint_as_float(m + 16u);
+    const uint32_t both = e4m3x2(lo, hi);
+    if ((both & 0xffu) == (both >> 8)) return (e4m3x2(q, 0.0f) & 0xffu);
+  }
+  return e4m3x2(__fdiv_rn(v, s), 0.0f) & 0xffu;
+}
+
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
+
+// FP8 payload.  A 128-column block is 256 bytes of bf16 = 8 lanes x 32 bytes,
+// so a warp covers four blocks per round (lanes 8b..8b+7 for block b).  Per
+// block: amax over the block (an 8-lane max reduction), scale = amax / 448
+// (IEEE division), codes of x / scale (e4m3_of_quotient).  A token row is
+// split into `nseg` segments of block quadruples, one warp per (token,
+// segment), so that small batches still fill the GPU; each segment is
+// quantised once and its codes and scales are stored to every destination.
 template <int U>
 __global__ void __launch_bounds__(kDThreads)
     dispatch_fp8_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ topk_idx,
@@ -135,46 +166,57 @@ __global__ void __launch_bounds__(kDThreads)
                         const int32_t* __restrict__ slot, int64_t cap, uint8_t* __restrict__ recv_x,
                         float* __restrict__ recv_scale, int32_t* __restrict__ recv_topk_idx,
                         float* __restrict__ recv_topk_w, int32_t* __restrict__ recv_src,
-                        int32_t* __restrict__ status) {
+                        int nseg, int32_t* __restrict__ status) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4, hl = lane & 15;
+  const int qb = lane >> 3, hl = lane & 7;  // block within the quad, lane within the block
   const int nb = H >> 7;
   const int n16 = H >> 3;
+  const int nquad = (nb + 3) >> 2;
+  const int per_seg = (nquad + nseg - 1) / nseg;
   const int64_t gwarp = ((int64_t)blockIdx.x * kDThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kDThreads) >> 5;
   bool cap_err = false;
-  for (int64_t t = gwarp; t < T; t += nwarps) {
+  for (int64_t u = gwarp; u < T * nseg; u += nwarps) {
+    const int64_t t = u / nseg;
+    const int seg = (int)(u - t * nseg);
     const Dests d = token_dests(slot, t, W, cap, lane);
-    cap_err |= d.cap_err;
-    carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
+    if (seg == 0) {
+      cap_err |= d.cap_err;
+      carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
+    }
     const uint4* src = x + t * n16;
-    for (int b0 = 0; b0 < nb; b0 += 2 * U) {
-      uint2 q[U];
+    const int q_end = (seg + 1) * per_seg < nquad ? (seg + 1) * per_seg : nquad;
+    for (int q0 = seg * per_seg; q0 < q_end; q0 += U) {
+      uint4 codes[U];
       float sc[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int b = b0 + 2 * u + half;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (b < nb) v = ld_stream_v4(src + b * 16 + hl);
-        const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(f[i]));
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(kFull, a, o));
-        const float s = __fdiv_rn(a, 448.0f);
-        sc[u] = s;
-        if (s == 0.0f) {
-          q[u] = make_uint2(0u, 0u);
-        } else {
-          uint32_t c[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            c[i] = e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
-          q[u] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+      for (int v = 0; v < U; ++v) {
+        const int b = (q0 + v) * 4 + qb;
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), c = make_uint4(0u, 0u, 0u, 0u);
+        if (q0 + v < q_end && b < nb) {
+          a = ld_stream_v4(src + b * 16 + hl * 2);
+          c = ld_stream_v4(src + b * 16 + hl * 2 + 1);
         }
+        const float f[16] = {bf16_lo(a.x), bf16_hi(a.x), bf16_lo(a.y), bf16_hi(a.y),
+                             bf16_lo(a.z), bf16_hi(a.z), bf16_lo(a.w), bf16_hi(a.w),
+                             bf16_lo(c.x), bf16_hi(c.x), bf16_lo(c.y), bf16_hi(c.y),
+                             bf16_lo(c.z), bf16_hi(c.z), bf16_lo(c.w), bf16_hi(c.w)};
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(f[i]));
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        const float s = __fdiv_rn(m, 448.0f);
+        sc[v] = s;
+        uint32_t w4[4] = {0u, 0u, 0u, 0u};
+        if (s != 0.0f) {
+          const float r = rcp_approx(s);
+          const bool r_ok = s >= 1.17549435e-38f && r < 3.0e38f;  // normal s, finite 1/s
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w4[i >> 2] |= e4m3_of_quotient(f[i], s, r, r_ok) << (8 * (i & 3));
+        }
+        codes[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
       for (int dg = 0; dg < d.nd; dg += 8) {
         int rows[8];
@@ -186,11 +228,11 @@ __global__ void __launch_bounds__(kDThreads)
             uint8_t* dst = recv_x + (int64_t)rows[qq] * H;
             float* dsc = recv_scale + (int64_t)rows[qq] * nb;
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const int b = b0 + 2 * u + half;
-              if (b < nb) {
-                st_v2(reinterpret_cast<uint2*>(dst + b * 128 + hl * 8), q[u]);
-                if (hl == 0) dsc[b] = sc[u];
+            for (int v = 0; v < U; ++v) {
+              const int b = (q0 + v) * 4 + qb;
+              if (q0 + v < q_end && b < nb) {
+                st_v4(reinterpret_cast<uint4*>(dst + b * 128 + hl * 16), codes[v]);
+                if (hl == 0) dsc[b] = sc[v];
               }
             }
           }
@@ -404,11 +446,25 @@ cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float*
                       topk_idx, topk_w, T, n16, k, W, slot, capacity_rows,
                       static_cast<uint4*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status);
   }
+  // segments per token: enough (token, segment) units to give every resident warp
+  // a few, but no more segments than block quadruples
   auto kern = dispatch_fp8_kernel<2>;
-  return launch_pdl(kern, dim3(grid_for(kern, T, kDThreads)), dim3(kDThreads), 0, stream, x4,
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDThreads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t warps = (int64_t)device_sm_count() * per_sm * (kDThreads / 32);
+  const int nquad = (H / 128 + 3) / 4;
+  int nseg = (int)((2 * warps + T - 1) / T);
+  nseg = nseg < 1 ? 1 : (nseg > nquad ? nquad : nseg);
+  const int64_t units = T * nseg;
+  const int64_t grid = (units * 32 + kDThreads - 1) / kDThreads < device_sm_count() * per_sm
+                           ? (units * 32 + kDThreads - 1) / kDThreads
+                           : (int64_t)device_sm_count() * per_sm;
+  return launch_pdl(kern, dim3((unsigned)(grid < 1 ? 1 : grid)), dim3(kDThreads), 0, stream, x4,
                     topk_idx, topk_w, T, H, k, W, slot, capacity_rows,
                     static_cast<uint8_t*>(recv_x), recv_scale, recv_topk_idx, recv_topk_w, recv_src,
-                    status);
+                    nseg, status);
 }
 
 }  // namespace ep

@@ -226,6 +226,39 @@ def test_fp8_many_values_match_oracle_encoder():
     _check_dispatch({"x": x, "topk_idx": idx, "topk_w": w}, lay, T, ep.EP_QUANT_FP8_E4M3_B128)
 
 
+def test_fp8_values_at_e4m3_rounding_boundaries():
+    """Values whose quotient x / scale falls on, or within a few fp32 ulps of, a
+    midpoint between two e4m3 values (and on exact e4m3 values), where a
+    quotient that is not correctly rounded would pick the wrong code."""
+    rng = np.random.default_rng(23)
+    tab = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    fin = np.unique(np.abs(tab[np.isfinite(tab)])).astype(np.float64)
+    mids = (fin[1:] + fin[:-1]) / 2
+    targets = np.concatenate([mids, fin])                     # quotients to aim at
+    T, H = 512, 1024
+    xs = np.zeros((T, H), np.float32)
+    for t in range(T):
+        # block scale 2^j exactly: amax = 448 * 2^j; other values x = target * 2^j, so
+        # x / scale lands on the target up to the bf16 rounding of x
+        j = int(rng.integers(-20, 20))
+        blk = rng.choice(targets, H) * 2.0 ** j
+        blk[::128] = 448.0 * 2.0 ** j
+        blk *= np.where(rng.random(H) < 0.5, -1.0, 1.0)
+        xs[t] = blk
+    x = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    # nudge half of the normal values by one bf16 ulp either way (never zeros,
+    # which would turn into NaN patterns)
+    nudge = rng.integers(-1, 2, x.shape).astype(np.int32)
+    nudge[:, ::128] = 0
+    expo = x & 0x7F80
+    nudge[(expo == 0) | (expo == 0x7F80)] = 0
+    x = (x.astype(np.int32) + nudge * (rng.random(x.shape) < 0.5)).astype(np.uint16)
+    idx = np.zeros((T, 1), np.int32)
+    w = np.ones((T, 1), np.float32)
+    lay = _check_layout(idx, 1, 1)
+    _check_dispatch({"x": x, "topk_idx": idx, "topk_w": w}, lay, T, ep.EP_QUANT_FP8_E4M3_B128)
+
+
 def test_invalid_expert_ids_are_ignored_and_flagged():
     rng = np.random.default_rng(31)
     T, E, k, W, H = 500, 64, 6, 8, 256

@@ -79,17 +79,27 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _kernel_source_hash(kernel_file: str) -> str:
+KERNEL_SOURCES = {
+    "dispatch": ("dispatch.cu", "dispatch_common.cuh", "ep_device.cuh"),
+    "combine": ("combine.cu", "ep_device.cuh"),
+    "layout": ("layout.cu", "ep_device.cuh"),
+    "dispatch_fp8": ("dispatch_fp8.cu", "dispatch_common.cuh", "ep_device.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """First 16 hex digits of the sha256 of the sources a kernel is built from."""
     h = hashlib.sha256()
-    for name in (kernel_file, "ep_device.cuh"):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "combine_ep_dispatch_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def _traffic_from_profile(kernel: str, kernel_file: str):
-    """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (its 'source_sha256_16' line), else None."""
+def _traffic_from_profile(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel sources (its
+    'source_sha256_16' line), else None."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_{WORKLOAD}.txt")
     try:
         txt = open(p).read()
@@ -97,7 +107,7 @@ def _traffic_from_profile(kernel: str, kernel_file: str):
         return None
     m = re.search(r"^source_sha256_16:\s*(\S+)", txt, re.M)
     b = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", txt, re.M)
-    if not m or not b or m.group(1) != _kernel_source_hash(kernel_file):
+    if not m or not b or m.group(1) != kernel_source_hash(kernel):
         return None
     return float(b.group(1))
 
@@ -322,8 +332,7 @@ def run_ours(args) -> dict | None:
         return None
 
     peak, peak_kind = _peaks()
-    dom, dom_file, dom_ms = (("dispatch", "dispatch.cu", d_ms) if d_ms >= c_ms
-                             else ("combine", "combine.cu", c_ms))
+    dom, dom_ms = ("dispatch", d_ms) if d_ms >= c_ms else ("combine", c_ms)
     achieved = nbytes[dom] / (dom_ms * 1e-3) / 1e9
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
     h2d = x_h.numel() * 2 + idx_h.numel() * 4 + w_h.numel() * 4
@@ -360,7 +369,7 @@ def run_ours(args) -> dict | None:
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": _traffic_from_profile(dom, dom_file)},
+                     "traffic": _traffic_from_profile(dom)},
         "cpu_baseline": cpu_baseline(args) if not args.no_cpu else None,
         "e2e": {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d,

@@ -1,67 +1,14 @@
-// Dispatch: one warp per token reads the token's row once and writes it to the
-// receive row of every destination rank (bf16 bit copy, or FP8 e4m3 with one
-// fp32 scale per 1x128 block), and carries the top-k ids, weights and the
-// source index along.
-#include "ep_device.cuh"
+// Dispatch of bf16 rows: one warp per token reads the token's row once and
+// writes it to the receive row of every destination rank, and carries the
+// top-k ids, weights and the source index along.  Rows of 1 KB and more go
+// through the bulk-copy (TMA) engine, smaller ones through 16-byte loads and
+// stores.  (FP8 rows: dispatch_fp8.cu.)
+#include "dispatch_common.cuh"
 
 namespace ep {
 namespace {
 
 constexpr int kDThreads = 256;
-
-// Destinations of token t in ascending rank order: lane i < nd holds the i-th
-// destination's receive row.  Rows at or beyond the capacity are dropped and
-// reported.  (The cached (token, rank) -> row map of "perf(ep): optimize
-// IntraNode dispatch kernel for MI350X", Technical Details 1, is `slot`.)
-struct Dests {
-  int nd;
-  int my_row;
-  bool cap_err;
-};
-
-__device__ __forceinline__ Dests token_dests(const int32_t* __restrict__ slot, int64_t t, int W,
-                                             int64_t cap, int lane) {
-  int s = -1;
-  if (lane < W) s = __ldg(slot + t * W + lane);
-  const bool keep = s >= 0 && (int64_t)s < cap;
-  const bool over = s >= 0 && (int64_t)s >= cap;
-  const unsigned dmask = __ballot_sync(kFull, keep);
-  const int r = nth_set_bit_of_lane(dmask, lane);
-  const int row = __shfl_sync(kFull, s, r & 31);
-  Dests d;
-  d.nd = __popc(dmask);
-  d.my_row = r >= 0 ? row : -1;
-  d.cap_err = __any_sync(kFull, over);
-  return d;
-}
-
-// Metadata of one token for all its destinations: per destination row, k ids,
-// k weights and the source index (2k+1 words), written by the whole warp at
-// once ("perf(ep): optimize IntraNode dispatch kernel for MI350X", Technical
-// Details 4).
-__device__ __forceinline__ void carry_metadata(const int32_t* __restrict__ topk_idx,
-                                               const float* __restrict__ topk_w, int64_t t, int k,
-                                               const Dests& d, int32_t* __restrict__ recv_topk_idx,
-                                               float* __restrict__ recv_topk_w,
-                                               int32_t* __restrict__ recv_src, int lane) {
-  const int per = 2 * k + 1;
-  const int total = d.nd * per;
-  for (int base = 0; base < total; base += 32) {
-    const int i = base + lane;
-    const int dd = i / per;
-    const int j = i - dd * per;
-    const int row = __shfl_sync(kFull, d.my_row, dd & 31);
-    if (i < total) {
-      if (j < k) {
-        if (recv_topk_idx) recv_topk_idx[(int64_t)row * k + j] = __ldg(topk_idx + t * k + j);
-      } else if (j < 2 * k) {
-        if (recv_topk_w) recv_topk_w[(int64_t)row * k + (j - k)] = __ldg(topk_w + t * k + (j - k));
-      } else if (recv_src) {
-        recv_src[row] = (int32_t)t;
-      }
-    }
-  }
-}
 
 // bf16 payload: lane l moves 16-byte chunks l, l+32, ... of the row; U chunks
 // are loaded before the stores of a round so that each lane keeps U loads in
@@ -102,138 +49,6 @@ __global__ void __launch_bounds__(kDThreads)
             for (int u = 0; u < U; ++u) {
               const int c = c0 + u * 32 + lane;
               if (c < n16) st_v4(dst + c, v[u]);
-            }
-          }
-        }
-      }
-    }
-  }
-  pdl_launch_dependents();
-  if (cap_err && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_CAPACITY);
-}
-
-// Two fp32 values to two e4m3 codes, round to nearest even, saturating to
-// +-448: `lo` goes to the low byte.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// One e4m3 code per value, of v / s with s > 0, exactly as if v / s were first
-// rounded to fp32 by IEEE division and that quotient then rounded to e4m3
-// (nearest, ties to even, saturating to +-448).  The e4m3 code is a
-// monotonic function of the quotient, so it is decided by a cheap quotient
-// q = v * (1/s) whenever the fp32 values 16 bit patterns below and above q
-// (in magnitude) map to the same code: |q - fl(v/s)| is only a few ulps
-// (rcp.approx has at most 1 ulp error, the product adds half an ulp), so the
-// correctly rounded quotient lies between them.  Otherwise (q near a rounding
-// boundary of e4m3, which happens for a few values in 10^5) the code comes from
-// the IEEE division itself.  `r` is 1/s from rcp.approx; r_ok is false when s
-// is subnormal or 1/s not finite, in which case every value takes the division.
-__device__ __forceinline__ uint32_t e4m3_of_quotient(float v, float s, float r, bool r_ok) {
-  if (r_ok) {
-    const float q = v * r;
-    const uint32_t m = __float_as_uint(q) & 0x7fffffffu;
-    const float lo = __uint_as_float(m > 16u ? m - 16u : 0u);
-    const float hi = __uint_as_float(m + 16u);
-    const uint32_t both = e4m3x2(lo, hi);
-    if ((both & 0xffu) == (both >> 8)) return (e4m3x2(q, 0.0f) & 0xffu);
-  }
-  return e4m3x2(__fdiv_rn(v, s), 0.0f) & 0xffu;
-}
-
-__device__ __forceinline__ float rcp_approx(float s) {
-  float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
-  return r;
-}
-
-// FP8 payload.  A 128-column block is 256 bytes of bf16 = 8 lanes x 32 bytes,
-// so a warp covers four blocks per round (lanes 8b..8b+7 for block b).  Per
-// block: amax over the block (an 8-lane max reduction), scale = amax / 448
-// (IEEE division), codes of x / scale (e4m3_of_quotient).  A token row is
-// split into `nseg` segments of block quadruples, one warp per (token,
-// segment), so that small batches still fill the GPU; each segment is
-// quantised once and its codes and scales are stored to every destination.
-template <int U>
-__global__ void __launch_bounds__(kDThreads)
-    dispatch_fp8_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ topk_idx,
-                        const float* __restrict__ topk_w, int64_t T, int H, int k, int W,
-                        const int32_t* __restrict__ slot, int64_t cap, uint8_t* __restrict__ recv_x,
-                        float* __restrict__ recv_scale, int32_t* __restrict__ recv_topk_idx,
-                        float* __restrict__ recv_topk_w, int32_t* __restrict__ recv_src,
-                        int nseg, int32_t* __restrict__ status) {
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int qb = lane >> 3, hl = lane & 7;  // block within the quad, lane within the block
-  const int nb = H >> 7;
-  const int n16 = H >> 3;
-  const int nquad = (nb + 3) >> 2;
-  const int per_seg = (nquad + nseg - 1) / nseg;
-  const int64_t gwarp = ((int64_t)blockIdx.x * kDThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * kDThreads) >> 5;
-  bool cap_err = false;
-  for (int64_t u = gwarp; u < T * nseg; u += nwarps) {
-    const int64_t t = u / nseg;
-    const int seg = (int)(u - t * nseg);
-    const Dests d = token_dests(slot, t, W, cap, lane);
-    if (seg == 0) {
-      cap_err |= d.cap_err;
-      carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
-    }
-    const uint4* src = x + t * n16;
-    const int q_end = (seg + 1) * per_seg < nquad ? (seg + 1) * per_seg : nquad;
-    for (int q0 = seg * per_seg; q0 < q_end; q0 += U) {
-      uint4 codes[U];
-      float sc[U];
-#pragma unroll
-      for (int v = 0; v < U; ++v) {
-        const int b = (q0 + v) * 4 + qb;
-        uint4 a = make_uint4(0u, 0u, 0u, 0u), c = make_uint4(0u, 0u, 0u, 0u);
-        if (q0 + v < q_end && b < nb) {
-          a = ld_stream_v4(src + b * 16 + hl * 2);
-          c = ld_stream_v4(src + b * 16 + hl * 2 + 1);
-        }
-        const float f[16] = {bf16_lo(a.x), bf16_hi(a.x), bf16_lo(a.y), bf16_hi(a.y),
-                             bf16_lo(a.z), bf16_hi(a.z), bf16_lo(a.w), bf16_hi(a.w),
-                             bf16_lo(c.x), bf16_hi(c.x), bf16_lo(c.y), bf16_hi(c.y),
-                             bf16_lo(c.z), bf16_hi(c.z), bf16_lo(c.w), bf16_hi(c.w)};
-        float m = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(f[i]));
-#pragma unroll
-        for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-        const float s = __fdiv_rn(m, 448.0f);
-        sc[v] = s;
-        uint32_t w4[4] = {0u, 0u, 0u, 0u};
-        if (s != 0.0f) {
-          const float r = rcp_approx(s);
-          const bool r_ok = s >= 1.17549435e-38f && r < 3.0e38f;  // normal s, finite 1/s
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w4[i >> 2] |= e4m3_of_quotient(f[i], s, r, r_ok) << (8 * (i & 3));
-        }
-        codes[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
-      for (int dg = 0; dg < d.nd; dg += 8) {
-        int rows[8];
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq) rows[qq] = __shfl_sync(kFull, d.my_row, (dg + qq) & 31);
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq) {
-          if (dg + qq < d.nd) {
-            uint8_t* dst = recv_x + (int64_t)rows[qq] * H;
-            float* dsc = recv_scale + (int64_t)rows[qq] * nb;
-#pragma unroll
-            for (int v = 0; v < U; ++v) {
-              const int b = (q0 + v) * 4 + qb;
-              if (q0 + v < q_end && b < nb) {
-                st_v4(reinterpret_cast<uint4*>(dst + b * 128 + hl * 16), codes[v]);
-                if (hl == 0) dsc[b] = sc[v];
-              }
             }
           }
         }
@@ -387,19 +202,13 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, 1)
   }
 }
 
-template <typename K>
-int grid_for(K kernel, int64_t T, int threads) {
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  const int64_t want = (T * 32 + threads - 1) / threads;  // one warp per token
-  const int64_t cap = (int64_t)device_sm_count() * per_sm;
-  int64_t g = want < cap ? want : cap;
-  return (int)(g < 1 ? 1 : g);
-}
-
 }  // namespace
+
+cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const float* topk_w,
+                                int64_t T, int H, int k, int W, const int32_t* slot,
+                                int64_t capacity_rows, void* recv_x, float* recv_scale,
+                                int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
+                                int32_t* status, cudaStream_t stream);
 
 cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w,
                             int64_t T, int H, int k, int W, const int32_t* slot,
@@ -446,25 +255,8 @@ cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float*
                       topk_idx, topk_w, T, n16, k, W, slot, capacity_rows,
                       static_cast<uint4*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status);
   }
-  // segments per token: enough (token, segment) units to give every resident warp
-  // a few, but no more segments than block quadruples
-  auto kern = dispatch_fp8_kernel<2>;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDThreads, 0) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  const int64_t warps = (int64_t)device_sm_count() * per_sm * (kDThreads / 32);
-  const int nquad = (H / 128 + 3) / 4;
-  int nseg = (int)((2 * warps + T - 1) / T);
-  nseg = nseg < 1 ? 1 : (nseg > nquad ? nquad : nseg);
-  const int64_t units = T * nseg;
-  const int64_t grid = (units * 32 + kDThreads - 1) / kDThreads < device_sm_count() * per_sm
-                           ? (units * 32 + kDThreads - 1) / kDThreads
-                           : (int64_t)device_sm_count() * per_sm;
-  return launch_pdl(kern, dim3((unsigned)(grid < 1 ? 1 : grid)), dim3(kDThreads), 0, stream, x4,
-                    topk_idx, topk_w, T, H, k, W, slot, capacity_rows,
-                    static_cast<uint8_t*>(recv_x), recv_scale, recv_topk_idx, recv_topk_w, recv_src,
-                    nseg, status);
+  return launch_dispatch_fp8(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, recv_x,
+                            recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream);
 }
 
 }  // namespace ep

@@ -72,13 +72,16 @@ __global__ void __launch_bounds__(kDThreads)
 #define EP_TMA_STAGES 3
 #endif
 #ifndef EP_TMA_SMEM_BUDGET
-#define EP_TMA_SMEM_BUDGET (200 * 1024)
+#define EP_TMA_SMEM_BUDGET 100000
 #endif
 #ifndef EP_TMA_MAX_WARPS
 #define EP_TMA_MAX_WARPS 8
 #endif
 #ifndef EP_TMA_CTAS_PER_SM
-#define EP_TMA_CTAS_PER_SM 1
+#define EP_TMA_CTAS_PER_SM 2
+#endif
+#ifndef EP_TMA_LANE_STORES
+#define EP_TMA_LANE_STORES 1
 #endif
 constexpr int kTmaStages = EP_TMA_STAGES;            // row buffers per warp
 constexpr int kTmaBarBytes = 1024;                   // barrier area ahead of the row buffers
@@ -92,7 +95,7 @@ __device__ __forceinline__ int load_slot(const int32_t* __restrict__ slot, int64
   return (t < T && lane < W) ? __ldg(slot + t * W + lane) : -1;
 }
 
-__global__ void __launch_bounds__(kTmaMaxWarps * 32, 1)
+__global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
     dispatch_bf16_tma_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
                              const float* __restrict__ topk_w, int64_t T, uint32_t row_bytes,
                              uint32_t stage_bytes, int k, int W, const int32_t* __restrict__ slot,
@@ -148,6 +151,16 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, 1)
     const int r = nth_set_bit_of_lane(dmask, lane);
     const int my_row = __shfl_sync(kFull, s_cur, r & 31);
 
+#if EP_TMA_LANE_STORES
+    // every lane observes the row's arrival, lane q sends it to destination q
+    const bool ok = mbar_wait_bounded(&full[st], parity);
+    if (!__all_sync(kFull, ok)) {
+      timed_out = true;
+      break;
+    }
+    if (lane < nd) bulk_store(recv_x + (int64_t)my_row * row_bytes, buf + st * stage_bytes, row_bytes);
+    bulk_commit();
+#else
     bool ok = true;
     if (lane == 0) ok = mbar_wait_bounded(&full[st], parity);
     if (!__shfl_sync(kFull, ok, 0)) {
@@ -159,6 +172,7 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, 1)
       if (lane == 0) bulk_store(recv_x + (int64_t)row * row_bytes, buf + st * stage_bytes, row_bytes);
     }
     if (lane == 0) bulk_commit();
+#endif
     if (meta_lanes) {
       for (int q = 0; q < nd; ++q) {
         const int64_t row = __shfl_sync(kFull, my_row, q);
@@ -178,6 +192,12 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, 1)
       carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
     }
     // refill the previous token's buffer once the copies out of it have read it
+#if EP_TMA_LANE_STORES
+    if (j >= 1 && issued < n) {
+      bulk_wait_read<1>();
+      __syncwarp();
+    }
+#endif
     if (lane == 0 && j >= 1 && issued < n) {
       bulk_wait_read<1>();
       const int sp = (int)((j - 1) % kTmaStages);
@@ -192,8 +212,8 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, 1)
     // never leave with a bulk copy still using this CTA's shared memory
     for (int64_t q = j; q < issued; ++q)
       (void)mbar_wait_bounded(&full[q % kTmaStages], (uint32_t)((q / kTmaStages) & 1));
-    bulk_wait_all();
   }
+  bulk_wait_all();
   __syncwarp();
   pdl_launch_dependents();
   if (lane == 0 && status != nullptr) {

@@ -299,6 +299,16 @@ def test_dispatch_without_metadata_outputs():
     _check_dispatch(inp, lay, int(lay["rank_offset"][-1]), ep.EP_QUANT_BF16, with_meta=False)
 
 
+@pytest.mark.parametrize("T,E,k,W", [(8192, 256, 8, 8), (8193, 256, 8, 8), (20000, 64, 6, 8),
+                                     (50000, 128, 8, 32), (30000, 96, 20, 3)])
+def test_layout_large_batches(T, E, k, W):
+    """Token counts on both sides of the one-CTA layout's limit (8192): the
+    larger ones go through the two-kernel layout with its workspace."""
+    idx = make_routing(np.random.default_rng(T + k), T, E, k, "zipf" if T % 2 else "uniform")
+    idx[np.random.default_rng(T).random(idx.shape) < 0.01] = -2
+    _check_layout(idx, E, W)
+
+
 @pytest.mark.parametrize("k,E,W", [(20, 64, 8), (8, 256, 8), (3, 48, 6)])
 def test_layout_unaligned_and_wide_rows(k, E, W):
     """topk_idx rows that are not 16-byte aligned, and k > 16 (scalar id loads)."""

@@ -61,8 +61,9 @@ def _routing(T, E, k, seed, invalid=0.0):
 
 
 @pytest.mark.parametrize("first,second", [
-    ((4096, 256, 8, 8, 0.0), (1000, 96, 5, 3, 0.05)),     # large call, then a smaller ragged one
-    ((257, 64, 6, 8, 0.02), (8192, 128, 8, 8, 0.0)),      # small call, then a larger one
+    ((40000, 256, 8, 8, 0.0), (12000, 96, 5, 3, 0.05)),   # large call, then a smaller ragged one
+    ((9000, 64, 6, 8, 0.02), (60000, 128, 8, 8, 0.0)),    # smaller call, then a larger one
+    ((4096, 256, 8, 8, 0.0), (20000, 256, 8, 8, 0.01)),   # the DeepSeek-V3 batch, then a large one
     ((0, 16, 4, 4, 0.0), (128, 16, 4, 4, 0.0)),           # empty call, then the tiny workload
 ])
 def test_noalloc_matches_workspace_layout_two_calls_in_a_row(first, second):

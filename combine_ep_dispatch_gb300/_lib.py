@@ -29,7 +29,10 @@ EP_QUANT_BF16 = 0
 EP_QUANT_FP8_E4M3_B128 = 1
 
 EXPORTED = ("ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_dispatch_layout", "ep_dispatch",
-            "ep_combine", "ep_status_string", "ep_dispatch_layout_noalloc")
+            "ep_combine", "ep_status_string", "ep_dispatch_layout_noalloc", "ep_dispatch_fused")
+
+# Largest batch ep_dispatch_fused takes.
+EP_FUSED_MAX_TOKENS = 1024
 
 # Size of the library's built-in layout workspace (ep_dispatch_layout_noalloc).
 EP_LAYOUT_NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -71,6 +74,9 @@ def load_library() -> ctypes.CDLL:
     lib.ep_combine.restype = _I
     lib.ep_dispatch_layout_noalloc.argtypes = [_P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, _P]
     lib.ep_dispatch_layout_noalloc.restype = _I
+    lib.ep_dispatch_fused.argtypes = [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I64, _P,
+                                      _P, _P, _P, _P, _P]
+    lib.ep_dispatch_fused.restype = _I
     lib.ep_status_string.argtypes = [_I]
     lib.ep_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -194,3 +200,31 @@ def ep_dispatch_layout_noalloc(topk_idx: torch.Tensor, E: int, W: int,
         _ptr(topk_idx), T, k, E, W, _ptr(num_tokens_per_expert), _ptr(num_tokens_per_rank),
         _ptr(rank_offset), _ptr(slot), _ptr(status), _stream(stream))
     _raise("ep_dispatch_layout_noalloc", rc)
+
+
+def ep_dispatch_fused(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor, E: int, W: int,
+                      num_tokens_per_expert: torch.Tensor, num_tokens_per_rank: torch.Tensor,
+                      rank_offset: torch.Tensor, slot: torch.Tensor, recv_x: torch.Tensor,
+                      recv_topk_idx: torch.Tensor | None = None,
+                      recv_topk_w: torch.Tensor | None = None,
+                      recv_src: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                      stream=None) -> None:
+    """ep_dispatch_layout + bf16 ep_dispatch in one launch (T <= EP_FUSED_MAX_TOKENS)."""
+    _check_cuda("x", x, torch.bfloat16)
+    for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
+                 ("num_tokens_per_rank", num_tokens_per_rank), ("rank_offset", rank_offset),
+                 ("slot", slot)):
+        _check_cuda(n, t, torch.int32)
+    _check_cuda("topk_w", topk_w, torch.float32)
+    _check_cuda("recv_x", recv_x, torch.bfloat16)
+    _check_cuda("recv_topk_idx", recv_topk_idx, torch.int32, optional=True)
+    _check_cuda("recv_topk_w", recv_topk_w, torch.float32, optional=True)
+    _check_cuda("recv_src", recv_src, torch.int32, optional=True)
+    _check_cuda("status", status, torch.int32, optional=True)
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    rc = load_library().ep_dispatch_fused(
+        _ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, E, W, _ptr(num_tokens_per_expert),
+        _ptr(num_tokens_per_rank), _ptr(rank_offset), _ptr(slot), recv_x.shape[0], _ptr(recv_x),
+        _ptr(recv_topk_idx), _ptr(recv_topk_w), _ptr(recv_src), _ptr(status), _stream(stream))
+    _raise("ep_dispatch_fused", rc)

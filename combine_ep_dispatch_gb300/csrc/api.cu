@@ -88,6 +88,30 @@ int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w, int
                                        status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int ep_dispatch_fused(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T,
+                      int H, int k, int E, int W, int32_t* num_tokens_per_expert,
+                      int32_t* num_tokens_per_rank, int32_t* rank_offset, int32_t* slot,
+                      int64_t capacity_rows, void* recv_x, int32_t* recv_topk_idx,
+                      float* recv_topk_w, int32_t* recv_src, int32_t* status, ep_stream_t stream) {
+  if (T < 0 || H < 1 || k < 1 || W < 1 || W > 32 || E < 1 || E > 8192 || E % W != 0 ||
+      capacity_rows < 0 || capacity_rows > kMaxRows)
+    return EP_ERR_INVALID_ARG;
+  if (T > ep::fused_max_tokens() || k > 16 || H % 8 != 0) return EP_ERR_UNSUPPORTED;
+  if (!num_tokens_per_expert || !num_tokens_per_rank || !rank_offset) return EP_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !topk_idx || !topk_w || !slot)) return EP_ERR_INVALID_ARG;
+  if (capacity_rows > 0 && !recv_x) return EP_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(recv_x, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+      !aligned(slot, 4) || !aligned(num_tokens_per_expert, 4) || !aligned(num_tokens_per_rank, 4) ||
+      !aligned(rank_offset, 4) || !aligned(recv_topk_idx, 4) || !aligned(recv_topk_w, 4) ||
+      !aligned(recv_src, 4) || !aligned(status, 4))
+    return EP_ERR_MISALIGNED;
+  return from_cuda(ep::launch_dispatch_fused(x, topk_idx, topk_w, T, H, k, E, W,
+                                             num_tokens_per_expert, num_tokens_per_rank,
+                                             rank_offset, slot, capacity_rows, recv_x,
+                                             recv_topk_idx, recv_topk_w, recv_src, status,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int ep_combine(const void* y, const int32_t* slot, int64_t T, int H, int W, int64_t capacity_rows,
                void* out, int32_t* status, ep_stream_t stream) {
   if (T < 0 || H < 1 || W < 1 || W > 32 || capacity_rows < 0 || capacity_rows > kMaxRows)

@@ -54,6 +54,14 @@ class DispatchCombine:
                          self.recv_topk_w, self.recv_src, self.recv_scale, self.quant, self.status,
                          stream)
 
+    def dispatch_fused(self, x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                       stream=None) -> None:
+        """layout() and dispatch() in one launch (bf16, T <= EP_FUSED_MAX_TOKENS)."""
+        _lib.ep_dispatch_fused(x, topk_idx, topk_w, self.E, self.W, self.num_tokens_per_expert,
+                               self.num_tokens_per_rank, self.rank_offset, self.slot, self.recv_x,
+                               self.recv_topk_idx, self.recv_topk_w, self.recv_src, self.status,
+                               stream)
+
     def combine(self, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
         """Sum each token's expert outputs ``y`` (default: the dispatched rows,
         i.e. identity experts; bf16 dispatch only) into ``self.out``."""

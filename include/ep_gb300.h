@@ -144,6 +144,29 @@ EP_API int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk
                 int32_t* status, ep_stream_t stream);
 
 /*
+ * ep_dispatch_layout followed by a bf16 ep_dispatch, in one launch, for small
+ * batches (decode): T <= EP_FUSED_MAX_TOKENS.  Every output is the one the two
+ * calls would produce (layout outputs included: slot is needed by combine), so
+ * it is a drop-in replacement for them where latency matters.  Every CTA
+ * recomputes the batch's layout from topk_idx and then sends the tokens it
+ * owns at once, which saves the second launch and the slot round trip.
+ * Follows the single-pass routing of the low-latency kernel discussed on
+ * "perf(ep): optimize IntraNode dispatch kernel for MI350X" (the IntraNodeLL
+ * comparison), with the deterministic slot numbering of ep_dispatch_layout.
+ *
+ * Arguments: those of ep_dispatch_layout and ep_dispatch (bf16 payload only),
+ * no workspace.  Limits: T <= EP_FUSED_MAX_TOKENS, 1 <= k <= 16, 1 <= W <= 32,
+ * E % W == 0, E <= 8192, H % 8 == 0; EP_ERR_UNSUPPORTED otherwise.
+ */
+#define EP_FUSED_MAX_TOKENS 1024
+EP_API int ep_dispatch_fused(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T,
+                             int H, int k, int E, int W, int32_t* num_tokens_per_expert,
+                             int32_t* num_tokens_per_rank, int32_t* rank_offset, int32_t* slot,
+                             int64_t capacity_rows, void* recv_x, int32_t* recv_topk_idx,
+                             float* recv_topk_w, int32_t* recv_src, int32_t* status,
+                             ep_stream_t stream);
+
+/*
  * Combine: out[t] = bf16_rne( ((+0 + y[s_0]) + y[s_1]) + ... ) with the fp32
  * sum taken over the ranks r in D(t) in ascending order, s_r = slot[t][r]; a
  * token with no rows gives +0.  Follows "perf(ep): optimize IntraNode dispatch

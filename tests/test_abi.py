@@ -119,6 +119,21 @@ def test_combine_rejects(lib, kw, code):
     assert rc == code
 
 
+@cpu_only
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=1025), _lib.EP_ERR_UNSUPPORTED),                    # beyond EP_FUSED_MAX_TOKENS
+    (dict(k=17), _lib.EP_ERR_UNSUPPORTED),
+    (dict(H=12), _lib.EP_ERR_UNSUPPORTED),
+    (dict(E=100), _lib.EP_ERR_INVALID_ARG),                     # E % W != 0
+    (dict(x_off=4), _lib.EP_ERR_MISALIGNED),
+])
+def test_fused_rejects(lib, kw, code):
+    rc = lib.ep_dispatch_fused(A + kw.get("x_off", 0), A, A, kw.get("T", 256), kw.get("H", 256),
+                               kw.get("k", 8), kw.get("E", 256), 8, A, A, A, A, 2048, A, A, A, A,
+                               None, None)
+    assert rc == code
+
+
 def test_binding_rejects_host_tensors(lib):
     idx = torch.zeros(4, 2, dtype=torch.int32)
     with pytest.raises(ValueError):

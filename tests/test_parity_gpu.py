@@ -176,7 +176,9 @@ def test_shapes_bf16(T, H, E, k, W):
 
 
 @pytest.mark.parametrize("T,H,E,k,W", [(1, 128, 8, 2, 2), (257, 384, 64, 6, 8), (64, 7168, 256, 8, 8),
-                                       (100, 1024, 64, 16, 32)])
+                                       (100, 1024, 64, 16, 32), (2000, 7168, 256, 8, 8),
+                                       (1500, 1024, 64, 16, 32), (1025, 384, 48, 3, 6),
+                                       (9000, 640, 64, 4, 8)])
 def test_shapes_fp8(T, H, E, k, W):
     rng = np.random.default_rng(T + H)
     x = make_bf16(rng, (T, H), scale=5.0)
@@ -217,7 +219,7 @@ def test_fp8_special_blocks():
 def test_fp8_many_values_match_oracle_encoder():
     """Codes for 8M random normal values across many binades."""
     rng = np.random.default_rng(22)
-    T, H = 1024, 8192
+    T, H = 2048, 8192
     xs = (rng.standard_normal((T, H)) * 2.0 ** rng.integers(-30, 30, (T, 1))).astype(np.float32)
     x = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     idx = np.zeros((T, 1), np.int32)
@@ -235,7 +237,7 @@ def test_fp8_values_at_e4m3_rounding_boundaries():
     fin = np.unique(np.abs(tab[np.isfinite(tab)])).astype(np.float64)
     mids = (fin[1:] + fin[:-1]) / 2
     targets = np.concatenate([mids, fin])                     # quotients to aim at
-    T, H = 512, 1024
+    T, H = 1536, 1024
     xs = np.zeros((T, H), np.float32)
     for t in range(T):
         # block scale 2^j exactly: amax = 448 * 2^j; other values x = target * 2^j, so

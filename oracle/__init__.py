@@ -18,7 +18,7 @@ import numpy as np
 from ._build import LIB, build_oracle
 
 __all__ = ["STATUS_BAD_EXPERT", "STATUS_CAPACITY", "QUANT_BF16", "QUANT_FP8",
-           "layout", "dispatch", "combine", "bf16_from_f32", "e4m3_from_f32",
+           "layout", "dispatch", "combine", "localize_ids", "bf16_from_f32", "e4m3_from_f32",
            "f32_from_e4m3", "f32_from_bf16", "run_all"]
 
 STATUS_BAD_EXPERT = 1
@@ -48,6 +48,8 @@ def _load():
         lib.ep_ref_bf16_from_f32_array.restype = None
         lib.ep_ref_e4m3_from_f32_array.argtypes = [_P, _I64, _P]
         lib.ep_ref_e4m3_from_f32_array.restype = None
+        lib.ep_ref_localize_ids.argtypes = [_P, _I64, _I, _I, _I, _P]
+        lib.ep_ref_localize_ids.restype = _I
         lib.ep_ref_f32_from_e4m3.argtypes = [ctypes.c_uint8]
         lib.ep_ref_f32_from_e4m3.restype = ctypes.c_float
         _lib = lib
@@ -109,6 +111,18 @@ def dispatch(x: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, slot: np.n
     if quant == QUANT_FP8:
         out["recv_scale"] = recv_scale
     return out
+
+
+def localize_ids(recv_topk_idx: np.ndarray, E: int, W: int, rank_offset: np.ndarray) -> np.ndarray:
+    """Local-id metadata: ids of rank r's receive rows become e - r*(E/W) for
+    experts hosted by r, -1 otherwise (returns a new array)."""
+    lib = _load()
+    ids = np.array(recv_topk_idx, dtype=np.int32, copy=True, order="C")
+    off = _c(rank_offset, np.int32)
+    rc = lib.ep_ref_localize_ids(_ptr(ids), ids.shape[0], ids.shape[1], E, W, _ptr(off))
+    if rc != 0:
+        raise ValueError("oracle localize_ids: invalid arguments")
+    return ids
 
 
 def combine(y: np.ndarray, slot: np.ndarray, cap: int | None = None) -> dict:

@@ -258,3 +258,26 @@ int ep_ref_combine(const uint16_t* y, const int32_t* slot, int64_t T, int H, int
   if (status) *status |= st;
   return 0;
 }
+
+/* --------------------------------------------------------- local expert ids */
+
+/* Local-id metadata (dispatch option): in receive row s of rank r (rows
+ * rank_offset[r] <= s < rank_offset[r+1]), an expert id e of the row's token is
+ * replaced by its index among rank r's experts, e - r * (E / W), when e is a
+ * valid id hosted by rank r, and by -1 otherwise.  Applied in place to the
+ * verbatim ids of rows [0, min(R, cap)). */
+int ep_ref_localize_ids(int32_t* recv_topk_idx, int64_t cap, int k, int E, int W,
+                        const int32_t* rank_offset) {
+  if (k < 1 || E < 1 || W < 1 || W > 32 || E % W != 0 || cap < 0) return -1;
+  int Er = E / W;
+  for (int r = 0; r < W; ++r) {
+    for (int64_t s = rank_offset[r]; s < rank_offset[r + 1] && s < cap; ++s) {
+      for (int j = 0; j < k; ++j) {
+        int32_t e = recv_topk_idx[s * k + j];
+        int hosted = e >= 0 && e < E && e / Er == r;
+        recv_topk_idx[s * k + j] = hosted ? e - r * Er : -1;
+      }
+    }
+  }
+  return 0;
+}

@@ -305,3 +305,41 @@ def test_combine_capacity_rows_are_skipped_and_flagged():
     slot = lay["slot"].copy()
     slot[slot >= R - 5] = -1
     np.testing.assert_array_equal(res["out"], oracle.combine(y, slot)["out"])
+
+
+def test_localize_ids_golden_hand_example():
+    """Hand-worked on the layout fixture (E=8, W=4, two experts per rank): rows
+    0-1 are rank 0 (tokens 0, 2), rows 2-3 rank 1 (tokens 0, 3), row 4 rank 2
+    (token 1), row 5 rank 3 (token 2)."""
+    g = _golden("layout_combine_tiny.json")
+    idx = np.array(g["topk_idx"], np.int32)
+    lay = oracle.layout(idx, g["E"], g["W"])
+    dis = oracle.dispatch(np.zeros((5, 8), np.uint16), idx, np.ones((5, 2), np.float32), lay["slot"], 6)
+    local = oracle.localize_ids(dis["recv_topk_idx"], g["E"], g["W"], lay["rank_offset"])
+    want = [[0, -1],    # token 0 [0, 3] on rank 0: 0 -> 0, 3 lives on rank 1
+            [-1, 1],    # token 2 [7, 1] on rank 0: 1 -> 1
+            [-1, 1],    # token 0 on rank 1: 3 -> 3 - 2 = 1
+            [-1, 0],    # token 3 [9, 2] on rank 1: 9 invalid, 2 -> 0
+            [1, 0],     # token 1 [5, 4] on rank 2: 5 -> 1, 4 -> 0
+            [1, -1]]    # token 2 [7, 1] on rank 3: 7 -> 1
+    np.testing.assert_array_equal(local, want)
+
+
+def test_localize_ids_restatement_random():
+    rng = np.random.default_rng(61)
+    T, E, W, k = 300, 48, 6, 5
+    idx = make_routing(rng, T, E, k)
+    idx[rng.random(idx.shape) < 0.05] = -4
+    lay = oracle.layout(idx, E, W)
+    R = int(lay["rank_offset"][-1])
+    dis = oracle.dispatch(make_bf16(rng, (T, 8)), idx, rng.random((T, k), dtype=np.float32), lay["slot"], R)
+    local = oracle.localize_ids(dis["recv_topk_idx"], E, W, lay["rank_offset"])
+    Er = E // W
+    for t in range(T):
+        for r in range(W):
+            s = lay["slot"][t, r]
+            if s < 0:
+                continue
+            want = [e - r * Er if 0 <= e < E and e // Er == r else -1 for e in idx[t]]
+            assert list(local[s]) == want
+            assert any(v >= 0 for v in want)      # a row is only sent to a rank hosting an expert

@@ -8,7 +8,7 @@ does, and raises ImportError when it has not been built.
 from ._lib import (EP_ERR_CUDA, EP_ERR_INVALID_ARG, EP_ERR_MISALIGNED, EP_ERR_UNSUPPORTED,
                    EP_ERR_WORKSPACE, EP_OK, EP_QUANT_BF16, EP_QUANT_FP8_E4M3_B128,
                    EP_STATUS_BAD_EXPERT, EP_STATUS_CAPACITY, EPError, ep_combine, ep_dispatch,
-                   ep_dispatch_fused, EP_FUSED_MAX_TOKENS,
+                   ep_dispatch_fused, EP_FUSED_MAX_TOKENS, ep_localize_expert_ids,
                    ep_dispatch_layout, ep_dispatch_layout_noalloc, ep_layout_workspace_bytes, ep_max_recv_rows,
                    ep_status_string, load_library)
 from .pipeline import DispatchCombine
@@ -18,5 +18,5 @@ __all__ = [
     "EP_ERR_WORKSPACE", "EP_STATUS_BAD_EXPERT", "EP_STATUS_CAPACITY", "EP_QUANT_BF16",
     "EP_QUANT_FP8_E4M3_B128", "EPError", "ep_dispatch_layout", "ep_dispatch", "ep_combine",
     "ep_dispatch_layout_noalloc", "ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_status_string", "load_library",
-    "DispatchCombine", "ep_dispatch_fused", "EP_FUSED_MAX_TOKENS",
+    "DispatchCombine", "ep_dispatch_fused", "EP_FUSED_MAX_TOKENS", "ep_localize_expert_ids",
 ]

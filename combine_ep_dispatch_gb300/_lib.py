@@ -29,7 +29,8 @@ EP_QUANT_BF16 = 0
 EP_QUANT_FP8_E4M3_B128 = 1
 
 EXPORTED = ("ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_dispatch_layout", "ep_dispatch",
-            "ep_combine", "ep_status_string", "ep_dispatch_layout_noalloc", "ep_dispatch_fused")
+            "ep_combine", "ep_status_string", "ep_dispatch_layout_noalloc", "ep_dispatch_fused",
+            "ep_localize_expert_ids")
 
 # Largest batch ep_dispatch_fused takes.
 EP_FUSED_MAX_TOKENS = 1024
@@ -77,6 +78,8 @@ def load_library() -> ctypes.CDLL:
     lib.ep_dispatch_fused.argtypes = [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I64, _P,
                                       _P, _P, _P, _P, _P]
     lib.ep_dispatch_fused.restype = _I
+    lib.ep_localize_expert_ids.argtypes = [_P, _P, _I64, _I, _I, _I, _P]
+    lib.ep_localize_expert_ids.restype = _I
     lib.ep_status_string.argtypes = [_I]
     lib.ep_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -228,3 +231,14 @@ def ep_dispatch_fused(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Ten
         _ptr(num_tokens_per_rank), _ptr(rank_offset), _ptr(slot), recv_x.shape[0], _ptr(recv_x),
         _ptr(recv_topk_idx), _ptr(recv_topk_w), _ptr(recv_src), _ptr(status), _stream(stream))
     _raise("ep_dispatch_fused", rc)
+
+
+def ep_localize_expert_ids(recv_topk_idx: torch.Tensor, rank_offset: torch.Tensor, E: int, W: int,
+                           stream=None) -> None:
+    """In place: ids of rank r's receive rows become local indices e - r*(E/W), or -1."""
+    _check_cuda("recv_topk_idx", recv_topk_idx, torch.int32)
+    _check_cuda("rank_offset", rank_offset, torch.int32)
+    cap, k = recv_topk_idx.shape
+    rc = load_library().ep_localize_expert_ids(_ptr(recv_topk_idx), _ptr(rank_offset), cap, k, E, W,
+                                               _stream(stream))
+    _raise("ep_localize_expert_ids", rc)

@@ -112,6 +112,18 @@ int ep_dispatch_fused(const void* x, const int32_t* topk_idx, const float* topk_
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int ep_localize_expert_ids(int32_t* recv_topk_idx, const int32_t* rank_offset,
+                           int64_t capacity_rows, int k, int E, int W, ep_stream_t stream) {
+  if (k < 1 || W < 1 || W > 32 || E < 1 || E % W != 0 || capacity_rows < 0 ||
+      capacity_rows > kMaxRows)
+    return EP_ERR_INVALID_ARG;
+  if (!rank_offset || (capacity_rows > 0 && !recv_topk_idx)) return EP_ERR_INVALID_ARG;
+  if (!aligned(recv_topk_idx, 4) || !aligned(rank_offset, 4)) return EP_ERR_MISALIGNED;
+  if (capacity_rows == 0) return EP_OK;
+  return from_cuda(ep::launch_localize_ids(recv_topk_idx, rank_offset, capacity_rows, k, E, W,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int ep_combine(const void* y, const int32_t* slot, int64_t T, int H, int W, int64_t capacity_rows,
                void* out, int32_t* status, ep_stream_t stream) {
   if (T < 0 || H < 1 || W < 1 || W > 32 || capacity_rows < 0 || capacity_rows > kMaxRows)

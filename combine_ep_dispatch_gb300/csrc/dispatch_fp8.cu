@@ -16,31 +16,6 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// e4m3 codes of v / s (s > 0), exactly as if v / s were first rounded to fp32
-// by IEEE division and that quotient then rounded to e4m3 (nearest, ties to
-// even, saturating to +-448).
-//
-// The code is a monotonic function of the fp32 quotient, so a cheap quotient
-// q = v * r, r = rcp.approx(s) (at most 1 ulp off, the product adds half an
-// ulp: a few ulps from the correctly rounded quotient), gives the same code
-// unless a rounding boundary of e4m3 lies within a few ulps of q.  For
-// 2^-6 <= |q| (normal e4m3) the boundaries, midpoints between neighbouring
-// e4m3 values (1 + (2j+1)/16) * 2^e, are exactly the fp32 values whose low 20
-// mantissa bits are 0x80000, so "near a boundary" is a bit test on q with a
-// margin of 16 bit patterns each way.  Values with 0 < |q| < 2^-6 (e4m3
-// subnormals) and values near a boundary take the IEEE division; that is a
-// few values in 10^5 for normally distributed rows.
-__device__ __forceinline__ bool e4m3_needs_division(float q) {
-  const uint32_t m = __float_as_uint(q) & 0x7fffffffu;
-  return (m - 1u) < 0x3c7fffffu || ((m + (16u - 0x80000u)) & 0xfffffu) <= 32u;
-}
-
-__device__ __noinline__ uint32_t e4m3_by_division(float v, float s) {
-  return e4m3x2(__fdiv_rn(v, s), 0.0f) & 0xffu;
-}
 
 __device__ __forceinline__ float rcp_approx(float s) {
   float r;
@@ -54,49 +29,54 @@ __device__ __forceinline__ float bf16x16_absmax(const uint32_t (&w)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     uint32_t a = w[i] & 0x7fff7fffu, r;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(m));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(m));  // |x| >= 0: order of the values
     m = r;
   }
   const uint32_t hi = m >> 16, lo = m & 0xffffu;
   return __uint_as_float((hi > lo ? hi : lo) << 16);
 }
 
-// Codes of the 16 bf16 values in w[0..7] (element 2i low half of w[i]) divided
-// by s > 0, packed little-endian into 16 bytes.
+// e4m3 codes of the 16 bf16 values in w[0..7] (element 2i in the low half of
+// w[i]) divided by s > 0, packed little-endian into 16 bytes: exactly the code
+// of the IEEE-rounded fp32 quotient fl(v/s) rounded to e4m3 (nearest, ties to
+// even, saturating to +-448), without a division per value.
+//
+// The code is a monotonic function of the quotient.  With r = rcp.approx(s)
+// (at most 1 ulp from 1/s), fl(v/s) lies between v*r*(1 - 2^-18) and
+// v*r*(1 + 2^-18) -- their distance from v/s is some thirty times the combined
+// rounding of r and of the products -- so when those two bracket values give
+// the same code, it is the code of fl(v/s).  When they differ, a rounding
+// boundary of e4m3 lies inside the bracket (a few values in 10^5 for normally
+// distributed rows) and the IEEE division decides.  A subnormal s or a
+// non-finite 1/s sends every value to the division.
 __device__ __forceinline__ uint4 e4m3x16_of_quotients(const uint32_t (&w)[8], float s) {
   const float r = rcp_approx(s);
-  const bool fast = s >= 1.17549435e-38f && r < 3.0e38f;  // normal s, finite 1/s
-  uint32_t out[4];
-  uint32_t slow = fast ? 0u : 0xffffu;
+  const bool fast = s >= 1.17549435e-38f && r < 3.0e38f;
+  const float r_lo = r * (1.0f - 0x1p-18f), r_hi = r * (1.0f + 0x1p-18f);
+  uint32_t c[8];
+  uint32_t slow = fast ? 0u : 0xffu;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float q0 = __uint_as_float(w[i] << 16) * r;
-    const float q1 = __uint_as_float(w[i] & 0xffff0000u) * r;
-    const uint32_t c = e4m3x2(q0, q1);
-    if (i & 1)
-      out[i >> 1] |= c << 16;
-    else
-      out[i >> 1] = c;
-    slow |= (e4m3_needs_division(q0) ? 1u : 0u) << (2 * i);
-    slow |= (e4m3_needs_division(q1) ? 1u : 0u) << (2 * i + 1);
+    const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xffff0000u);
+    const uint32_t lo = e4m3x2(a * r_lo, b * r_lo), hi = e4m3x2(a * r_hi, b * r_hi);
+    c[i] = lo;
+    slow |= (lo != hi ? 1u : 0u) << i;
   }
   if (slow) {
-    for (int e = 0; e < 16; ++e) {
-      if (slow & (1u << e)) {
-        const uint32_t bits = (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16);
-        const uint32_t code = e4m3_by_division(__uint_as_float(bits), s);
-        const int sh = 8 * (e & 3);
-        out[e >> 2] = (out[e >> 2] & ~(0xffu << sh)) | (code << sh);
-      }
-    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (slow & (1u << i))
+        c[i] = e4m3x2(__fdiv_rn(__uint_as_float(w[i] << 16), s),
+                      __fdiv_rn(__uint_as_float(w[i] & 0xffff0000u), s));
   }
-  return make_uint4(out[0], out[1], out[2], out[3]);
+  return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16),
+                    c[6] | (c[7] << 16));
 }
 
 // FP8 payload.  A 128-column block is 256 bytes of bf16 = 8 lanes x 32 bytes,
 // so a warp covers four blocks per round (lanes 8b..8b+7 for block b).  Per
 // block: amax over the block (an 8-lane max reduction), scale = amax / 448
-// (IEEE division), codes of x / scale (e4m3_of_quotient).  A token row is
+// (IEEE division), codes of x / scale (e4m3x16_of_quotients).  A token row is
 // split into `nseg` segments of block quadruples, one warp per (token,
 // segment), so that small batches still fill the GPU; each segment is
 // quantised once and its codes and scales are stored to every destination.

@@ -197,6 +197,9 @@ cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float*
                             int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
                             int32_t* status, cudaStream_t stream);
 
+cudaError_t launch_localize_ids(int32_t* recv_topk_idx, const int32_t* rank_offset, int64_t cap,
+                                int k, int E, int W, cudaStream_t stream);
+
 int64_t fused_max_tokens();
 cudaError_t launch_dispatch_fused(const void* x, const int32_t* topk_idx, const float* topk_w,
                                   int64_t T, int H, int k, int E, int W, int32_t* ne, int32_t* nr,

@@ -488,3 +488,46 @@ extern "C" EP_API int ep_dispatch_layout_noalloc(const int32_t* topk_idx, int64_
                             status, stream);
 }
 
+
+// ---------------------------------------------------------------------------
+// Local expert ids of the receive rows, in place.  Row s belongs to rank r
+// with rank_offset[r] <= s < rank_offset[r+1]; each of its k ids e becomes
+// e - r * (E / W) when e is a valid expert hosted by rank r, and -1 otherwise,
+// so that rank r's expert side reads directly which of its experts a row needs.
+namespace ep {
+namespace {
+
+__global__ void __launch_bounds__(256)
+    localize_ids_kernel(int32_t* __restrict__ recv_topk_idx, const int32_t* __restrict__ rank_offset,
+                        int64_t cap, int k, int E, int W) {
+  pdl_wait();
+  __shared__ int32_t s_off[33];
+  if (threadIdx.x <= (unsigned)W) s_off[threadIdx.x] = rank_offset[threadIdx.x];
+  __syncthreads();
+  const int64_t rows = (int64_t)s_off[W] < cap ? (int64_t)s_off[W] : cap;
+  const int Er = E / W;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < rows * k;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t s = i / k;
+    int lo = 0, hi = W - 1;  // the rank whose region holds row s
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)s_off[mid] <= s) lo = mid; else hi = mid - 1;
+    }
+    const int32_t e = recv_topk_idx[i];
+    recv_topk_idx[i] = (e >= 0 && e < E && e / Er == lo) ? e - lo * Er : -1;
+  }
+  pdl_launch_dependents();
+}
+
+}  // namespace
+
+cudaError_t launch_localize_ids(int32_t* recv_topk_idx, const int32_t* rank_offset, int64_t cap,
+                                int k, int E, int W, cudaStream_t stream) {
+  const int64_t sms = device_sm_count();
+  const int grid = (int)(sms > 0 ? sms * 4 : 1);
+  return launch_pdl(localize_ids_kernel, dim3(grid), dim3(256), 0, stream, recv_topk_idx,
+                    rank_offset, cap, k, E, W);
+}
+
+}  // namespace ep

@@ -144,6 +144,20 @@ EP_API int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk
                 int32_t* status, ep_stream_t stream);
 
 /*
+ * Local expert ids, in place, after ep_dispatch on the same stream: in receive
+ * row s of rank r (rank_offset[r] <= s < rank_offset[r+1], s < capacity_rows)
+ * each of the k ids e in recv_topk_idx[s] becomes e - r * (E / W) when e is a
+ * valid expert hosted by rank r, and -1 otherwise; rows from rank_offset[W] on
+ * are untouched.  Gives each rank's expert side the local experts a row needs,
+ * from the per-rank destination rule of "perf(ep): optimize IntraNode dispatch
+ * kernel for MI350X", Technical Details 1 (expert e lives on rank e / (E/W)).
+ *  recv_topk_idx  int32 [capacity_rows, k], rank_offset int32 [W + 1]
+ * Limits: 1 <= k; 1 <= W <= 32; E % W == 0.
+ */
+EP_API int ep_localize_expert_ids(int32_t* recv_topk_idx, const int32_t* rank_offset,
+                                  int64_t capacity_rows, int k, int E, int W, ep_stream_t stream);
+
+/*
  * ep_dispatch_layout followed by a bf16 ep_dispatch, in one launch, for small
  * batches (decode): T <= EP_FUSED_MAX_TOKENS.  Every output is the one the two
  * calls would produce (layout outputs included: slot is needed by combine), so

@@ -363,3 +363,26 @@ def test_host_errors_through_binding():
     x = torch.zeros(cfg.T, cfg.H + 8, dtype=torch.bfloat16, device="cuda")[:, 1:cfg.H + 1]
     with pytest.raises(ValueError):
         ep.ep_dispatch(x, idx, idx.float(), cfg.W, dc.slot, dc.recv_x)      # not contiguous
+
+
+@pytest.mark.parametrize("name,T,W", [("tiny", None, None), ("dsv3", None, None), ("qwen", 3000, None),
+                                      ("tiny", 200, 1)])
+def test_localize_expert_ids(name, T, W):
+    """ep_localize_expert_ids after dispatch against the oracle's local ids."""
+    inp = make_inputs(name, seed=51, T=T)
+    cfg = inp["cfg"]
+    W = W or cfg.W
+    idx = inp["topk_idx"].copy()
+    idx[np.random.default_rng(52).random(idx.shape) < 0.02] = -1
+    lay = oracle.layout(idx, cfg.E, W)
+    R = int(lay["rank_offset"][-1])
+    cap = R + 5
+    dis = oracle.dispatch(inp["x"], idx, inp["topk_w"], lay["slot"], cap)
+    want = oracle.localize_ids(dis["recv_topk_idx"], cfg.E, W, lay["rank_offset"])
+    ids = torch.from_numpy(dis["recv_topk_idx"]).cuda()
+    off = torch.from_numpy(lay["rank_offset"]).cuda()
+    ep.ep_localize_expert_ids(ids, off, cfg.E, W)
+    torch.cuda.synchronize()
+    got = ids.cpu().numpy()
+    assert_rows_equal(got[:R], want[:R], "local ids")
+    np.testing.assert_array_equal(got[R:], dis["recv_topk_idx"][R:])   # rows beyond R untouched

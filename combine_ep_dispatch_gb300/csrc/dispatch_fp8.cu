@@ -127,23 +127,25 @@ __global__ void __launch_bounds__(kDThreads)
         sc[v] = s;
         codes[v] = s != 0.0f ? e4m3x16_of_quotients(w, s) : make_uint4(0u, 0u, 0u, 0u);
       }
-      for (int dg = 0; dg < d.nd; dg += 8) {
-        int rows[8];
+      // the lane's byte offsets in a row, and whether each of its blocks exists
+      bool has[U];
+      int boff[U];
 #pragma unroll
-        for (int qq = 0; qq < 8; ++qq) rows[qq] = __shfl_sync(kFull, d.my_row, (dg + qq) & 31);
+      for (int v = 0; v < U; ++v) {
+        const int b = (q0 + v) * 4 + qb;
+        has[v] = q0 + v < q_end && b < nb;
+        boff[v] = b * 128 + hl * 16;
+      }
+#pragma unroll 1
+      for (int qq = 0; qq < d.nd; ++qq) {  // the token's destinations only
+        const int64_t row = __shfl_sync(kFull, d.my_row, qq);
+        uint8_t* dst = recv_x + row * H;
+        float* dsc = recv_scale + row * nb;
 #pragma unroll
-        for (int qq = 0; qq < 8; ++qq) {
-          if (dg + qq < d.nd) {
-            uint8_t* dst = recv_x + (int64_t)rows[qq] * H;
-            float* dsc = recv_scale + (int64_t)rows[qq] * nb;
-#pragma unroll
-            for (int v = 0; v < U; ++v) {
-              const int b = (q0 + v) * 4 + qb;
-              if (q0 + v < q_end && b < nb) {
-                st_v4(reinterpret_cast<uint4*>(dst + b * 128 + hl * 16), codes[v]);
-                if (hl == 0) dsc[b] = sc[v];
-              }
-            }
+        for (int v = 0; v < U; ++v) {
+          if (has[v]) {
+            st_v4(reinterpret_cast<uint4*>(dst + boff[v]), codes[v]);
+            if (hl == 0) dsc[(q0 + v) * 4 + qb] = sc[v];
           }
         }
       }

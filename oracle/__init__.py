@@ -18,7 +18,7 @@ import numpy as np
 from ._build import LIB, build_oracle
 
 __all__ = ["STATUS_BAD_EXPERT", "STATUS_CAPACITY", "QUANT_BF16", "QUANT_FP8",
-           "layout", "dispatch", "combine", "localize_ids", "bf16_from_f32", "e4m3_from_f32",
+           "layout", "dispatch", "combine", "localize_ids", "layout_experts", "combine_weighted", "bf16_from_f32", "e4m3_from_f32",
            "f32_from_e4m3", "f32_from_bf16", "run_all"]
 
 STATUS_BAD_EXPERT = 1
@@ -48,6 +48,10 @@ def _load():
         lib.ep_ref_bf16_from_f32_array.restype = None
         lib.ep_ref_e4m3_from_f32_array.argtypes = [_P, _I64, _P]
         lib.ep_ref_e4m3_from_f32_array.restype = None
+        lib.ep_ref_layout_experts.argtypes = [_P, _I64, _I, _I, _P, _P, _P, _P, _P]
+        lib.ep_ref_layout_experts.restype = _I
+        lib.ep_ref_combine_weighted.argtypes = [_P, _P, _P, _I64, _I, _I, _I64, _P, _P, _P]
+        lib.ep_ref_combine_weighted.restype = _I
         lib.ep_ref_localize_ids.argtypes = [_P, _I64, _I, _I, _I, _P]
         lib.ep_ref_localize_ids.restype = _I
         lib.ep_ref_f32_from_e4m3.argtypes = [ctypes.c_uint8]
@@ -123,6 +127,42 @@ def localize_ids(recv_topk_idx: np.ndarray, E: int, W: int, rank_offset: np.ndar
     if rc != 0:
         raise ValueError("oracle localize_ids: invalid arguments")
     return ids
+
+
+def layout_experts(topk_idx: np.ndarray, E: int) -> dict:
+    """Expert-major layout: per-expert counts, expert_offset [E+1], slot [T, k]."""
+    lib = _load()
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    ne = np.zeros(E, np.int32)
+    off = np.zeros(E + 1, np.int32)
+    slot = np.zeros((T, k), np.int32)
+    nxt = np.zeros(E, np.int32)
+    st = np.zeros(1, np.int32)
+    rc = lib.ep_ref_layout_experts(_ptr(idx), T, k, E, _ptr(ne), _ptr(off), _ptr(slot), _ptr(nxt),
+                                   _ptr(st))
+    if rc != 0:
+        raise ValueError("oracle layout_experts: invalid arguments")
+    return {"num_tokens_per_expert": ne, "expert_offset": off, "slot": slot, "status": int(st[0])}
+
+
+def combine_weighted(y: np.ndarray, slot: np.ndarray, w: np.ndarray, cap: int | None = None) -> dict:
+    """Weighted combine: fp32 fused multiply-add chain over the slot columns in order."""
+    lib = _load()
+    y = _c(y, np.uint16)
+    slot = _c(slot, np.int32)
+    w = _c(w, np.float32)
+    T, C = slot.shape
+    H = y.shape[1]
+    cap = y.shape[0] if cap is None else cap
+    out = np.zeros((T, H), np.uint16)
+    acc = np.zeros(H, np.float32)
+    st = np.zeros(1, np.int32)
+    rc = lib.ep_ref_combine_weighted(_ptr(y), _ptr(slot), _ptr(w), T, H, C, cap, _ptr(out),
+                                     _ptr(acc), _ptr(st))
+    if rc != 0:
+        raise ValueError("oracle combine_weighted: invalid arguments")
+    return {"out": out, "status": int(st[0])}
 
 
 def combine(y: np.ndarray, slot: np.ndarray, cap: int | None = None) -> dict:

@@ -281,3 +281,75 @@ int ep_ref_localize_ids(int32_t* recv_topk_idx, int64_t cap, int k, int E, int W
   }
   return 0;
 }
+
+/* ------------------------------------------------------ expert-major layout */
+
+/* Expert-major layout: one receive row per valid (token, expert slot) pair,
+ * grouped by expert.  counts per expert as in ep_ref_layout; expert_offset[0..E]
+ * = exclusive prefix sum of the counts; slot[t][j] = expert_offset[e] + (number
+ * of pairs (t', j') before (t, j) in (token, then j) order with the same expert
+ * e = topk_idx[t][j]) for a valid e, else -1.  Rank r's experts r*Er..(r+1)*Er-1
+ * are consecutive, so rank r's rows are one range as well.  This is the
+ * per-expert receive layout of the recv kernel in "Optimizing Distributed
+ * Inference Kernels for AMD DEVELOPER CHALLENGE 2025" (section 3.1, item 1:
+ * rows of local expert e start at e times a per-expert maximum), with each
+ * expert's rows packed by a scan of the counts instead of a fixed per-expert
+ * capacity, and in token order. */
+int ep_ref_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,
+                          int32_t* num_tokens_per_expert, int32_t* expert_offset, int32_t* slot,
+                          int32_t* next_scratch, int32_t* status) {
+  if (T < 0 || k < 1 || E < 1) return -1;
+  int32_t st = 0;
+  for (int e = 0; e < E; ++e) num_tokens_per_expert[e] = 0;
+  for (int64_t i = 0; i < T * k; ++i) {
+    int32_t e = topk_idx[i];
+    if (e < 0 || e >= E) {
+      st |= EP_REF_STATUS_BAD_EXPERT;
+      continue;
+    }
+    num_tokens_per_expert[e] += 1;
+  }
+  expert_offset[0] = 0;
+  for (int e = 0; e < E; ++e) expert_offset[e + 1] = expert_offset[e] + num_tokens_per_expert[e];
+  for (int e = 0; e < E; ++e) next_scratch[e] = expert_offset[e];
+  for (int64_t t = 0; t < T; ++t) {
+    for (int j = 0; j < k; ++j) {
+      int32_t e = topk_idx[t * k + j];
+      slot[t * k + j] = (e < 0 || e >= E) ? -1 : next_scratch[e]++;
+    }
+  }
+  if (status) *status |= st;
+  return 0;
+}
+
+/* ------------------------------------------------------- weighted combine */
+
+/* Weighted combine over a slot table of C columns: out[t][h] =
+ * bf16( fma(w[t][C-1], y[s_{C-1}][h], ... fma(w[t][0], y[s_0][h], +0)) ) over the
+ * columns c in ascending order with s_c = slot[t][c] >= 0 (rows >= cap skipped
+ * and flagged), each step one fused multiply-add rounded once (fmaf).  With the
+ * expert-major slot table and w = topk_w this is the gate-weighted sum of the
+ * token's expert outputs; with weights 1 it is the plain combine. */
+int ep_ref_combine_weighted(const uint16_t* y, const int32_t* slot, const float* w, int64_t T,
+                            int H, int C, int64_t cap, uint16_t* out, float* acc_scratch,
+                            int32_t* status) {
+  if (T < 0 || H < 1 || C < 1 || cap < 0) return -1;
+  int32_t st = 0;
+  for (int64_t t = 0; t < T; ++t) {
+    for (int h = 0; h < H; ++h) acc_scratch[h] = 0.0f;
+    for (int c = 0; c < C; ++c) {
+      int32_t s = slot[t * C + c];
+      if (s < 0) continue;
+      if ((int64_t)s >= cap) {
+        st |= EP_REF_STATUS_CAPACITY;
+        continue;
+      }
+      const float wt = w[t * C + c];
+      const uint16_t* row = y + (int64_t)s * H;
+      for (int h = 0; h < H; ++h) acc_scratch[h] = fmaf(wt, ep_ref_f32_from_bf16(row[h]), acc_scratch[h]);
+    }
+    for (int h = 0; h < H; ++h) out[t * H + h] = ep_ref_bf16_from_f32(acc_scratch[h]);
+  }
+  if (status) *status |= st;
+  return 0;
+}

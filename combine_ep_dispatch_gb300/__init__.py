@@ -10,7 +10,8 @@ from ._lib import (EP_ERR_CUDA, EP_ERR_INVALID_ARG, EP_ERR_MISALIGNED, EP_ERR_UN
                    EP_STATUS_BAD_EXPERT, EP_STATUS_CAPACITY, EPError, ep_combine, ep_dispatch,
                    ep_dispatch_fused, EP_FUSED_MAX_TOKENS, ep_localize_expert_ids,
                    ep_dispatch_layout, ep_dispatch_layout_noalloc, ep_layout_workspace_bytes, ep_max_recv_rows,
-                   ep_status_string, load_library)
+                   ep_status_string, load_library, ep_layout_experts_workspace_bytes,
+                   ep_dispatch_layout_experts, ep_combine_weighted)
 from .pipeline import DispatchCombine
 
 __all__ = [
@@ -19,4 +20,5 @@ __all__ = [
     "EP_QUANT_FP8_E4M3_B128", "EPError", "ep_dispatch_layout", "ep_dispatch", "ep_combine",
     "ep_dispatch_layout_noalloc", "ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_status_string", "load_library",
     "DispatchCombine", "ep_dispatch_fused", "EP_FUSED_MAX_TOKENS", "ep_localize_expert_ids",
+    "ep_layout_experts_workspace_bytes", "ep_dispatch_layout_experts", "ep_combine_weighted",
 ]

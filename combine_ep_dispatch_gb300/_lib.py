@@ -30,7 +30,8 @@ EP_QUANT_FP8_E4M3_B128 = 1
 
 EXPORTED = ("ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_dispatch_layout", "ep_dispatch",
             "ep_combine", "ep_status_string", "ep_dispatch_layout_noalloc", "ep_dispatch_fused",
-            "ep_localize_expert_ids")
+            "ep_localize_expert_ids", "ep_layout_experts_workspace_bytes",
+            "ep_dispatch_layout_experts", "ep_combine_weighted")
 
 # Largest batch ep_dispatch_fused takes.
 EP_FUSED_MAX_TOKENS = 1024
@@ -80,6 +81,13 @@ def load_library() -> ctypes.CDLL:
     lib.ep_dispatch_fused.restype = _I
     lib.ep_localize_expert_ids.argtypes = [_P, _P, _I64, _I, _I, _I, _P]
     lib.ep_localize_expert_ids.restype = _I
+    lib.ep_layout_experts_workspace_bytes.argtypes = [_I64, _I, _I]
+    lib.ep_layout_experts_workspace_bytes.restype = ctypes.c_size_t
+    lib.ep_dispatch_layout_experts.argtypes = [_P, _I64, _I, _I, _P, _P, _P, _P, ctypes.c_size_t,
+                                               _P, _P]
+    lib.ep_dispatch_layout_experts.restype = _I
+    lib.ep_combine_weighted.argtypes = [_P, _P, _P, _I64, _I, _I, _I64, _P, _P, _P]
+    lib.ep_combine_weighted.restype = _I
     lib.ep_status_string.argtypes = [_I]
     lib.ep_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -242,3 +250,48 @@ def ep_localize_expert_ids(recv_topk_idx: torch.Tensor, rank_offset: torch.Tenso
     rc = load_library().ep_localize_expert_ids(_ptr(recv_topk_idx), _ptr(rank_offset), cap, k, E, W,
                                                _stream(stream))
     _raise("ep_localize_expert_ids", rc)
+
+
+def ep_layout_experts_workspace_bytes(T: int, k: int, E: int) -> int:
+    return int(load_library().ep_layout_experts_workspace_bytes(T, k, E))
+
+
+def ep_dispatch_layout_experts(topk_idx: torch.Tensor, E: int, num_tokens_per_expert: torch.Tensor,
+                               expert_offset: torch.Tensor, slot: torch.Tensor,
+                               workspace: torch.Tensor, status: torch.Tensor | None = None,
+                               stream=None) -> None:
+    """Expert-major layout: slot [T, k] gives each valid (token, column) pair its
+    own row, rows grouped by expert (expert_offset [E + 1])."""
+    for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
+                 ("expert_offset", expert_offset), ("slot", slot)):
+        _check_cuda(n, t, torch.int32)
+    _check_cuda("workspace", workspace)
+    _check_cuda("status", status, torch.int32, optional=True)
+    T, k = topk_idx.shape
+    if tuple(slot.shape) != (T, k):
+        raise ValueError("slot must be [T, k]")
+    rc = load_library().ep_dispatch_layout_experts(
+        _ptr(topk_idx), T, k, E, _ptr(num_tokens_per_expert), _ptr(expert_offset), _ptr(slot),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream))
+    _raise("ep_dispatch_layout_experts", rc)
+
+
+def ep_combine_weighted(y: torch.Tensor, slot: torch.Tensor, w: torch.Tensor, out: torch.Tensor,
+                        status: torch.Tensor | None = None, stream=None) -> None:
+    """out[t] = bf16 of the fp32 FMA chain over the columns c of slot[t] >= 0,
+    in ascending order, of w[t][c] * y[slot[t][c]]."""
+    _check_cuda("y", y, torch.bfloat16)
+    _check_cuda("slot", slot, torch.int32)
+    _check_cuda("w", w, torch.float32)
+    _check_cuda("out", out, torch.bfloat16)
+    _check_cuda("status", status, torch.int32, optional=True)
+    T, C = slot.shape
+    H = out.shape[1]
+    if y.dim() != 2 or y.shape[1] != H:
+        raise ValueError("y must be [capacity_rows, H] with the same H as out")
+    if tuple(w.shape) != (T, C):
+        raise ValueError("w must have the shape of slot")
+    rc = load_library().ep_combine_weighted(_ptr(y), _ptr(slot), _ptr(w), T, H, C, y.shape[0],
+                                            _ptr(out), _ptr(status), _stream(stream))
+    _raise("ep_combine_weighted", rc)

@@ -138,6 +138,44 @@ int ep_combine(const void* y, const int32_t* slot, int64_t T, int H, int W, int6
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t ep_layout_experts_workspace_bytes(int64_t T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return 0;
+  return ep::layout_experts_workspace_bytes(T, k, E);
+}
+
+int ep_dispatch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,
+                               int32_t* num_tokens_per_expert, int32_t* expert_offset,
+                               int32_t* slot, void* workspace, size_t workspace_bytes,
+                               int32_t* status, ep_stream_t stream) {
+  if (T < 0 || k < 1 || E < 1 || E > ep::layout_experts_max_experts()) return EP_ERR_INVALID_ARG;
+  if (T > kMaxRows / k) return EP_ERR_UNSUPPORTED;
+  if (!num_tokens_per_expert || !expert_offset || !workspace) return EP_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !slot)) return EP_ERR_INVALID_ARG;
+  if (workspace_bytes < ep::layout_experts_workspace_bytes(T, k, E)) return EP_ERR_WORKSPACE;
+  if (!aligned(topk_idx, 4) || !aligned(num_tokens_per_expert, 4) || !aligned(expert_offset, 4) ||
+      !aligned(slot, 4) || !aligned(workspace, 16) || !aligned(status, 4))
+    return EP_ERR_MISALIGNED;
+  return from_cuda(ep::launch_layout_experts(topk_idx, T, k, E, num_tokens_per_expert,
+                                             expert_offset, slot, workspace, status,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ep_combine_weighted(const void* y, const int32_t* slot, const float* w, int64_t T, int H,
+                        int C, int64_t capacity_rows, void* out, int32_t* status,
+                        ep_stream_t stream) {
+  if (T < 0 || H < 1 || C < 1 || C > 32 || capacity_rows < 0 || capacity_rows > kMaxRows)
+    return EP_ERR_INVALID_ARG;
+  if (H % 8 != 0) return EP_ERR_UNSUPPORTED;
+  if (T > kMaxRows / C) return EP_ERR_UNSUPPORTED;
+  if (T > 0 && (!slot || !w || !out)) return EP_ERR_INVALID_ARG;
+  if (T > 0 && capacity_rows > 0 && !y) return EP_ERR_INVALID_ARG;
+  if (!aligned(y, 16) || !aligned(out, 16) || !aligned(slot, 4) || !aligned(w, 4) ||
+      !aligned(status, 4))
+    return EP_ERR_MISALIGNED;
+  return from_cuda(ep::launch_combine_weighted(y, slot, w, T, H, C, capacity_rows, out, status,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* ep_status_string(int code) {
   switch (code) {
     case EP_OK:

@@ -28,14 +28,30 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v) {
   acc[7] = acc[7] + __uint_as_float(v.w & 0xffff0000u);
 }
 
+// acc[i] = fma(wt, y[i], acc[i]): one rounding per step.
+__device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float wt, const uint4& v) {
+  acc[0] = __fmaf_rn(wt, __uint_as_float(v.x << 16), acc[0]);
+  acc[1] = __fmaf_rn(wt, __uint_as_float(v.x & 0xffff0000u), acc[1]);
+  acc[2] = __fmaf_rn(wt, __uint_as_float(v.y << 16), acc[2]);
+  acc[3] = __fmaf_rn(wt, __uint_as_float(v.y & 0xffff0000u), acc[3]);
+  acc[4] = __fmaf_rn(wt, __uint_as_float(v.z << 16), acc[4]);
+  acc[5] = __fmaf_rn(wt, __uint_as_float(v.z & 0xffff0000u), acc[5]);
+  acc[6] = __fmaf_rn(wt, __uint_as_float(v.w << 16), acc[6]);
+  acc[7] = __fmaf_rn(wt, __uint_as_float(v.w & 0xffff0000u), acc[7]);
+}
+
 // Lane l handles 16-byte chunks l, l+32, ... of the hidden dimension.  For a
 // round of U chunks the loads of up to 8 destination rows are all issued before
 // the first addition (8*U loads in flight per lane); the additions then run in
-// ascending rank order, which fixes the rounding of the sum.
-template <int U>
+// ascending column order, which fixes the rounding of the sum.  WEIGHTED:
+// each row enters as a fused multiply-add with the weight of its column,
+// w[t][c] ("perf(ep): optimize IntraNode dispatch kernel for MI350X",
+// Remaining gap: combine accumulates the rows with FMA).
+template <int U, bool WEIGHTED>
 __global__ void __launch_bounds__(kCThreads)
-    combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ slot, int64_t T, int n16,
-                   int W, int64_t cap, uint4* __restrict__ out, int32_t* __restrict__ status) {
+    combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ slot,
+                   const float* __restrict__ w, int64_t T, int n16, int W, int64_t cap,
+                   uint4* __restrict__ out, int32_t* __restrict__ status) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = ((int64_t)blockIdx.x * kCThreads + threadIdx.x) >> 5;
@@ -52,6 +68,11 @@ __global__ void __launch_bounds__(kCThreads)
     const int nd = __popc(dmask);
     const int r = nth_set_bit_of_lane(dmask, lane);
     const int my_row = __shfl_sync(kFull, s, r & 31);  // lane i: row of i-th destination
+    float my_w = 0.0f;
+    if constexpr (WEIGHTED) {
+      const float wl = lane < W ? __ldg(w + t * W + lane) : 0.0f;
+      my_w = __shfl_sync(kFull, wl, r & 31);               // and its weight
+    }
     uint4* dst = out + t * n16;
     for (int c0 = 0; c0 < n16; c0 += 32 * U) {
       float acc[U][8];
@@ -61,8 +82,12 @@ __global__ void __launch_bounds__(kCThreads)
         for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
       for (int dg = 0; dg < nd; dg += 8) {
         int rows[8];
+        float wts[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) rows[q] = __shfl_sync(kFull, my_row, (dg + q) & 31);
+        for (int q = 0; q < 8; ++q) {
+          rows[q] = __shfl_sync(kFull, my_row, (dg + q) & 31);
+          wts[q] = WEIGHTED ? __shfl_sync(kFull, my_w, (dg + q) & 31) : 1.0f;
+        }
         uint4 v[8][U];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -77,7 +102,12 @@ __global__ void __launch_bounds__(kCThreads)
         for (int q = 0; q < 8; ++q) {
           if (dg + q < nd) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) add_bf16x8(acc[u], v[q][u]);
+            for (int u = 0; u < U; ++u) {
+              if constexpr (WEIGHTED)
+                fma_bf16x8(acc[u], wts[q], v[q][u]);
+              else
+                add_bf16x8(acc[u], v[q][u]);
+            }
           }
         }
       }
@@ -272,6 +302,24 @@ __global__ void __launch_bounds__((kCWarps + 1) * 32, 1)
 
 }  // namespace
 
+// One warp per token, as many CTAs as fit on the device at once (grid-stride
+// over the tokens beyond that).
+template <typename K>
+cudaError_t launch_combine_regs(K kern, const void* y, const int32_t* slot, const float* w,
+                                int64_t T, int H, int W, int64_t capacity_rows, void* out,
+                                int32_t* status, cudaStream_t stream) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCThreads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t want = (T * 32 + kCThreads - 1) / kCThreads;
+  const int64_t most = (int64_t)device_sm_count() * per_sm;
+  const int grid = (int)(want < most ? want : most);
+  return launch_pdl(kern, dim3(grid < 1 ? 1 : grid), dim3(kCThreads), 0, stream,
+                    static_cast<const uint4*>(y), slot, w, T, H / 8, W, capacity_rows,
+                    static_cast<uint4*>(out), status);
+}
+
 cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H, int W,
                            int64_t capacity_rows, void* out, int32_t* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
@@ -298,17 +346,16 @@ cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H,
                       smem, stream, static_cast<const uint8_t*>(y), slot, T, row_bytes, chunk, W,
                       capacity_rows, static_cast<uint8_t*>(out), status);
   }
-  auto kern = combine_kernel<EP_COMBINE_U>;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCThreads, 0) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  const int64_t want = (T * 32 + kCThreads - 1) / kCThreads;
-  const int64_t most = (int64_t)device_sm_count() * per_sm;
-  const int grid = (int)(want < most ? want : most);
-  return launch_pdl(kern, dim3(grid < 1 ? 1 : grid), dim3(kCThreads), 0, stream,
-                    static_cast<const uint4*>(y), slot, T, H / 8, W, capacity_rows,
-                    static_cast<uint4*>(out), status);
+  return launch_combine_regs(combine_kernel<EP_COMBINE_U, false>, y, slot, nullptr, T, H, W,
+                             capacity_rows, out, status, stream);
+}
+
+cudaError_t launch_combine_weighted(const void* y, const int32_t* slot, const float* w, int64_t T,
+                                    int H, int C, int64_t capacity_rows, void* out,
+                                    int32_t* status, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  return launch_combine_regs(combine_kernel<EP_COMBINE_U, true>, y, slot, w, T, H, C,
+                             capacity_rows, out, status, stream);
 }
 
 }  // namespace ep

@@ -209,6 +209,16 @@ cudaError_t launch_dispatch_fused(const void* x, const int32_t* topk_idx, const 
 
 cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H, int W,
                            int64_t capacity_rows, void* out, int32_t* status, cudaStream_t stream);
+cudaError_t launch_combine_weighted(const void* y, const int32_t* slot, const float* w, int64_t T,
+                                    int H, int C, int64_t capacity_rows, void* out,
+                                    int32_t* status, cudaStream_t stream);
+
+int layout_experts_max_experts();
+size_t layout_experts_workspace_bytes(int64_t T, int k, int E);
+cudaError_t launch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,
+                                  int32_t* num_tokens_per_expert, int32_t* expert_offset,
+                                  int32_t* slot, void* workspace, int32_t* status,
+                                  cudaStream_t stream);
 
 // cudaLaunchKernelEx with the programmatic-stream-serialization attribute.
 template <typename... KArgs, typename... Args>

@@ -1,0 +1,370 @@
+// Expert-major layout: one receive row per valid (token, top-k column) pair,
+// grouped by expert.  Expert e owns rows [expert_offset[e], expert_offset[e+1]),
+// the exclusive prefix sum of the per-expert pair counts; inside it the pairs
+// follow (token, column) order.  This is the per-expert receive layout of the
+// recv kernel in "Optimizing Distributed Inference Kernels for AMD DEVELOPER
+// CHALLENGE 2025" (section 3.1, item 1), packed by a scan instead of a fixed
+// per-expert maximum, so that each expert's rows are one dense block for a
+// grouped GEMM.  The experts of rank r are consecutive, so rank r's rows are
+// one range as well.
+//
+// The (token, column) pairs are taken in their flat order p = t * k + j, which
+// is the order of topk_idx and of the slot table in memory.  A warp handles
+// groups of 32 consecutive pairs: within a group, the pairs before p with the
+// same expert are the lanes below p's in __match_any_sync(e), and the groups of
+// a warp are consecutive, so per warp a running count per expert completes the
+// rank.  Across warps and chunks the counts are scanned per expert.
+//
+// Up to kXSingleMax pairs and 1024 experts: one CTA of 32 warps does it all.
+// Larger: chunks of kXPairs pairs and three kernels
+//   count:  per-chunk, per-expert pair counts;
+//   scan:   per expert, the pairs in earlier chunks (in place) and the total;
+//   assign: offsets by a block scan of the totals, then the slots.
+// Integer counts only: the layout is a pure function of topk_idx.
+#include "ep_device.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kXWarps = 8;                     // warps of a chunk CTA
+constexpr int kXGroups = 4;                    // groups of 32 pairs per warp
+constexpr int kXPairs = kXWarps * kXGroups * 32;  // 1024 pairs per chunk
+constexpr int kXSingleWarps = 32;
+constexpr int kXSingleGroups = 8;
+constexpr int64_t kXSingleMax = kXSingleWarps * kXSingleGroups * 32;  // 8192 pairs
+constexpr int kXSingleMaxE = 1024;
+constexpr int kXMaxE = 4096;
+
+inline size_t a256(size_t b) { return (b + 255) & ~size_t(255); }
+inline int64_t x_chunks(int64_t P) { return P <= 0 ? 1 : (P + kXPairs - 1) / kXPairs; }
+
+struct XWs {
+  int32_t* cnt;  // [C][E]: pairs of chunk c with expert e; after the scan, pairs in chunks < c
+  int32_t* tot;  // [E]
+};
+
+XWs x_carve(void* ws, int64_t P, int E) {
+  char* p = static_cast<char*>(ws);
+  XWs w;
+  w.cnt = reinterpret_cast<int32_t*>(p);
+  p += a256(sizeof(int32_t) * (size_t)(x_chunks(P) * E));
+  w.tot = reinterpret_cast<int32_t*>(p);
+  return w;
+}
+
+// Block-wide exclusive scan of s_val[0..n) into s_out[0..n], s_out[n] = total;
+// every thread of the block calls it.  Thread i takes a run of consecutive
+// entries; runs are combined with a warp scan and a scan of the warp totals.
+__device__ void block_exclusive_scan(const int32_t* s_val, int32_t* s_out, int n,
+                                     int32_t* s_warp /* [32] */) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int per = (n + nthreads - 1) / nthreads;
+  const int lo = tid * per;
+  const int hi = min(lo + per, n);
+  int run = 0;
+  for (int i = lo; i < hi; ++i) run += s_val[i];
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < nwarps ? s_warp[lane] : 0;
+    int wi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, wi, o);
+      if (lane >= o) wi += y;
+    }
+    s_warp[lane] = wi - v;  // exclusive, per warp
+  }
+  __syncthreads();
+  int acc = s_warp[warp] + incl - run;
+  for (int i = lo; i < hi; ++i) {
+    const int v = s_val[i];
+    s_out[i] = acc;
+    acc += v;
+  }
+  if (hi == n && lo < n) s_out[n] = acc;
+  if (n == 0 && tid == 0) s_out[0] = 0;
+  __syncthreads();
+}
+
+// Ranks of a warp's pairs, in flat order, given s_run[e] = the first row of
+// expert e for this warp.  ids[i] is the expert of the lane's pair in group i
+// (valid[i] false for pairs that get no row).
+template <int G>
+__device__ __forceinline__ void rank_groups(const int (&ids)[G], const bool (&valid)[G], int ng,
+                                            int32_t* s_run, int (&row)[G]) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = lanemask_lt();
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    row[i] = -1;
+    if (i < ng) {
+      const int key = valid[i] ? ids[i] : -1 - lane;  // invalid pairs match nobody
+      const unsigned peers = __match_any_sync(kFull, key);
+      if (valid[i]) row[i] = s_run[ids[i]] + __popc(peers & lt);
+      __syncwarp();
+      if (valid[i] && (peers & lt) == 0) s_run[ids[i]] += __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
+// Per-warp counts of experts, added to s_cnt[e] (this warp's row).
+template <int G>
+__device__ __forceinline__ void count_groups(const int (&ids)[G], const bool (&valid)[G], int ng,
+                                             int32_t* s_cnt) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = lanemask_lt();
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    if (i < ng) {
+      const int key = valid[i] ? ids[i] : -1 - lane;
+      const unsigned peers = __match_any_sync(kFull, key);
+      if (valid[i] && (peers & lt) == 0) s_cnt[ids[i]] += __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
+// The ids of groups g0 .. g0+ng-1 of 32 pairs starting at flat pair `base`.
+template <int G>
+__device__ __forceinline__ bool load_groups(const int32_t* __restrict__ topk_idx, int64_t P,
+                                            int64_t base, int ng, int E, int (&ids)[G],
+                                            bool (&valid)[G]) {
+  const int lane = threadIdx.x & 31;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    const int64_t p = base + (int64_t)i * 32 + lane;
+    const bool live = i < ng && p < P;
+    const int e = live ? __ldg(topk_idx + p) : -1;
+    ids[i] = e;
+    valid[i] = live && (unsigned)e < (unsigned)E;
+    bad |= live && !valid[i];
+  }
+  return bad;
+}
+
+// One CTA, all pairs (P <= kXSingleMax, E <= kXSingleMaxE).
+__global__ void __launch_bounds__(kXSingleWarps * 32, 1)
+    xlayout_single_kernel(const int32_t* __restrict__ topk_idx, int64_t P, int E,
+                          int32_t* __restrict__ num_tokens_per_expert,
+                          int32_t* __restrict__ expert_offset, int32_t* __restrict__ slot,
+                          int32_t* __restrict__ status) {
+  pdl_wait();
+  extern __shared__ int32_t s_dyn[];
+  int32_t* s_cnt = s_dyn;                          // [32][E]
+  int32_t* s_tot = s_cnt + kXSingleWarps * E;      // [E]
+  int32_t* s_off = s_tot + E;                      // [E + 1]
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ng = (int)((P + kXSingleWarps * 32 - 1) / (kXSingleWarps * 32));  // groups per warp
+  const int64_t base = (int64_t)warp * ng * 32;
+  int ids[kXSingleGroups];
+  bool valid[kXSingleGroups];
+  const bool bad = load_groups<kXSingleGroups>(topk_idx, P, base, ng, E, ids, valid);
+  if (__any_sync(kFull, bad) && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_BAD_EXPERT);
+  for (int i = tid; i < kXSingleWarps * E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  count_groups<kXSingleGroups>(ids, valid, ng, s_cnt + warp * E);
+  __syncthreads();
+  // per expert: exclusive prefix over the warps (in place) and the total
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = 0;
+#pragma unroll 8
+    for (int w = 0; w < kXSingleWarps; ++w) {
+      const int v = s_cnt[w * E + e];
+      s_cnt[w * E + e] = run;
+      run += v;
+    }
+    s_tot[e] = run;
+    num_tokens_per_expert[e] = run;
+  }
+  __syncthreads();
+  block_exclusive_scan(s_tot, s_off, E, s_warp);
+  for (int e = tid; e <= E; e += blockDim.x) expert_offset[e] = s_off[e];
+  for (int e = tid; e < E; e += blockDim.x) {
+#pragma unroll 8
+    for (int w = 0; w < kXSingleWarps; ++w) s_cnt[w * E + e] += s_off[e];
+  }
+  __syncthreads();
+  int row[kXSingleGroups];
+  rank_groups<kXSingleGroups>(ids, valid, ng, s_cnt + warp * E, row);
+#pragma unroll
+  for (int i = 0; i < kXSingleGroups; ++i) {
+    const int64_t p = base + (int64_t)i * 32 + lane;
+    if (i < ng && p < P) slot[p] = row[i];
+  }
+  pdl_launch_dependents();
+}
+
+// Chunk c: per-expert counts of its kXPairs pairs.
+__global__ void __launch_bounds__(kXWarps * 32)
+    xlayout_count_kernel(const int32_t* __restrict__ topk_idx, int64_t P, int E, XWs ws,
+                         int32_t* __restrict__ status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  extern __shared__ int32_t s_hist[];  // [E]
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t c = blockIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) s_hist[e] = 0;
+  __syncthreads();
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < kXPairs / (kXWarps * 32); ++i) {
+    const int64_t p = c * kXPairs + (int64_t)i * kXWarps * 32 + tid;
+    const int e = p < P ? __ldg(topk_idx + p) : -1;
+    if (p < P) {
+      if ((unsigned)e < (unsigned)E) atomicAdd(&s_hist[e], 1);
+      else bad = true;
+    }
+  }
+  if (__any_sync(kFull, bad) && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_BAD_EXPERT);
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) ws.cnt[c * E + e] = s_hist[e];
+}
+
+// Experts 32b .. 32b+31 (one per lane): the 8 warps split the chunks into 8
+// consecutive ranges; a first pass sums each range, a second writes, per
+// chunk, the pairs of the expert in all earlier chunks.
+__global__ void __launch_bounds__(kXWarps * 32)
+    xlayout_scan_kernel(int64_t C, int E, XWs ws, int32_t* __restrict__ num_tokens_per_expert) {
+  pdl_wait();
+  __shared__ int32_t s_part[kXWarps][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane;
+  const bool live = e < E;
+  const int64_t per = (C + kXWarps - 1) / kXWarps;
+  const int64_t lo = warp * per;
+  const int64_t hi = lo + per < C ? lo + per : C;
+  int sum = 0;
+  if (live) {
+#pragma unroll 4
+    for (int64_t c = lo; c < hi; ++c) sum += ws.cnt[c * E + e];
+  }
+  s_part[warp][lane] = sum;
+  __syncthreads();
+  int run = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kXWarps; ++w) {
+    const int v = s_part[w][lane];
+    if (w < warp) run += v;
+    total += v;
+  }
+  if (live) {
+#pragma unroll 4
+    for (int64_t c = lo; c < hi; ++c) {
+      const int v = ws.cnt[c * E + e];
+      ws.cnt[c * E + e] = run;
+      run += v;
+    }
+    if (warp == 0) {
+      ws.tot[e] = total;
+      num_tokens_per_expert[e] = total;
+    }
+  }
+  pdl_launch_dependents();
+}
+
+// Chunk c: expert offsets from the totals, then the slots of its pairs.
+__global__ void __launch_bounds__(kXWarps * 32)
+    xlayout_assign_kernel(const int32_t* __restrict__ topk_idx, int64_t P, int E, XWs ws,
+                          int32_t* __restrict__ expert_offset, int32_t* __restrict__ slot) {
+  pdl_wait();
+  extern __shared__ int32_t s_dyn[];
+  int32_t* s_cnt = s_dyn;                  // [kXWarps][E]
+  int32_t* s_tot = s_cnt + kXWarps * E;    // [E]
+  int32_t* s_off = s_tot + E;              // [E + 1]
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t c = blockIdx.x;
+  const int64_t base = c * kXPairs + (int64_t)warp * kXGroups * 32;
+  int ids[kXGroups];
+  bool valid[kXGroups];
+  load_groups<kXGroups>(topk_idx, P, base, kXGroups, E, ids, valid);
+  for (int e = tid; e < E; e += blockDim.x) s_tot[e] = ws.tot[e];
+  for (int i = tid; i < kXWarps * E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  count_groups<kXGroups>(ids, valid, kXGroups, s_cnt + warp * E);
+  block_exclusive_scan(s_tot, s_off, E, s_warp);  // (synchronises)
+  if (c == 0)
+    for (int e = tid; e <= E; e += blockDim.x) expert_offset[e] = s_off[e];
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = s_off[e] + ws.cnt[c * E + e];
+#pragma unroll
+    for (int w = 0; w < kXWarps; ++w) {
+      const int v = s_cnt[w * E + e];
+      s_cnt[w * E + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  int row[kXGroups];
+  rank_groups<kXGroups>(ids, valid, kXGroups, s_cnt + warp * E, row);
+#pragma unroll
+  for (int i = 0; i < kXGroups; ++i) {
+    const int64_t p = base + (int64_t)i * 32 + lane;
+    if (p < P) slot[p] = row[i];
+  }
+  pdl_launch_dependents();
+}
+
+cudaError_t set_smem(const void* fn, size_t bytes, bool* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  if (done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
+}  // namespace
+
+int layout_experts_max_experts() { return kXMaxE; }
+
+size_t layout_experts_workspace_bytes(int64_t T, int k, int E) {
+  const int64_t P = T * k;
+  return a256(sizeof(int32_t) * (size_t)(x_chunks(P) * E)) + a256(sizeof(int32_t) * (size_t)E);
+}
+
+cudaError_t launch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,
+                                  int32_t* num_tokens_per_expert, int32_t* expert_offset,
+                                  int32_t* slot, void* workspace, int32_t* status,
+                                  cudaStream_t stream) {
+  const int64_t P = T * k;
+  if (P <= kXSingleMax && E <= kXSingleMaxE) {
+    static bool done[128];
+    const size_t most = sizeof(int32_t) * ((size_t)(kXSingleWarps + 2) * kXSingleMaxE + 1);
+    cudaError_t e = set_smem(reinterpret_cast<const void*>(xlayout_single_kernel), most, done);
+    if (e != cudaSuccess) return e;
+    const size_t smem = sizeof(int32_t) * ((size_t)(kXSingleWarps + 2) * E + 1);
+    return launch_pdl(xlayout_single_kernel, dim3(1), dim3(kXSingleWarps * 32), smem, stream,
+                      topk_idx, P, E, num_tokens_per_expert, expert_offset, slot, status);
+  }
+  const int64_t C = x_chunks(P);
+  const XWs ws = x_carve(workspace, P, E);
+  static bool done[128];
+  const size_t most = sizeof(int32_t) * ((size_t)(kXWarps + 2) * kXMaxE + 1);
+  cudaError_t e = set_smem(reinterpret_cast<const void*>(xlayout_assign_kernel), most, done);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(xlayout_count_kernel, dim3((unsigned)C), dim3(kXWarps * 32),
+                 sizeof(int32_t) * (size_t)E, stream, topk_idx, P, E, ws, status);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(xlayout_scan_kernel, dim3((unsigned)((E + 31) / 32)), dim3(kXWarps * 32), 0,
+                 stream, C, E, ws, num_tokens_per_expert);
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(int32_t) * ((size_t)(kXWarps + 2) * E + 1);
+  return launch_pdl(xlayout_assign_kernel, dim3((unsigned)C), dim3(kXWarps * 32), smem, stream,
+                    topk_idx, P, E, ws, expert_offset, slot);
+}
+
+}  // namespace ep

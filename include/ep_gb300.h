@@ -225,6 +225,61 @@ EP_API int ep_dispatch_layout_noalloc(const int32_t* topk_idx, int64_t T, int k,
                                       int32_t* rank_offset, int32_t* slot, int32_t* status,
                                       ep_stream_t stream);
 
+/*
+ * Expert-major layout: one receive row per valid (token, top-k column) pair,
+ * grouped by expert, for an expert side that runs one grouped GEMM over its
+ * experts.  Expert e owns rows [expert_offset[e], expert_offset[e+1]), the
+ * exclusive prefix sum of num_tokens_per_expert, and inside them the pairs
+ * come in (token, column) order; slot[t][j] is the row of pair (t, j), or -1
+ * when topk_idx[t][j] is outside [0, E) (then EP_STATUS_BAD_EXPERT is set).  A
+ * token that names one expert twice gets two rows.  The experts of rank r
+ * are r*Er .. (r+1)*Er - 1, so rank r's rows are the range
+ * [expert_offset[r*Er], expert_offset[(r+1)*Er]).  This is the per-expert
+ * receive layout of the recv kernel in "Optimizing Distributed Inference
+ * Kernels for AMD DEVELOPER CHALLENGE 2025", section 3.1 item 1, packed by a
+ * scan of the counts instead of a fixed per-expert maximum.
+ *
+ * The payload moves with ep_dispatch(..., W = k, slot, ...), which copies the
+ * token row to every row its slot table names (here one per valid column), and
+ * comes back with ep_combine_weighted(y, slot, topk_w, T, H, k, ...).
+ *
+ *  topk_idx               int32 [T, k]
+ *  num_tokens_per_expert  int32 [E]      valid pairs per expert
+ *  expert_offset          int32 [E + 1]  expert_offset[E] = number of rows
+ *  slot                   int32 [T, k]
+ *  workspace              >= ep_layout_experts_workspace_bytes(T, k, E) bytes,
+ *                         16-byte aligned, no initialisation
+ * Limits: 1 <= k; 1 <= E <= 4096; T * k < 2^31.  Up to 8192 pairs and 1024
+ * experts it is one kernel on one CTA, above that three kernels.
+ */
+EP_API size_t ep_layout_experts_workspace_bytes(int64_t T, int k, int E);
+EP_API int ep_dispatch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,
+                                      int32_t* num_tokens_per_expert, int32_t* expert_offset,
+                                      int32_t* slot, void* workspace, size_t workspace_bytes,
+                                      int32_t* status, ep_stream_t stream);
+
+/*
+ * Weighted combine over a slot table of C columns:
+ *   out[t] = bf16_rne( fma(w[t][c_n], y[s_n], ... fma(w[t][c_1], y[s_1], +0)) )
+ * over the columns c with s = slot[t][c] >= 0 in ascending order, each step one
+ * fp32 fused multiply-add (rounded once).  With the expert-major slot table and
+ * w = topk_w it is the gate-weighted sum of the token's expert outputs; with a
+ * rank-major slot table [T, W] and per-(token, rank) weights it is the weighted
+ * form of ep_combine, which it equals bit for bit when every weight is 1.
+ * Follows "perf(ep): optimize IntraNode dispatch kernel for MI350X", "Remaining
+ * gap" (combine accumulates the pre-routed rows with FMA).
+ *
+ *  y     bf16 [capacity_rows, H]   expert outputs, one per receive row
+ *  slot  int32 [T, C]
+ *  w     fp32 [T, C]               read only where slot >= 0
+ *  out   bf16 [T, H]
+ * Rows >= capacity_rows are skipped and set EP_STATUS_CAPACITY.
+ * Limits: H % 8 == 0; 1 <= C <= 32.
+ */
+EP_API int ep_combine_weighted(const void* y, const int32_t* slot, const float* w, int64_t T,
+                               int H, int C, int64_t capacity_rows, void* out, int32_t* status,
+                               ep_stream_t stream);
+
 /* Human-readable name of an EP_* return code (static string). */
 EP_API const char* ep_status_string(int code);
 

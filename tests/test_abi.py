@@ -134,6 +134,44 @@ def test_fused_rejects(lib, kw, code):
     assert rc == code
 
 
+@cpu_only
+@pytest.mark.parametrize("args,code", [
+    # (T, k, E, workspace_bytes, slot offset)
+    ((100, 8, 5000, 1 << 20, 0), _lib.EP_ERR_INVALID_ARG),      # E > 4096
+    ((100, 0, 256, 1 << 20, 0), _lib.EP_ERR_INVALID_ARG),       # k < 1
+    ((-3, 8, 256, 1 << 20, 0), _lib.EP_ERR_INVALID_ARG),        # T < 0
+    ((100000, 8, 256, 64, 0), _lib.EP_ERR_WORKSPACE),           # workspace too small
+    ((100, 8, 256, 1 << 20, 2), _lib.EP_ERR_MISALIGNED),        # slot 2-byte aligned
+    ((1 << 29, 8, 256, 1 << 40, 0), _lib.EP_ERR_UNSUPPORTED),   # rows overflow int32
+])
+def test_layout_experts_rejects(lib, args, code):
+    T, k, E, wsb, off = args
+    rc = lib.ep_dispatch_layout_experts(A, T, k, E, A, A, A + off, A, wsb, None, None)
+    assert rc == code
+
+
+def test_layout_experts_workspace_size(lib):
+    assert ep.ep_layout_experts_workspace_bytes(4096, 8, 256) >= 32 * 256 * 4 + 256 * 4
+    assert ep.ep_layout_experts_workspace_bytes(0, 8, 256) > 0
+    assert ep.ep_layout_experts_workspace_bytes(10, 0, 256) == 0
+
+
+@cpu_only
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=12), _lib.EP_ERR_UNSUPPORTED),
+    (dict(C=33), _lib.EP_ERR_INVALID_ARG),
+    (dict(C=0), _lib.EP_ERR_INVALID_ARG),
+    (dict(w_null=True), _lib.EP_ERR_INVALID_ARG),
+    (dict(w_off=2), _lib.EP_ERR_MISALIGNED),
+    (dict(y_off=4), _lib.EP_ERR_MISALIGNED),
+])
+def test_combine_weighted_rejects(lib, kw, code):
+    w = None if kw.get("w_null") else A + kw.get("w_off", 0)
+    rc = lib.ep_combine_weighted(A + kw.get("y_off", 0), A, w, 100, kw.get("H", 256), kw.get("C", 8),
+                                 800, A, None, None)
+    assert rc == code
+
+
 def test_binding_rejects_host_tensors(lib):
     idx = torch.zeros(4, 2, dtype=torch.int32)
     with pytest.raises(ValueError):

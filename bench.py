@@ -243,7 +243,7 @@ def run_ours(args) -> dict | None:
 
     # correctness guard of the timed configuration: identity experts give d_t * x
     with torch.cuda.stream(stream):
-        dc.combine(y, stream)
+        dc.combine(y, stream=stream)
     stream.synchronize()
     d = (dc.slot >= 0).sum(dim=1, keepdim=True).to(torch.float32)
     ok = torch.equal(dc.out, (x.float() * d).to(torch.bfloat16)) and int(dc.status.item()) == 0
@@ -259,7 +259,7 @@ def run_ours(args) -> dict | None:
         dc.dispatch(x, idx, w, stream)
         if events is not None and len(events) == 4:
             events[2].record(stream)
-        dc.combine(y, stream)
+        dc.combine(y, stream=stream)
         if events is not None:
             events[-1].record(stream)
 

@@ -8,6 +8,9 @@ namespace {
 #ifndef EP_COMBINE_U
 #define EP_COMBINE_U 2
 #endif
+#ifndef EP_COMBINE_SEG_F
+#define EP_COMBINE_SEG_F 4.0
+#endif
 
 constexpr int kCThreads = 256;
 
@@ -40,27 +43,36 @@ __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float wt, const uint
   acc[7] = __fmaf_rn(wt, __uint_as_float(v.w & 0xffff0000u), acc[7]);
 }
 
-// Lane l handles 16-byte chunks l, l+32, ... of the hidden dimension.  For a
-// round of U chunks the loads of up to 8 destination rows are all issued before
-// the first addition (8*U loads in flight per lane); the additions then run in
+// A warp takes one (token, segment) unit at a time: segment s of a token is
+// the 16-byte chunks [s * seg16, (s + 1) * seg16) of its hidden dimension, so
+// that small batches still give every SM enough warps (S segments per token).
+// Lane l handles chunks l, l+32, ... of the segment.  For a round of U chunks
+// the loads of up to 8 destination rows are all issued before the first
+// addition (8*U loads in flight per lane); the additions then run in
 // ascending column order, which fixes the rounding of the sum.  WEIGHTED:
 // each row enters as a fused multiply-add with the weight of its column,
 // w[t][c] ("perf(ep): optimize IntraNode dispatch kernel for MI350X",
 // Remaining gap: combine accumulates the rows with FMA).
-template <int U, bool WEIGHTED>
+template <int U, bool WEIGHTED, bool SEG>
 __global__ void __launch_bounds__(kCThreads)
     combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ slot,
-                   const float* __restrict__ w, int64_t T, int n16, int W, int64_t cap,
-                   uint4* __restrict__ out, int32_t* __restrict__ status) {
+                   const float* __restrict__ w, int64_t T, int n16, int S, int seg16, int W,
+                   int64_t cap, uint4* __restrict__ out, int32_t* __restrict__ status) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = ((int64_t)blockIdx.x * kCThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kCThreads) >> 5;
+  if constexpr (!SEG) S = 1;  // whole rows: the unit is the token
+  const int64_t units = T * S;
   bool cap_err = false;
-  int s_next = (gwarp < T && lane < W) ? __ldg(slot + gwarp * W + lane) : -1;
-  for (int64_t t = gwarp; t < T; t += nwarps) {
+  int s_next = (gwarp < units && lane < W) ? __ldg(slot + (SEG ? gwarp / S : gwarp) * W + lane) : -1;
+  for (int64_t un = gwarp; un < units; un += nwarps) {
+    const int64_t t = SEG ? un / S : un;
+    const int c_lo = SEG ? (int)(un - t * S) * seg16 : 0;
+    const int c_hi = SEG ? min(c_lo + seg16, n16) : n16;
     int s = s_next;
-    s_next = (t + nwarps < T && lane < W) ? __ldg(slot + (t + nwarps) * W + lane) : -1;
+    const int64_t un2 = un + nwarps;
+    s_next = (un2 < units && lane < W) ? __ldg(slot + (SEG ? un2 / S : un2) * W + lane) : -1;
 
     const bool keep = s >= 0 && (int64_t)s < cap;
     cap_err |= __any_sync(kFull, s >= 0 && (int64_t)s >= cap);
@@ -74,7 +86,7 @@ __global__ void __launch_bounds__(kCThreads)
       my_w = __shfl_sync(kFull, wl, r & 31);               // and its weight
     }
     uint4* dst = out + t * n16;
-    for (int c0 = 0; c0 < n16; c0 += 32 * U) {
+    for (int c0 = c_lo; c0 < c_hi; c0 += 32 * U) {
       float acc[U][8];
 #pragma unroll
       for (int u = 0; u < U; ++u)
@@ -95,7 +107,7 @@ __global__ void __launch_bounds__(kCThreads)
           for (int u = 0; u < U; ++u) {
             const int c = c0 + u * 32 + lane;
             v[q][u] = make_uint4(0u, 0u, 0u, 0u);
-            if (dg + q < nd && c < n16) v[q][u] = ld_stream_v4(y + (int64_t)rows[q] * n16 + c);
+            if (dg + q < nd && c < c_hi) v[q][u] = ld_stream_v4(y + (int64_t)rows[q] * n16 + c);
           }
         }
 #pragma unroll
@@ -114,7 +126,7 @@ __global__ void __launch_bounds__(kCThreads)
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int c = c0 + u * 32 + lane;
-        if (c < n16) {
+        if (c < c_hi) {
           const uint4 o = make_uint4(bf16x2_rn(acc[u][0], acc[u][1]), bf16x2_rn(acc[u][2], acc[u][3]),
                                      bf16x2_rn(acc[u][4], acc[u][5]), bf16x2_rn(acc[u][6], acc[u][7]));
           st_v4(dst + c, o);
@@ -138,15 +150,19 @@ __global__ void __launch_bounds__(kCThreads)
 // order, a stage is handed back as soon as it has been added, and no token has
 // to sit in shared memory whole: the ring only holds bytes in flight.
 // Whole-row copies and several issuing lanes keep the copy engine streaming.
-// Used for T <= EP_COMBINE_TMA_MAX_T: measured on GB300 (H=7168, top-8, W=8)
-// it wins where the register kernel has too few warps to keep loads in flight
-// (T=256: 14 us against 23 us), ties at T=1024 and loses from T=2048 on
-// (T=4096: 71 us against 66 us), where the register kernel takes over.
+// Used for EP_COMBINE_TMA_MIN_T <= T <= EP_COMBINE_TMA_MAX_T: measured on
+// GB300 (H=7168, top-8, W=8) it beats the register kernel at T=1024 (26 us
+// against 27-28 us) and loses at T=4096 (71 us against 66 us); below T=768 the
+// register kernel with row segments keeps more loads in flight (T=256: 12 us
+// against 14.8 us).
 #ifndef EP_COMBINE_TMA
 #define EP_COMBINE_TMA 1
 #endif
 #ifndef EP_COMBINE_TMA_MAX_T
 #define EP_COMBINE_TMA_MAX_T 1024
+#endif
+#ifndef EP_COMBINE_TMA_MIN_T
+#define EP_COMBINE_TMA_MIN_T 768
 #endif
 #ifndef EP_COMBINE_WARPS
 #define EP_COMBINE_WARPS 8
@@ -304,20 +320,36 @@ __global__ void __launch_bounds__((kCWarps + 1) * 32, 1)
 
 // One warp per token, as many CTAs as fit on the device at once (grid-stride
 // over the tokens beyond that).
-template <typename K>
-cudaError_t launch_combine_regs(K kern, const void* y, const int32_t* slot, const float* w,
-                                int64_t T, int H, int W, int64_t capacity_rows, void* out,
-                                int32_t* status, cudaStream_t stream) {
+template <typename K1, typename KS>
+cudaError_t launch_combine_regs(K1 kern_rows, KS kern_seg, const void* y, const int32_t* slot,
+                                const float* w, int64_t T, int H, int W, int64_t capacity_rows,
+                                void* out, int32_t* status, cudaStream_t stream) {
   int per_sm = 0;
+  auto kern = kern_seg;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCThreads, 0) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
-  const int64_t want = (T * 32 + kCThreads - 1) / kCThreads;
   const int64_t most = (int64_t)device_sm_count() * per_sm;
+  // Segments, when the batch has fewer tokens than the device has warp slots:
+  // enough (token, segment) units for EP_COMBINE_SEG_F units per slot, each
+  // segment at least one full round (32 * U chunks).  Measured on GB300 with
+  // H = 7168, top-8: T = 256 runs in 12 us instead of 17 us, T = 512 in 16 us
+  // instead of 22 us; from T = 4096 on whole rows are best.
+  const int n16 = H / 8;
+  const int64_t resident = most * (kCThreads / 32);
+  const int64_t target = (int64_t)(EP_COMBINE_SEG_F * (double)resident);
+  int64_t S = (T > 0 && T < resident) ? (target + T - 1) / T : 1;
+  const int64_t max_s = n16 / (32 * EP_COMBINE_U);
+  if (S > max_s) S = max_s;
+  if (S < 1) S = 1;
+  int seg16 = (int)((n16 + S - 1) / S);
+  seg16 = (seg16 + 31) & ~31;
+  S = (n16 + seg16 - 1) / seg16;
+  const int64_t want = (T * S * 32 + kCThreads - 1) / kCThreads;
   const int grid = (int)(want < most ? want : most);
-  return launch_pdl(kern, dim3(grid < 1 ? 1 : grid), dim3(kCThreads), 0, stream,
-                    static_cast<const uint4*>(y), slot, w, T, H / 8, W, capacity_rows,
-                    static_cast<uint4*>(out), status);
+  return launch_pdl(S > 1 ? kern_seg : kern_rows, dim3(grid < 1 ? 1 : grid), dim3(kCThreads), 0,
+                    stream, static_cast<const uint4*>(y), slot, w, T, n16, (int)S, seg16, W,
+                    capacity_rows, static_cast<uint4*>(out), status);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H, int W,
@@ -326,7 +358,7 @@ cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H,
   const uint32_t row_bytes = (uint32_t)H * 2u;
   // (a token's rows must fit the ring at once: W <= kCStages)
   if (EP_COMBINE_TMA && !EP_FORCE_LSU && row_bytes >= 1024 && W <= kCStages &&
-      T <= EP_COMBINE_TMA_MAX_T) {
+      T <= EP_COMBINE_TMA_MAX_T && T >= EP_COMBINE_TMA_MIN_T) {
     // chunks of at most one stage, equal up to 16 bytes
     const uint32_t nch = (row_bytes + kCStage - 1) / kCStage;
     const uint32_t chunk = ((row_bytes / nch + 15u) & ~15u);
@@ -346,7 +378,8 @@ cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H,
                       smem, stream, static_cast<const uint8_t*>(y), slot, T, row_bytes, chunk, W,
                       capacity_rows, static_cast<uint8_t*>(out), status);
   }
-  return launch_combine_regs(combine_kernel<EP_COMBINE_U, false>, y, slot, nullptr, T, H, W,
+  return launch_combine_regs(combine_kernel<EP_COMBINE_U, false, false>,
+                             combine_kernel<EP_COMBINE_U, false, true>, y, slot, nullptr, T, H, W,
                              capacity_rows, out, status, stream);
 }
 
@@ -354,7 +387,8 @@ cudaError_t launch_combine_weighted(const void* y, const int32_t* slot, const fl
                                     int H, int C, int64_t capacity_rows, void* out,
                                     int32_t* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  return launch_combine_regs(combine_kernel<EP_COMBINE_U, true>, y, slot, w, T, H, C,
+  return launch_combine_regs(combine_kernel<EP_COMBINE_U, true, false>,
+                             combine_kernel<EP_COMBINE_U, true, true>, y, slot, w, T, H, C,
                              capacity_rows, out, status, stream);
 }
 

@@ -31,7 +31,14 @@ constexpr int kXGroups = 4;                    // groups of 32 pairs per warp
 constexpr int kXPairs = kXWarps * kXGroups * 32;  // 1024 pairs per chunk
 constexpr int kXSingleWarps = 32;
 constexpr int kXSingleGroups = 8;
-constexpr int64_t kXSingleMax = kXSingleWarps * kXSingleGroups * 32;  // 8192 pairs
+#ifndef EP_XSINGLE_MAX
+#define EP_XSINGLE_MAX 2048
+#endif
+#ifndef EP_XMATCH_BALLOT
+#define EP_XMATCH_BALLOT 1
+#endif
+constexpr int64_t kXSingleMax = EP_XSINGLE_MAX;  // <= kXSingleWarps * kXSingleGroups * 32
+static_assert(kXSingleMax <= kXSingleWarps * kXSingleGroups * 32, "one CTA holds 8192 pairs");
 constexpr int kXSingleMaxE = 1024;
 constexpr int kXMaxE = 4096;
 
@@ -94,20 +101,36 @@ __device__ void block_exclusive_scan(const int32_t* s_val, int32_t* s_out, int n
   __syncthreads();
 }
 
+// Lanes whose pair has the same expert as this lane's (valid pairs only; an
+// invalid pair matches nobody and its result is not used).  With ballots: one
+// per bit of the expert id, nbits = bits of E - 1.
+__device__ __forceinline__ unsigned peers_of(int e, bool valid, int nbits) {
+#if EP_XMATCH_BALLOT
+  unsigned m = __ballot_sync(kFull, valid);
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (e >> b) & 1;
+    const unsigned v = __ballot_sync(kFull, bit);
+    m &= bit ? v : ~v;
+  }
+  return m;
+#else
+  (void)nbits;
+  return __match_any_sync(kFull, valid ? e : -1 - (int)(threadIdx.x & 31));
+#endif
+}
+
 // Ranks of a warp's pairs, in flat order, given s_run[e] = the first row of
 // expert e for this warp.  ids[i] is the expert of the lane's pair in group i
 // (valid[i] false for pairs that get no row).
 template <int G>
 __device__ __forceinline__ void rank_groups(const int (&ids)[G], const bool (&valid)[G], int ng,
-                                            int32_t* s_run, int (&row)[G]) {
-  const int lane = threadIdx.x & 31;
+                                            int nbits, int32_t* s_run, int (&row)[G]) {
   const unsigned lt = lanemask_lt();
 #pragma unroll
   for (int i = 0; i < G; ++i) {
     row[i] = -1;
     if (i < ng) {
-      const int key = valid[i] ? ids[i] : -1 - lane;  // invalid pairs match nobody
-      const unsigned peers = __match_any_sync(kFull, key);
+      const unsigned peers = peers_of(ids[i], valid[i], nbits);
       if (valid[i]) row[i] = s_run[ids[i]] + __popc(peers & lt);
       __syncwarp();
       if (valid[i] && (peers & lt) == 0) s_run[ids[i]] += __popc(peers);
@@ -119,14 +142,12 @@ __device__ __forceinline__ void rank_groups(const int (&ids)[G], const bool (&va
 // Per-warp counts of experts, added to s_cnt[e] (this warp's row).
 template <int G>
 __device__ __forceinline__ void count_groups(const int (&ids)[G], const bool (&valid)[G], int ng,
-                                             int32_t* s_cnt) {
-  const int lane = threadIdx.x & 31;
+                                             int nbits, int32_t* s_cnt) {
   const unsigned lt = lanemask_lt();
 #pragma unroll
   for (int i = 0; i < G; ++i) {
     if (i < ng) {
-      const int key = valid[i] ? ids[i] : -1 - lane;
-      const unsigned peers = __match_any_sync(kFull, key);
+      const unsigned peers = peers_of(ids[i], valid[i], nbits);
       if (valid[i] && (peers & lt) == 0) s_cnt[ids[i]] += __popc(peers);
       __syncwarp();
     }
@@ -154,7 +175,7 @@ __device__ __forceinline__ bool load_groups(const int32_t* __restrict__ topk_idx
 
 // One CTA, all pairs (P <= kXSingleMax, E <= kXSingleMaxE).
 __global__ void __launch_bounds__(kXSingleWarps * 32, 1)
-    xlayout_single_kernel(const int32_t* __restrict__ topk_idx, int64_t P, int E,
+    xlayout_single_kernel(const int32_t* __restrict__ topk_idx, int64_t P, int E, int nbits,
                           int32_t* __restrict__ num_tokens_per_expert,
                           int32_t* __restrict__ expert_offset, int32_t* __restrict__ slot,
                           int32_t* __restrict__ status) {
@@ -173,7 +194,7 @@ __global__ void __launch_bounds__(kXSingleWarps * 32, 1)
   if (__any_sync(kFull, bad) && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_BAD_EXPERT);
   for (int i = tid; i < kXSingleWarps * E; i += blockDim.x) s_cnt[i] = 0;
   __syncthreads();
-  count_groups<kXSingleGroups>(ids, valid, ng, s_cnt + warp * E);
+  count_groups<kXSingleGroups>(ids, valid, ng, nbits, s_cnt + warp * E);
   __syncthreads();
   // per expert: exclusive prefix over the warps (in place) and the total
   for (int e = tid; e < E; e += blockDim.x) {
@@ -196,7 +217,7 @@ __global__ void __launch_bounds__(kXSingleWarps * 32, 1)
   }
   __syncthreads();
   int row[kXSingleGroups];
-  rank_groups<kXSingleGroups>(ids, valid, ng, s_cnt + warp * E, row);
+  rank_groups<kXSingleGroups>(ids, valid, ng, nbits, s_cnt + warp * E, row);
 #pragma unroll
   for (int i = 0; i < kXSingleGroups; ++i) {
     const int64_t p = base + (int64_t)i * 32 + lane;
@@ -275,7 +296,7 @@ __global__ void __launch_bounds__(kXWarps * 32)
 
 // Chunk c: expert offsets from the totals, then the slots of its pairs.
 __global__ void __launch_bounds__(kXWarps * 32)
-    xlayout_assign_kernel(const int32_t* __restrict__ topk_idx, int64_t P, int E, XWs ws,
+    xlayout_assign_kernel(const int32_t* __restrict__ topk_idx, int64_t P, int E, int nbits, XWs ws,
                           int32_t* __restrict__ expert_offset, int32_t* __restrict__ slot) {
   pdl_wait();
   extern __shared__ int32_t s_dyn[];
@@ -292,7 +313,7 @@ __global__ void __launch_bounds__(kXWarps * 32)
   for (int e = tid; e < E; e += blockDim.x) s_tot[e] = ws.tot[e];
   for (int i = tid; i < kXWarps * E; i += blockDim.x) s_cnt[i] = 0;
   __syncthreads();
-  count_groups<kXGroups>(ids, valid, kXGroups, s_cnt + warp * E);
+  count_groups<kXGroups>(ids, valid, kXGroups, nbits, s_cnt + warp * E);
   block_exclusive_scan(s_tot, s_off, E, s_warp);  // (synchronises)
   if (c == 0)
     for (int e = tid; e <= E; e += blockDim.x) expert_offset[e] = s_off[e];
@@ -307,7 +328,7 @@ __global__ void __launch_bounds__(kXWarps * 32)
   }
   __syncthreads();
   int row[kXGroups];
-  rank_groups<kXGroups>(ids, valid, kXGroups, s_cnt + warp * E, row);
+  rank_groups<kXGroups>(ids, valid, kXGroups, nbits, s_cnt + warp * E, row);
 #pragma unroll
   for (int i = 0; i < kXGroups; ++i) {
     const int64_t p = base + (int64_t)i * 32 + lane;
@@ -341,6 +362,8 @@ cudaError_t launch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int
                                   int32_t* slot, void* workspace, int32_t* status,
                                   cudaStream_t stream) {
   const int64_t P = T * k;
+  int nbits = 0;  // bits of the largest valid id
+  while ((1 << nbits) < E) ++nbits;
   if (P <= kXSingleMax && E <= kXSingleMaxE) {
     static bool done[128];
     const size_t most = sizeof(int32_t) * ((size_t)(kXSingleWarps + 2) * kXSingleMaxE + 1);
@@ -348,7 +371,7 @@ cudaError_t launch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int
     if (e != cudaSuccess) return e;
     const size_t smem = sizeof(int32_t) * ((size_t)(kXSingleWarps + 2) * E + 1);
     return launch_pdl(xlayout_single_kernel, dim3(1), dim3(kXSingleWarps * 32), smem, stream,
-                      topk_idx, P, E, num_tokens_per_expert, expert_offset, slot, status);
+                      topk_idx, P, E, nbits, num_tokens_per_expert, expert_offset, slot, status);
   }
   const int64_t C = x_chunks(P);
   const XWs ws = x_carve(workspace, P, E);
@@ -364,7 +387,7 @@ cudaError_t launch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(int32_t) * ((size_t)(kXWarps + 2) * E + 1);
   return launch_pdl(xlayout_assign_kernel, dim3((unsigned)C), dim3(kXWarps * 32), smem, stream,
-                    topk_idx, P, E, ws, expert_offset, slot);
+                    topk_idx, P, E, nbits, ws, expert_offset, slot);
 }
 
 }  // namespace ep

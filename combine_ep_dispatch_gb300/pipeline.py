@@ -13,24 +13,45 @@ from . import _lib
 class DispatchCombine:
     """Buffers for T tokens of hidden size H routed top-k over E experts on W ranks.
 
-    ``capacity_rows`` defaults to the worst case T * min(k, W), so dispatch can
-    never overflow.  ``quant`` selects the dispatch payload (bf16 or FP8 e4m3
-    with 1x128 block scales); combine always reads bf16 expert outputs.
+    ``order`` picks the receive layout:
+      - "rank" (default): one row per (token, destination rank), the token's
+        experts on a rank share it; combine sums a token's rows unweighted (or
+        with per-(token, rank) weights given to ``combine``);
+      - "expert": one row per valid (token, expert) pair, rows grouped by
+        expert (``expert_offset``), for a grouped expert GEMM; combine takes
+        the gate weights ``topk_w`` and forms their FMA-weighted sum.
+    ``capacity_rows`` defaults to the worst case (T * min(k, W), or T * k for
+    "expert"), so dispatch can never overflow.  ``quant`` selects the dispatch
+    payload (bf16 or FP8 e4m3 with 1x128 block scales); combine always reads
+    bf16 expert outputs.
     """
 
     def __init__(self, T: int, H: int, E: int, k: int, W: int, capacity_rows: int | None = None,
-                 quant: int = _lib.EP_QUANT_BF16, device: str | torch.device = "cuda"):
+                 quant: int = _lib.EP_QUANT_BF16, device: str | torch.device = "cuda",
+                 order: str = "rank"):
+        if order not in ("rank", "expert"):
+            raise ValueError(f"order must be 'rank' or 'expert', got {order!r}")
         self.T, self.H, self.E, self.k, self.W, self.quant = T, H, E, k, W, quant
+        self.order = order
         dev = torch.device(device)
-        cap = _lib.ep_max_recv_rows(T, k, W) if capacity_rows is None else capacity_rows
+        worst = T * k if order == "expert" else _lib.ep_max_recv_rows(T, k, W)
+        cap = worst if capacity_rows is None else capacity_rows
         self.capacity_rows = cap
         i32 = dict(dtype=torch.int32, device=dev)
         self.num_tokens_per_expert = torch.empty(E, **i32)
-        self.num_tokens_per_rank = torch.empty(W, **i32)
-        self.rank_offset = torch.empty(W + 1, **i32)
-        self.slot = torch.empty(T, W, **i32)
-        self.workspace = torch.empty(max(_lib.ep_layout_workspace_bytes(T, W, E), 16),
-                                     dtype=torch.uint8, device=dev)
+        if order == "rank":
+            self.num_tokens_per_rank = torch.empty(W, **i32)
+            self.rank_offset = torch.empty(W + 1, **i32)
+            self.expert_offset = None
+            self.slot = torch.empty(T, W, **i32)
+            ws = _lib.ep_layout_workspace_bytes(T, W, E)
+        else:
+            self.num_tokens_per_rank = None
+            self.rank_offset = None
+            self.expert_offset = torch.empty(E + 1, **i32)
+            self.slot = torch.empty(T, k, **i32)
+            ws = _lib.ep_layout_experts_workspace_bytes(T, k, E)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         if quant == _lib.EP_QUANT_BF16:
             self.recv_x = torch.empty(cap, H, dtype=torch.bfloat16, device=dev)
             self.recv_scale = None
@@ -44,35 +65,51 @@ class DispatchCombine:
         self.status = torch.zeros(1, **i32)
 
     def layout(self, topk_idx: torch.Tensor, stream=None) -> None:
-        _lib.ep_dispatch_layout(topk_idx, self.E, self.W, self.num_tokens_per_expert,
-                                self.num_tokens_per_rank, self.rank_offset, self.slot,
-                                self.workspace, self.status, stream)
+        if self.order == "rank":
+            _lib.ep_dispatch_layout(topk_idx, self.E, self.W, self.num_tokens_per_expert,
+                                    self.num_tokens_per_rank, self.rank_offset, self.slot,
+                                    self.workspace, self.status, stream)
+        else:
+            _lib.ep_dispatch_layout_experts(topk_idx, self.E, self.num_tokens_per_expert,
+                                            self.expert_offset, self.slot, self.workspace,
+                                            self.status, stream)
 
     def dispatch(self, x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
                  stream=None) -> None:
-        _lib.ep_dispatch(x, topk_idx, topk_w, self.W, self.slot, self.recv_x, self.recv_topk_idx,
-                         self.recv_topk_w, self.recv_src, self.recv_scale, self.quant, self.status,
-                         stream)
+        _lib.ep_dispatch(x, topk_idx, topk_w, self.slot.shape[1], self.slot, self.recv_x,
+                         self.recv_topk_idx, self.recv_topk_w, self.recv_src, self.recv_scale,
+                         self.quant, self.status, stream)
 
     def dispatch_fused(self, x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
                        stream=None) -> None:
-        """layout() and dispatch() in one launch (bf16, T <= EP_FUSED_MAX_TOKENS)."""
+        """layout() and dispatch() in one launch (rank order, bf16, T <= EP_FUSED_MAX_TOKENS)."""
+        if self.order != "rank":
+            raise ValueError("dispatch_fused builds the rank-major layout")
         _lib.ep_dispatch_fused(x, topk_idx, topk_w, self.E, self.W, self.num_tokens_per_expert,
                                self.num_tokens_per_rank, self.rank_offset, self.slot, self.recv_x,
                                self.recv_topk_idx, self.recv_topk_w, self.recv_src, self.status,
                                stream)
 
-    def combine(self, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-        """Sum each token's expert outputs ``y`` (default: the dispatched rows,
-        i.e. identity experts; bf16 dispatch only) into ``self.out``."""
+    def combine(self, y: torch.Tensor | None = None, w: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+        """Bring each token's expert outputs ``y`` (default: the dispatched rows,
+        i.e. identity experts; bf16 dispatch only) back into ``self.out``.
+        ``w`` has the slot table's shape: per-(token, rank) weights for "rank"
+        (optional: without it the sum is unweighted), the gate weights topk_w
+        for "expert" (required)."""
         if y is None:
             if self.quant != _lib.EP_QUANT_BF16:
                 raise ValueError("identity experts need a bf16 dispatch")
             y = self.recv_x
-        _lib.ep_combine(y, self.slot, self.out, self.status, stream)
+        if w is None and self.order == "expert":
+            raise ValueError("the expert-major combine needs the gate weights")
+        if w is None:
+            _lib.ep_combine(y, self.slot, self.out, self.status, stream)
+        else:
+            _lib.ep_combine_weighted(y, self.slot, w, self.out, self.status, stream)
         return self.out
 
     def step(self, x, topk_idx, topk_w, y=None, stream=None) -> torch.Tensor:
         self.layout(topk_idx, stream)
         self.dispatch(x, topk_idx, topk_w, stream)
-        return self.combine(y, stream)
+        return self.combine(y, topk_w if self.order == "expert" else None, stream)

@@ -6,7 +6,10 @@ needs:
   python -m combine_ep_dispatch_gb300.run_step --workload dsv3 --iters 3
 
 Combine reads the dispatched rows (identity experts; for the FP8 workload a
-bf16 dispatch of the same routing provides them).
+bf16 dispatch of the same routing provides them).  --order expert runs the
+expert-major path (one row per (token, expert) pair, combine weighted by the
+gate weights); --fused uses the one-launch layout + dispatch (rank order,
+bf16, small batches).
 """
 from __future__ import annotations
 
@@ -25,6 +28,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="dsv3", choices=sorted(CONFIGS))
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--order", default="rank", choices=("rank", "expert"))
+    ap.add_argument("--fused", action="store_true")
     args = ap.parse_args(argv)
 
     inp = make_inputs(args.workload, seed=args.seed)
@@ -34,22 +39,29 @@ def main(argv=None):
     idx = torch.from_numpy(inp["topk_idx"]).to(dev)
     w = torch.from_numpy(inp["topk_w"]).to(dev)
     quant = _lib.EP_QUANT_FP8_E4M3_B128 if cfg.quant == "fp8" else _lib.EP_QUANT_BF16
-    probe = DispatchCombine(cfg.T, 8, cfg.E, cfg.k, cfg.W, capacity_rows=0, device=dev)
+    order = args.order
+    probe = DispatchCombine(cfg.T, 8, cfg.E, cfg.k, cfg.W, capacity_rows=0, device=dev,
+                            order=order)
     probe.layout(idx)
-    R = int(probe.rank_offset[cfg.W].item())
+    R = int(probe.rank_offset[cfg.W].item() if order == "rank" else
+            probe.expert_offset[cfg.E].item())
     dc = DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, capacity_rows=R, quant=quant,
-                         device=dev)
+                         device=dev, order=order)
     ident = dc if quant == _lib.EP_QUANT_BF16 else DispatchCombine(
-        cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, capacity_rows=R, device=dev)
+        cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, capacity_rows=R, device=dev, order=order)
+    weights = w if order == "expert" else None
     for _ in range(args.iters):
-        dc.layout(idx)
-        dc.dispatch(x, idx, w)
+        if args.fused:
+            dc.dispatch_fused(x, idx, w)
+        else:
+            dc.layout(idx)
+            dc.dispatch(x, idx, w)
         if ident is not dc:
             ident.layout(idx)
             ident.dispatch(x, idx, w)
-        dc.combine(ident.recv_x)
+        dc.combine(ident.recv_x, weights)
     torch.cuda.synchronize()
-    print(f"{args.workload}: T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} W={cfg.W} R={R} "
+    print(f"{args.workload} ({order}{', fused' if args.fused else ''}): T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} W={cfg.W} R={R} "
           f"iters={args.iters} status={int(dc.status.item())}")
 
 

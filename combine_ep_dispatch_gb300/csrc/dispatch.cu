@@ -87,6 +87,14 @@ constexpr int kTmaStages = EP_TMA_STAGES;            // row buffers per warp
 constexpr int kTmaBarBytes = 1024;                   // barrier area ahead of the row buffers
 constexpr int kTmaSmemBudget = EP_TMA_SMEM_BUDGET;   // row buffers per CTA
 constexpr int kTmaMaxWarps = EP_TMA_MAX_WARPS;
+// L2 priority of the received rows (0: none, 1: evict_first, 2: evict_last).
+// evict_last keeps the rows just written in L2 for their consumer (the expert
+// GEMM reads them next) and moves part of their write-back out of this kernel:
+// measured on GB300 it shortens the layout + dispatch + combine step by 1.3 to
+// 2.5 us at T=4096 (H=7168) and T=8192 (H=4096); evict_first changed nothing.
+#ifndef EP_TMA_STORE_HINT
+#define EP_TMA_STORE_HINT 2
+#endif
 constexpr int kTmaCtasPerSm = EP_TMA_CTAS_PER_SM;
 constexpr uint32_t kTmaMinRowBytes = 1024;  // smaller rows: 16-byte stores from registers
 
@@ -158,7 +166,13 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
       timed_out = true;
       break;
     }
+#if EP_TMA_STORE_HINT
+    if (lane < nd)
+      bulk_store_hint(recv_x + (int64_t)my_row * row_bytes, buf + st * stage_bytes, row_bytes,
+                      make_l2_policy<EP_TMA_STORE_HINT>());
+#else
     if (lane < nd) bulk_store(recv_x + (int64_t)my_row * row_bytes, buf + st * stage_bytes, row_bytes);
+#endif
     bulk_commit();
 #else
     bool ok = true;

@@ -151,6 +151,27 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uin
                : "memory");
 }
 
+// The same with an L2 eviction-priority hint (a policy from make_l2_policy).
+__device__ __forceinline__ void bulk_store_hint(void* gdst, const void* smem_src, uint32_t bytes,
+                                                uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
+               "r"(smem_u32(smem_src)), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+// L2 policy: 1 = evict_first, 2 = evict_last, 3 = evict_unchanged (whole access).
+template <int KIND>
+__device__ __forceinline__ uint64_t make_l2_policy() {
+  uint64_t p;
+  if constexpr (KIND == 1)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  else if constexpr (KIND == 2)
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_unchanged.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N of this thread's bulk groups still read shared memory.

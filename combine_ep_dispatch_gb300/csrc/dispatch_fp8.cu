@@ -17,57 +17,60 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 }
 
 
-__device__ __forceinline__ float rcp_approx(float s) {
-  float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
+// max(|a|, |b|) per bf16 half (the sign bit of each half is the xor of the
+// operands' signs and is cleared at the end).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 
-// Largest |x| of the 16 bf16 values in w[0..7], as fp32 (exact).
+// Largest |x| of the 16 bf16 values in w[0..7], as fp32 (exact): a tree of
+// packed |max| operations, then the larger half.
 __device__ __forceinline__ float bf16x16_absmax(const uint32_t (&w)[8]) {
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t a = w[i] & 0x7fff7fffu, r;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(m));  // |x| >= 0: order of the values
-    m = r;
-  }
+  const uint32_t m01 = absmax_bf16x2(w[0], w[1]), m23 = absmax_bf16x2(w[2], w[3]);
+  const uint32_t m45 = absmax_bf16x2(w[4], w[5]), m67 = absmax_bf16x2(w[6], w[7]);
+  const uint32_t m = absmax_bf16x2(absmax_bf16x2(m01, m23), absmax_bf16x2(m45, m67)) & 0x7fff7fffu;
   const uint32_t hi = m >> 16, lo = m & 0xffffu;
   return __uint_as_float((hi > lo ? hi : lo) << 16);
 }
 
+// fl(v / s), the IEEE quotient rounded to nearest even, from y = RN(1/s)
+// with fused multiply-adds: a first quotient q0 = RN(v y) lies within 1.5 ulp
+// of v / s, one correction q1 = RN(q0 + (v - s q0) y) brings it within one
+// ulp, and a second correction of q1 is the correctly rounded quotient by
+// Markstein's theorem (P. Markstein, IBM J. Res. Dev. 34(1), 1990: with y
+// within half an ulp of 1/s and q within one ulp of v/s, the residual
+// v - s q is exact and RN(q + (v - s q) y) = RN(v / s)).  The residual is
+// formed as s q - v and subtracted, which keeps the sign of a zero quotient.
+// Valid while nothing underflows or overflows: 2^-80 <= s <= 2^100 (a quotient
+// too small for that has an e4m3 code of zero either way).
+__device__ __forceinline__ float quotient_rn(float v, float s, float y) {
+  float q = __fmul_rn(v, y);
+  float r = __fmaf_rn(s, q, -v);
+  q = __fmaf_rn(-r, y, q);
+  r = __fmaf_rn(s, q, -v);
+  return __fmaf_rn(-r, y, q);
+}
+
 // e4m3 codes of the 16 bf16 values in w[0..7] (element 2i in the low half of
-// w[i]) divided by s > 0, packed little-endian into 16 bytes: exactly the code
-// of the IEEE-rounded fp32 quotient fl(v/s) rounded to e4m3 (nearest, ties to
-// even, saturating to +-448), without a division per value.
-//
-// The code is a monotonic function of the quotient.  With r = rcp.approx(s)
-// (at most 1 ulp from 1/s), fl(v/s) lies between v*r*(1 - 2^-18) and
-// v*r*(1 + 2^-18) -- their distance from v/s is some thirty times the combined
-// rounding of r and of the products -- so when those two bracket values give
-// the same code, it is the code of fl(v/s).  When they differ, a rounding
-// boundary of e4m3 lies inside the bracket (a few values in 10^5 for normally
-// distributed rows) and the IEEE division decides.  A subnormal s or a
-// non-finite 1/s sends every value to the division.
-__device__ __forceinline__ uint4 e4m3x16_of_quotients(const uint32_t (&w)[8], float s) {
-  const float r = rcp_approx(s);
-  const bool fast = s >= 1.17549435e-38f && r < 3.0e38f;
-  const float r_lo = r * (1.0f - 0x1p-18f), r_hi = r * (1.0f + 0x1p-18f);
+// w[i]) divided by s > 0, packed little-endian into 16 bytes: the code of the
+// IEEE-rounded fp32 quotient fl(v/s) rounded to e4m3 (nearest, ties to even,
+// saturating to +-448).  y = RN(1/s).  Scales outside [2^-80, 2^100] take the
+// IEEE division per value.
+__device__ __forceinline__ uint4 e4m3x16_of_quotients(const uint32_t (&w)[8], float s, float y) {
   uint32_t c[8];
-  uint32_t slow = fast ? 0u : 0xffu;
+  if (s >= 0x1p-80f && s <= 0x1p100f) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xffff0000u);
-    const uint32_t lo = e4m3x2(a * r_lo, b * r_lo), hi = e4m3x2(a * r_hi, b * r_hi);
-    c[i] = lo;
-    slow |= (lo != hi ? 1u : 0u) << i;
-  }
-  if (slow) {
+    for (int i = 0; i < 8; ++i) {
+      const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xffff0000u);
+      c[i] = e4m3x2(quotient_rn(a, s, y), quotient_rn(b, s, y));
+    }
+  } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (slow & (1u << i))
-        c[i] = e4m3x2(__fdiv_rn(__uint_as_float(w[i] << 16), s),
-                      __fdiv_rn(__uint_as_float(w[i] & 0xffff0000u), s));
+      c[i] = e4m3x2(__fdiv_rn(__uint_as_float(w[i] << 16), s),
+                    __fdiv_rn(__uint_as_float(w[i] & 0xffff0000u), s));
   }
   return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16),
                     c[6] | (c[7] << 16));
@@ -87,19 +90,19 @@ __global__ void __launch_bounds__(kDThreads)
                         const int32_t* __restrict__ slot, int64_t cap, uint8_t* __restrict__ recv_x,
                         float* __restrict__ recv_scale, int32_t* __restrict__ recv_topk_idx,
                         float* __restrict__ recv_topk_w, int32_t* __restrict__ recv_src,
-                        int nseg, int32_t* __restrict__ status) {
+                        int nseg, int per_seg, int32_t* __restrict__ status) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int qb = lane >> 3, hl = lane & 7;  // block within the quad, lane within the block
   const int nb = H >> 7;
   const int n16 = H >> 3;
   const int nquad = (nb + 3) >> 2;
-  const int per_seg = (nquad + nseg - 1) / nseg;
   const int64_t gwarp = ((int64_t)blockIdx.x * kDThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kDThreads) >> 5;
+  const bool narrow = T * nseg < 0x7fffffffLL;  // 32-bit unit arithmetic suffices
   bool cap_err = false;
   for (int64_t u = gwarp; u < T * nseg; u += nwarps) {
-    const int64_t t = u / nseg;
+    const int64_t t = narrow ? (int64_t)((uint32_t)u / (uint32_t)nseg) : u / nseg;
     const int seg = (int)(u - t * nseg);
     const Dests d = token_dests(slot, t, W, cap, lane);
     if (seg == 0) {
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kDThreads)
         for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
         const float s = __fdiv_rn(m, 448.0f);
         sc[v] = s;
-        codes[v] = s != 0.0f ? e4m3x16_of_quotients(w, s) : make_uint4(0u, 0u, 0u, 0u);
+        codes[v] = s != 0.0f ? e4m3x16_of_quotients(w, s, __frcp_rn(s)) : make_uint4(0u, 0u, 0u, 0u);
       }
       // the lane's byte offsets in a row, and whether each of its blocks exists
       bool has[U];
@@ -175,6 +178,10 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
   const int nquad = (H / 128 + 3) / 4;
   int nseg = (int)((2 * warps + T - 1) / T);
   nseg = nseg < 1 ? 1 : (nseg > nquad ? nquad : nseg);
+  // segments of whole rounds of 2 quads (the kernel's unroll: no half-empty
+  // rounds), and no empty segments
+  const int per_seg = ((nquad + nseg - 1) / nseg + 1) / 2 * 2;
+  nseg = (nquad + per_seg - 1) / per_seg;
   const int64_t units = T * nseg;
   const int64_t grid = (units * 32 + kDThreads - 1) / kDThreads < device_sm_count() * per_sm
                            ? (units * 32 + kDThreads - 1) / kDThreads
@@ -182,7 +189,7 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
   return launch_pdl(kern, dim3((unsigned)(grid < 1 ? 1 : grid)), dim3(kDThreads), 0, stream, x4,
                     topk_idx, topk_w, T, H, k, W, slot, capacity_rows,
                     static_cast<uint8_t*>(recv_x), recv_scale, recv_topk_idx, recv_topk_w, recv_src,
-                    nseg, status);
+                    nseg, per_seg, status);
 }
 
 }  // namespace ep

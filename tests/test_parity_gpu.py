@@ -261,6 +261,33 @@ def test_fp8_values_at_e4m3_rounding_boundaries():
     _check_dispatch({"x": x, "topk_idx": idx, "topk_w": w}, lay, T, ep.EP_QUANT_FP8_E4M3_B128)
 
 
+def test_fp8_every_significand_ratio():
+    """bf16 values have 8-bit significands, so x / scale = 448 * x / amax lands
+    exactly on e4m3 midpoints far more often than real-valued data would.  One
+    block per (amax significand, exponent gap d, sign pattern): the amax is
+    m_a * 2^E, the other 127 values are every other significand m * 2^(E - d),
+    so every significand ratio m / m_a at 13 gaps is quantised once."""
+    rng = np.random.default_rng(24)
+    blocks = []
+    mant = np.arange(128, 256, dtype=np.float64)
+    for m_a in range(128, 256):
+        for d in range(0, 13):
+            E = int(rng.integers(-30, 30))
+            vals = mant * 2.0 ** (E - 7 - d)              # m * 2^(E - d), with m/128 in [1, 2)
+            vals = vals[vals != m_a * 2.0 ** (E - 7 - d)] if d == 0 else vals[:127]
+            vals = vals[:127]
+            blk = np.concatenate([[m_a * 2.0 ** (E - 7)], vals])
+            sign = np.where(rng.random(128) < 0.5, -1.0, 1.0)
+            blocks.append(blk * sign)
+    xs = np.array(blocks, np.float32).reshape(-1, 1024)  # 8 blocks per row
+    x = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    T = x.shape[0]
+    idx = np.zeros((T, 1), np.int32)
+    w = np.ones((T, 1), np.float32)
+    lay = _check_layout(idx, 1, 1)
+    _check_dispatch({"x": x, "topk_idx": idx, "topk_w": w}, lay, T, ep.EP_QUANT_FP8_E4M3_B128)
+
+
 def test_invalid_expert_ids_are_ignored_and_flagged():
     rng = np.random.default_rng(31)
     T, E, k, W, H = 500, 64, 6, 8, 256

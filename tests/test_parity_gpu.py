@@ -13,7 +13,7 @@ import oracle
 from combine_ep_dispatch_gb300.inputs import (CONFIGS, f32_from_bf16_bits, make_bf16, make_inputs,
                                               make_routing)
 from gpu_util import (SENT_BF16, SENT_I32, SENT_U8, assert_rows_equal, run_combine, run_dispatch,
-                      run_layout)
+                      run_layout, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -187,6 +187,49 @@ def test_shapes_fp8(T, H, E, k, W):
     lay = _check_layout(idx, E, W)
     _check_dispatch({"x": x, "topk_idx": idx, "topk_w": w}, lay, int(lay["rank_offset"][-1]),
                     ep.EP_QUANT_FP8_E4M3_B128)
+
+
+@pytest.mark.parametrize("T,H,E,k,W", [(2048, 7168, 256, 8, 8), (3001, 512, 64, 6, 8),
+                                       (4096, 1024, 64, 16, 32), (2500, 2048, 96, 5, 3),
+                                       (6000, 4096, 128, 8, 8)])
+def test_fp8_large_batches(T, H, E, k, W):
+    """Large FP8 batches, ragged and Zipf-skewed, with and without a capacity
+    overflow."""
+    rng = np.random.default_rng(T * 3 + H)
+    x = make_bf16(rng, (T, H), scale=5.0)
+    idx = make_routing(rng, T, E, k, "zipf" if T % 2 else "uniform")
+    w = rng.random((T, k), dtype=np.float32)
+    lay = _check_layout(idx, E, W)
+    R = int(lay["rank_offset"][-1])
+    _check_dispatch({"x": x, "topk_idx": idx, "topk_w": w}, lay, R, ep.EP_QUANT_FP8_E4M3_B128)
+    want, got = _check_dispatch({"x": x, "topk_idx": idx, "topk_w": w}, lay, R - 300,
+                                ep.EP_QUANT_FP8_E4M3_B128)
+    assert got["status"] & ep.EP_STATUS_CAPACITY
+
+
+def test_fp8_large_batch_unaligned_scales():
+    """recv_scale only 4-byte aligned (the C ABI's rule for index and scale
+    arrays): every scale lands at its place."""
+    rng = np.random.default_rng(44)
+    T, H, E, k, W = 3000, 1024, 64, 8, 8
+    x = make_bf16(rng, (T, H))
+    idx = make_routing(rng, T, E, k)
+    w = rng.random((T, k), dtype=np.float32)
+    lay = oracle.layout(idx, E, W)
+    R = int(lay["rank_offset"][-1])
+    want = oracle.dispatch(x, idx, w, lay["slot"], R, ep.EP_QUANT_FP8_E4M3_B128)
+    nb = H // 128
+    flat = torch.full((R * nb + 1,), -7.0, dtype=torch.float32, device="cuda")
+    rs = flat[1:].view(R, nb)
+    rx = torch.full((R, H), 0xA5, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_dispatch(to_dev_bf16(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(), W,
+                   torch.from_numpy(lay["slot"]).cuda(), rx, None, None, None, rs,
+                   ep.EP_QUANT_FP8_E4M3_B128, st)
+    torch.cuda.synchronize()
+    assert_rows_equal(rx.cpu().numpy(), want["recv_x"], "recv_x")
+    assert_rows_equal(rs.cpu().numpy().view(np.uint32), want["recv_scale"].view(np.uint32), "recv_scale")
+    assert int(st.item()) == 0
 
 
 def test_fp8_special_blocks():

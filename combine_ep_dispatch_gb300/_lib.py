@@ -31,7 +31,7 @@ EP_QUANT_FP8_E4M3_B128 = 1
 EXPORTED = ("ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_dispatch_layout", "ep_dispatch",
             "ep_combine", "ep_status_string", "ep_dispatch_layout_noalloc", "ep_dispatch_fused",
             "ep_localize_expert_ids", "ep_layout_experts_workspace_bytes",
-            "ep_dispatch_layout_experts", "ep_combine_weighted")
+            "ep_dispatch_layout_experts", "ep_combine_weighted", "ep_selftest_wait_timeout")
 
 # Largest batch ep_dispatch_fused takes.
 EP_FUSED_MAX_TOKENS = 1024
@@ -88,6 +88,8 @@ def load_library() -> ctypes.CDLL:
     lib.ep_dispatch_layout_experts.restype = _I
     lib.ep_combine_weighted.argtypes = [_P, _P, _P, _I64, _I, _I, _I64, _P, _P, _P]
     lib.ep_combine_weighted.restype = _I
+    lib.ep_selftest_wait_timeout.argtypes = [_P, _P]
+    lib.ep_selftest_wait_timeout.restype = _I
     lib.ep_status_string.argtypes = [_I]
     lib.ep_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -295,3 +297,11 @@ def ep_combine_weighted(y: torch.Tensor, slot: torch.Tensor, w: torch.Tensor, ou
     rc = load_library().ep_combine_weighted(_ptr(y), _ptr(slot), _ptr(w), T, H, C, y.shape[0],
                                             _ptr(out), _ptr(status), _stream(stream))
     _raise("ep_combine_weighted", rc)
+
+
+def ep_selftest_wait_timeout(status: torch.Tensor, stream=None) -> None:
+    """Diagnostic: a kernel whose bounded wait must run out (about one second)
+    and set EP_STATUS_TIMEOUT in ``status``."""
+    _check_cuda("status", status, torch.int32)
+    rc = load_library().ep_selftest_wait_timeout(_ptr(status), _stream(stream))
+    _raise("ep_selftest_wait_timeout", rc)

@@ -280,6 +280,17 @@ EP_API int ep_combine_weighted(const void* y, const int32_t* slot, const float* 
                                int H, int C, int64_t capacity_rows, void* out, int32_t* status,
                                ep_stream_t stream);
 
+/*
+ * Self-test of the bounded waits (diagnostic, not part of the data path).
+ * Launches one kernel that waits, with the helper every kernel of the library
+ * uses for its on-chip waits, on a barrier that nothing completes.  After
+ * about one second the wait gives up: the kernel ORs EP_STATUS_TIMEOUT into
+ * *status (device int32, required) and returns, and the context stays usable.
+ * Returns EP_OK once the kernel is enqueued; the caller synchronises and reads
+ * *status.
+ */
+EP_API int ep_selftest_wait_timeout(int32_t* status, ep_stream_t stream);
+
 /* Human-readable name of an EP_* return code (static string). */
 EP_API const char* ep_status_string(int code);
 

@@ -7,6 +7,12 @@ namespace ep {
 namespace {
 
 constexpr int kDThreads = 256;
+#ifndef EP_FP8_U
+#define EP_FP8_U 1  // block quadruples per step
+#endif
+#ifndef EP_FP8_MINB
+#define EP_FP8_MINB 4  // CTAs per SM the register allocation must allow
+#endif
 
 // Two fp32 values to two e4m3 codes, round to nearest even, saturating to
 // +-448: `lo` goes to the low byte.
@@ -84,7 +90,7 @@ __device__ __forceinline__ uint4 e4m3x16_of_quotients(const uint32_t (&w)[8], fl
 // segment), so that small batches still fill the GPU; each segment is
 // quantised once and its codes and scales are stored to every destination.
 template <int U>
-__global__ void __launch_bounds__(kDThreads)
+__global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
     dispatch_fp8_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ topk_idx,
                         const float* __restrict__ topk_w, int64_t T, int H, int k, int W,
                         const int32_t* __restrict__ slot, int64_t cap, uint8_t* __restrict__ recv_x,
@@ -100,59 +106,121 @@ __global__ void __launch_bounds__(kDThreads)
   const int64_t gwarp = ((int64_t)blockIdx.x * kDThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kDThreads) >> 5;
   const bool narrow = T * nseg < 0x7fffffffLL;  // 32-bit unit arithmetic suffices
+  const int64_t units = T * nseg;
   bool cap_err = false;
-  for (int64_t u = gwarp; u < T * nseg; u += nwarps) {
-    const int64_t t = narrow ? (int64_t)((uint32_t)u / (uint32_t)nseg) : u / nseg;
-    const int seg = (int)(u - t * nseg);
-    const Dests d = token_dests(slot, t, W, cap, lane);
-    if (seg == 0) {
-      cap_err |= d.cap_err;
-      carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
+  // The warp walks its steps (unit u, quad round q0) in order and issues the
+  // loads of the next step (and, at a unit's last step, the next unit's slot
+  // row) before working on the current one, so loads stay in flight while it
+  // quantises and stores.
+  auto split = [&](int64_t uu, int64_t& tt, int& sg, int& qs, int& qe) {
+    tt = narrow ? (int64_t)((uint32_t)uu / (uint32_t)nseg) : uu / nseg;
+    sg = (int)(uu - tt * nseg);
+    qs = sg * per_seg;
+    qe = (sg + 1) * per_seg < nquad ? (sg + 1) * per_seg : nquad;
+  };
+  auto load_step = [&](int64_t tt, int q, int qe, uint4 (&A)[U], uint4 (&C)[U]) {
+    const uint4* src = x + tt * n16;
+#pragma unroll
+    for (int v = 0; v < U; ++v) {
+      const int b = (q + v) * 4 + qb;
+      A[v] = make_uint4(0u, 0u, 0u, 0u);
+      C[v] = make_uint4(0u, 0u, 0u, 0u);
+      if (q + v < qe && b < nb) {  // the lane's 32 contiguous bytes (L1-cached pair)
+        A[v] = __ldg(src + b * 16 + hl * 2);
+        C[v] = __ldg(src + b * 16 + hl * 2 + 1);
+      }
     }
-    const uint4* src = x + t * n16;
-    const int q_end = (seg + 1) * per_seg < nquad ? (seg + 1) * per_seg : nquad;
-    for (int q0 = seg * per_seg; q0 < q_end; q0 += U) {
-      uint4 codes[U];
-      float sc[U];
-#pragma unroll
-      for (int v = 0; v < U; ++v) {
-        const int b = (q0 + v) * 4 + qb;
-        uint4 a = make_uint4(0u, 0u, 0u, 0u), c = make_uint4(0u, 0u, 0u, 0u);
-        if (q0 + v < q_end && b < nb) {  // the lane's 32 contiguous bytes (L1-cached pair)
-          a = __ldg(src + b * 16 + hl * 2);
-          c = __ldg(src + b * 16 + hl * 2 + 1);
-        }
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-        float m = bf16x16_absmax(w);
-#pragma unroll
-        for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-        const float s = __fdiv_rn(m, 448.0f);
-        sc[v] = s;
-        codes[v] = s != 0.0f ? e4m3x16_of_quotients(w, s, __frcp_rn(s)) : make_uint4(0u, 0u, 0u, 0u);
+  };
+  int64_t u = gwarp, t = 0;
+  int seg = 0, q0 = 0, q_end = 0;
+  uint4 A[U], C[U];
+  int s_raw = -1;  // the current unit's slot entry of this lane
+  if (u < units) {
+    split(u, t, seg, q0, q_end);
+    load_step(t, q0, q_end, A, C);
+    s_raw = lane < W ? __ldg(slot + t * W + lane) : -1;
+  }
+  Dests d;
+  d.nd = 0;
+  d.my_row = -1;
+  while (u < units) {
+    // the next step, and its loads
+    int64_t u2 = u, t2 = t;
+    int seg2 = seg, q2 = q0 + U, qe2 = q_end;
+    int s_raw2 = s_raw;
+    if (q2 >= q_end) {
+      u2 = u + nwarps;
+      if (u2 < units) {
+        split(u2, t2, seg2, q2, qe2);
+        s_raw2 = lane < W ? __ldg(slot + t2 * W + lane) : -1;
       }
-      // the lane's byte offsets in a row, and whether each of its blocks exists
-      bool has[U];
-      int boff[U];
+    }
+    uint4 A2[U], C2[U];
+    if (u2 < units) {
+      load_step(t2, q2, qe2, A2, C2);
+    } else {
 #pragma unroll
-      for (int v = 0; v < U; ++v) {
-        const int b = (q0 + v) * 4 + qb;
-        has[v] = q0 + v < q_end && b < nb;
-        boff[v] = b * 128 + hl * 16;
+      for (int v = 0; v < U; ++v) A2[v] = C2[v] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (q0 == seg * per_seg) {  // a unit's first step: its destinations and metadata
+      const bool keep = s_raw >= 0 && (int64_t)s_raw < cap;
+      const bool over = s_raw >= 0 && (int64_t)s_raw >= cap;
+      const unsigned dmask = __ballot_sync(kFull, keep);
+      const int r = nth_set_bit_of_lane(dmask, lane);
+      const int rowv = __shfl_sync(kFull, s_raw, r & 31);
+      d.nd = __popc(dmask);
+      d.my_row = r >= 0 ? rowv : -1;
+      d.cap_err = __any_sync(kFull, over);
+      if (seg == 0) {
+        cap_err |= d.cap_err;
+        carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
       }
+    }
+    uint4 codes[U];
+    float sc[U];
+#pragma unroll
+    for (int v = 0; v < U; ++v) {
+      const uint32_t w[8] = {A[v].x, A[v].y, A[v].z, A[v].w, C[v].x, C[v].y, C[v].z, C[v].w};
+      float m = bf16x16_absmax(w);
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      const float sv = __fdiv_rn(m, 448.0f);
+      sc[v] = sv;
+      codes[v] = sv != 0.0f ? e4m3x16_of_quotients(w, sv, __frcp_rn(sv)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // the lane's byte offsets in a row, and whether each of its blocks exists
+    bool has[U];
+    int boff[U];
+#pragma unroll
+    for (int v = 0; v < U; ++v) {
+      const int b = (q0 + v) * 4 + qb;
+      has[v] = q0 + v < q_end && b < nb;
+      boff[v] = b * 128 + hl * 16;
+    }
 #pragma unroll 1
-      for (int qq = 0; qq < d.nd; ++qq) {  // the token's destinations only
-        const int64_t row = __shfl_sync(kFull, d.my_row, qq);
-        uint8_t* dst = recv_x + row * H;
-        float* dsc = recv_scale + row * nb;
+    for (int qq = 0; qq < d.nd; ++qq) {  // the token's destinations only
+      const int64_t row = __shfl_sync(kFull, d.my_row, qq);
+      uint8_t* dst = recv_x + row * H;
+      float* dsc = recv_scale + row * nb;
 #pragma unroll
-        for (int v = 0; v < U; ++v) {
-          if (has[v]) {
-            st_v4(reinterpret_cast<uint4*>(dst + boff[v]), codes[v]);
-            if (hl == 0) dsc[(q0 + v) * 4 + qb] = sc[v];
-          }
+      for (int v = 0; v < U; ++v) {
+        if (has[v]) {
+          st_v4(reinterpret_cast<uint4*>(dst + boff[v]), codes[v]);
+          if (hl == 0) dsc[(q0 + v) * 4 + qb] = sc[v];
         }
       }
     }
+#pragma unroll
+    for (int v = 0; v < U; ++v) {
+      A[v] = A2[v];
+      C[v] = C2[v];
+    }
+    u = u2;
+    t = t2;
+    seg = seg2;
+    q0 = q2;
+    q_end = qe2;
+    s_raw = s_raw2;
   }
   pdl_launch_dependents();
   if (cap_err && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_CAPACITY);
@@ -169,7 +237,7 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
   const uint4* x4 = static_cast<const uint4*>(x);
   // segments per token: enough (token, segment) units to give every resident warp
   // a few, but no more segments than block quadruples
-  auto kern = dispatch_fp8_kernel<2>;
+  auto kern = dispatch_fp8_kernel<EP_FP8_U>;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDThreads, 0) != cudaSuccess ||
       per_sm < 1)
@@ -180,7 +248,7 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
   nseg = nseg < 1 ? 1 : (nseg > nquad ? nquad : nseg);
   // segments of whole rounds of 2 quads (the kernel's unroll: no half-empty
   // rounds), and no empty segments
-  const int per_seg = ((nquad + nseg - 1) / nseg + 1) / 2 * 2;
+  const int per_seg = ((nquad + nseg - 1) / nseg + EP_FP8_U - 1) / EP_FP8_U * EP_FP8_U;
   nseg = (nquad + per_seg - 1) / per_seg;
   const int64_t units = T * nseg;
   const int64_t grid = (units * 32 + kDThreads - 1) / kDThreads < device_sm_count() * per_sm

@@ -18,7 +18,8 @@ import numpy as np
 from ._build import LIB, build_oracle
 
 __all__ = ["STATUS_BAD_EXPERT", "STATUS_CAPACITY", "QUANT_BF16", "QUANT_FP8",
-           "layout", "dispatch", "combine", "localize_ids", "layout_experts", "combine_weighted", "bf16_from_f32", "e4m3_from_f32",
+           "layout", "dispatch", "combine", "localize_ids", "layout_experts", "combine_weighted",
+           "cast_transpose", "cast_transpose_t_bytes", "bf16_from_f32", "e4m3_from_f32",
            "f32_from_e4m3", "f32_from_bf16", "run_all"]
 
 STATUS_BAD_EXPERT = 1
@@ -48,6 +49,8 @@ def _load():
         lib.ep_ref_bf16_from_f32_array.restype = None
         lib.ep_ref_e4m3_from_f32_array.argtypes = [_P, _I64, _P]
         lib.ep_ref_e4m3_from_f32_array.restype = None
+        lib.ep_ref_cast_transpose.argtypes = [_P, _P, _I, _I, _P, _P, _P, _P]
+        lib.ep_ref_cast_transpose.restype = _I
         lib.ep_ref_layout_experts.argtypes = [_P, _I64, _I, _I, _P, _P, _P, _P, _P]
         lib.ep_ref_layout_experts.restype = _I
         lib.ep_ref_combine_weighted.argtypes = [_P, _P, _P, _I64, _I, _I, _I64, _P, _P, _P]
@@ -163,6 +166,32 @@ def combine_weighted(y: np.ndarray, slot: np.ndarray, w: np.ndarray, cap: int | 
     if rc != 0:
         raise ValueError("oracle combine_weighted: invalid arguments")
     return {"out": out, "status": int(st[0])}
+
+
+def cast_transpose_t_bytes(expert_offset: np.ndarray, H: int) -> int:
+    n = np.diff(np.asarray(expert_offset, np.int64))
+    return int(H * ((n + 15) // 16 * 16).sum())
+
+
+def cast_transpose(y: np.ndarray, expert_offset: np.ndarray, scale: np.ndarray,
+                   amax: np.ndarray | None = None) -> dict:
+    """FP8 cast and per-expert transposed cast of the expert-major rows; amax
+    starts from ``amax`` (zeros by default)."""
+    lib = _load()
+    y = _c(y, np.uint16)
+    off = _c(expert_offset, np.int32)
+    sc = _c(scale, np.float32)
+    E = off.size - 1
+    H = y.shape[1]
+    R = int(off[-1])
+    out_c = np.zeros((R, H), np.uint8)
+    out_t = np.zeros(cast_transpose_t_bytes(off, H), np.uint8)
+    am = np.zeros(E, np.float32) if amax is None else _c(amax, np.float32).copy()
+    rc = lib.ep_ref_cast_transpose(_ptr(y), _ptr(off), E, H, _ptr(sc), _ptr(out_c), _ptr(out_t),
+                                   _ptr(am))
+    if rc != 0:
+        raise ValueError("oracle cast_transpose: invalid arguments")
+    return {"out_c": out_c, "out_t": out_t, "amax": am}
 
 
 def combine(y: np.ndarray, slot: np.ndarray, cap: int | None = None) -> dict:

@@ -19,6 +19,9 @@
  *          CHALLENGE 2025: All-to-All, GEMM-ReduceScatter, and AllGather-GEMM",
  *          §3.1 -- dispatch sends each token's row to every rank that hosts one
  *          of its experts, combine brings the rows back and reduces them.
+ *  [te]    "Optimized rocm specific multicast transpose kernel" (ROCm/
+ *          TransformerEngine pull 586): the FP8 cast and transposed cast of
+ *          every expert's tensor in one launch, with the amax fused.
  *  Readings where the pages leave a step open (fixed by the problem statement
  *  of this library, not by the pages):
  *   - receive rows of rank r form one contiguous region starting at the
@@ -351,5 +354,49 @@ int ep_ref_combine_weighted(const uint16_t* y, const int32_t* slot, const float*
     for (int h = 0; h < H; ++h) out[t * H + h] = ep_ref_bf16_from_f32(acc_scratch[h]);
   }
   if (status) *status |= st;
+  return 0;
+}
+
+/* ------------------------------------------------- FP8 cast and transpose */
+
+/* Cast and transposed cast of the expert-major rows ("Optimized rocm specific
+ * multicast transpose kernel", ROCm/TransformerEngine pull 586: an FP8 cast and
+ * an FP8 transposed cast of every expert's tensor in one launch, with the amax
+ * fused).  Expert e owns rows off[e] .. off[e+1]-1 of y (n_e rows of H); with
+ * the expert's scale s_e, every element gets code = e4m3(fl(x * s_e)) (fp32
+ * product rounded to nearest even, then e4m3 round to nearest even with
+ * saturation, as the dispatch encoder):
+ *   out_c[row][h] = code            (row-major, rows as in y),
+ *   out_t[tb_e + h * ld_e + i] = code of row off[e] + i, column h, where
+ *     ld_e = n_e rounded up to a multiple of 16 and tb_e = H * (ld_0 + ... +
+ *     ld_{e-1}); the padding bytes i >= n_e are 0,
+ *   amax[e] = max(amax[e], max |x| over the expert's rows).
+ * The caller zeroes amax for a fresh maximum. */
+int ep_ref_cast_transpose(const uint16_t* y, const int32_t* off, int E, int H, const float* scale,
+                          uint8_t* out_c, uint8_t* out_t, float* amax) {
+  if (E < 1 || H < 1) return -1;
+  int64_t tb = 0;
+  for (int e = 0; e < E; ++e) {
+    const int64_t r0 = off[e], n = (int64_t)off[e + 1] - off[e];
+    if (n < 0) return -1;
+    const int64_t ld = (n + 15) / 16 * 16;
+    float m = amax[e];
+    for (int64_t i = 0; i < ld; ++i) {
+      for (int h = 0; h < H; ++h) {
+        uint8_t code = 0;
+        if (i < n) {
+          const float x = ep_ref_f32_from_bf16(y[(r0 + i) * H + h]);
+          const float q = x * scale[e];
+          code = ep_ref_e4m3_from_f32(q);
+          out_c[(r0 + i) * H + h] = code;
+          const float a = fabsf(x);
+          if (a > m) m = a;
+        }
+        out_t[tb + (int64_t)h * ld + i] = code;
+      }
+    }
+    amax[e] = m;
+    tb += (int64_t)H * ld;
+  }
   return 0;
 }

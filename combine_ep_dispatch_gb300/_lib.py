@@ -31,7 +31,8 @@ EP_QUANT_FP8_E4M3_B128 = 1
 EXPORTED = ("ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_dispatch_layout", "ep_dispatch",
             "ep_combine", "ep_status_string", "ep_dispatch_layout_noalloc", "ep_dispatch_fused",
             "ep_localize_expert_ids", "ep_layout_experts_workspace_bytes",
-            "ep_dispatch_layout_experts", "ep_combine_weighted", "ep_selftest_wait_timeout")
+            "ep_dispatch_layout_experts", "ep_combine_weighted", "ep_selftest_wait_timeout",
+            "ep_cast_transpose_t_bytes", "ep_cast_transpose_experts")
 
 # Largest batch ep_dispatch_fused takes.
 EP_FUSED_MAX_TOKENS = 1024
@@ -88,6 +89,10 @@ def load_library() -> ctypes.CDLL:
     lib.ep_dispatch_layout_experts.restype = _I
     lib.ep_combine_weighted.argtypes = [_P, _P, _P, _I64, _I, _I, _I64, _P, _P, _P]
     lib.ep_combine_weighted.restype = _I
+    lib.ep_cast_transpose_t_bytes.argtypes = [_I64, _I, _I]
+    lib.ep_cast_transpose_t_bytes.restype = ctypes.c_size_t
+    lib.ep_cast_transpose_experts.argtypes = [_P, _P, _I, _I, _P, _I64, _P, _P, _P, _P, _P]
+    lib.ep_cast_transpose_experts.restype = _I
     lib.ep_selftest_wait_timeout.argtypes = [_P, _P]
     lib.ep_selftest_wait_timeout.restype = _I
     lib.ep_status_string.argtypes = [_I]
@@ -305,3 +310,31 @@ def ep_selftest_wait_timeout(status: torch.Tensor, stream=None) -> None:
     _check_cuda("status", status, torch.int32)
     rc = load_library().ep_selftest_wait_timeout(_ptr(status), _stream(stream))
     _raise("ep_selftest_wait_timeout", rc)
+
+
+def ep_cast_transpose_t_bytes(capacity_rows: int, E: int, H: int) -> int:
+    return int(load_library().ep_cast_transpose_t_bytes(capacity_rows, E, H))
+
+
+def ep_cast_transpose_experts(y: torch.Tensor, expert_offset: torch.Tensor, scale: torch.Tensor,
+                              out_c: torch.Tensor, out_t: torch.Tensor, amax: torch.Tensor,
+                              status: torch.Tensor | None = None, stream=None) -> None:
+    """FP8 cast (out_c) and per-expert transposed cast (out_t) of the
+    expert-major rows y, amax[e] = max(amax[e], max |x|)."""
+    _check_cuda("y", y, torch.bfloat16)
+    _check_cuda("expert_offset", expert_offset, torch.int32)
+    _check_cuda("scale", scale, torch.float32)
+    _check_cuda("out_c", out_c, torch.uint8)
+    _check_cuda("out_t", out_t, torch.uint8)
+    _check_cuda("amax", amax, torch.float32)
+    _check_cuda("status", status, torch.int32, optional=True)
+    cap, H = y.shape
+    E = expert_offset.numel() - 1
+    if tuple(out_c.shape) != (cap, H):
+        raise ValueError("out_c must have the shape of y")
+    if out_t.numel() < ep_cast_transpose_t_bytes(cap, E, H):
+        raise ValueError("out_t is smaller than ep_cast_transpose_t_bytes(capacity_rows, E, H)")
+    rc = load_library().ep_cast_transpose_experts(_ptr(y), _ptr(expert_offset), E, H, _ptr(scale),
+                                                  cap, _ptr(out_c), _ptr(out_t), _ptr(amax),
+                                                  _ptr(status), _stream(stream))
+    _raise("ep_cast_transpose_experts", rc)

@@ -176,6 +176,28 @@ int ep_combine_weighted(const void* y, const int32_t* slot, const float* w, int6
                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t ep_cast_transpose_t_bytes(int64_t capacity_rows, int E, int H) {
+  if (capacity_rows < 0 || E < 1 || H < 1) return 0;
+  return ep::cast_transpose_t_bytes(capacity_rows, E, H);
+}
+
+int ep_cast_transpose_experts(const void* y, const int32_t* expert_offset, int E, int H,
+                              const float* scale, int64_t capacity_rows, void* out_c, void* out_t,
+                              float* amax, int32_t* status, ep_stream_t stream) {
+  if (E < 1 || E > 8192 || H < 1 || capacity_rows < 0 || capacity_rows > kMaxRows)
+    return EP_ERR_INVALID_ARG;
+  if (H % 256 != 0) return EP_ERR_UNSUPPORTED;
+  if (!expert_offset || !scale || !amax) return EP_ERR_INVALID_ARG;
+  if (capacity_rows > 0 && (!y || !out_c || !out_t)) return EP_ERR_INVALID_ARG;
+  if (!aligned(y, 16) || !aligned(out_c, 16) || !aligned(out_t, 16) ||
+      !aligned(expert_offset, 4) || !aligned(scale, 4) || !aligned(amax, 4) || !aligned(status, 4))
+    return EP_ERR_MISALIGNED;
+  return from_cuda(ep::launch_cast_transpose(y, expert_offset, E, H, scale, capacity_rows,
+                                             static_cast<uint8_t*>(out_c),
+                                             static_cast<uint8_t*>(out_t), amax, status,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* ep_status_string(int code) {
   switch (code) {
     case EP_OK:

@@ -234,6 +234,12 @@ cudaError_t launch_combine_weighted(const void* y, const int32_t* slot, const fl
                                     int H, int C, int64_t capacity_rows, void* out,
                                     int32_t* status, cudaStream_t stream);
 
+size_t cast_transpose_t_bytes(int64_t R, int E, int H);
+cudaError_t launch_cast_transpose(const void* y, const int32_t* expert_offset, int E, int H,
+                                  const float* scale, int64_t capacity_rows, uint8_t* out_c,
+                                  uint8_t* out_t, float* amax, int32_t* status,
+                                  cudaStream_t stream);
+
 int layout_experts_max_experts();
 size_t layout_experts_workspace_bytes(int64_t T, int k, int E);
 cudaError_t launch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,

@@ -281,6 +281,37 @@ EP_API int ep_combine_weighted(const void* y, const int32_t* slot, const float* 
                                ep_stream_t stream);
 
 /*
+ * FP8 cast and transposed cast of the expert-major rows, with the amax fused,
+ * for expert GEMMs that take FP8 operands (row-major for the forward product,
+ * transposed for the weight gradient).  Expert e owns rows
+ * [expert_offset[e], expert_offset[e+1]) of y (n_e rows); with its scale s_e
+ * every element gets code = e4m3(fl(x * s_e)) (fp32 product, then round to
+ * nearest even, saturating to +-448):
+ *   out_c[row][h] = code (row-major, the rows of y),
+ *   out_t[H * (ld_0 + ... + ld_{e-1}) + h * ld_e + i] = code of row
+ *     expert_offset[e] + i, column h, with ld_e = n_e rounded up to a multiple
+ *     of 16 (the padding bytes are 0): one [H][ld_e] block per expert,
+ *   amax[e] = max(amax[e], max |x| over the expert's rows) (zero amax first
+ *     for a fresh maximum).
+ * Follows "Optimized rocm specific multicast transpose kernel" (ROCm/
+ * TransformerEngine pull 586): both casts of every expert's tensor in one
+ * launch, amax fused, pad-16 rows.
+ *
+ *  y              bf16 [capacity_rows, H]   (from ep_dispatch into the expert-major layout)
+ *  expert_offset  int32 [E + 1], nondecreasing (from ep_dispatch_layout_experts)
+ *  scale          fp32 [E]
+ *  out_c          uint8 [capacity_rows, H]
+ *  out_t          uint8, ep_cast_transpose_t_bytes(capacity_rows, E, H) bytes
+ *  amax           fp32 [E], read and written
+ * Experts whose rows leave [0, capacity_rows) are skipped and set
+ * EP_STATUS_CAPACITY.  Limits: H % 256 == 0; 1 <= E <= 8192.
+ */
+EP_API size_t ep_cast_transpose_t_bytes(int64_t capacity_rows, int E, int H);
+EP_API int ep_cast_transpose_experts(const void* y, const int32_t* expert_offset, int E, int H,
+                                     const float* scale, int64_t capacity_rows, void* out_c,
+                                     void* out_t, float* amax, int32_t* status, ep_stream_t stream);
+
+/*
  * Self-test of the bounded waits (diagnostic, not part of the data path).
  * Launches one kernel that waits, with the helper every kernel of the library
  * uses for its on-chip waits, on a barrier that nothing completes.  After

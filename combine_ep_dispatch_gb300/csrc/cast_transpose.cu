@@ -146,15 +146,23 @@ __global__ void __launch_bounds__(kCtThreads)
     const int h0 = ct * kCtCols;
     const float s = scale[e];
 
-    // 1. cast: 64 rows x 32 vectors of 8 columns, 8 vectors per thread
+    // 1. cast: 64 rows x 32 vectors of 8 columns, 8 vectors per thread, all
+    //    loaded before the first is used
     float m = 0.0f;
+    uint4 wv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = (tid + j * kCtThreads) >> 5, cv = tid & 31;
+      wv[j] = r < nrows ? ld_stream_v4(y + (r0 + i0 + r) * n16 + (h0 >> 3) + cv)
+                        : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int v = tid + j * kCtThreads;
       const int r = v >> 5, cv = v & 31;
       uint2 codes = make_uint2(0u, 0u);
       if (r < nrows) {
-        const uint4 w = ld_stream_v4(y + (r0 + i0 + r) * n16 + (h0 >> 3) + cv);
+        const uint4 w = wv[j];
         const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
         uint32_t c[4];
 #pragma unroll

@@ -172,6 +172,27 @@ def test_combine_weighted_rejects(lib, kw, code):
     assert rc == code
 
 
+@cpu_only
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=7168 + 128), _lib.EP_ERR_UNSUPPORTED),             # H % 256
+    (dict(E=0), _lib.EP_ERR_INVALID_ARG),
+    (dict(E=9000), _lib.EP_ERR_INVALID_ARG),
+    (dict(t_off=8), _lib.EP_ERR_MISALIGNED),                   # out_t 8-byte aligned
+    (dict(scale_null=True), _lib.EP_ERR_INVALID_ARG),
+    (dict(cap=-1), _lib.EP_ERR_INVALID_ARG),
+])
+def test_cast_transpose_rejects(lib, kw, code):
+    scale = None if kw.get("scale_null") else A
+    rc = lib.ep_cast_transpose_experts(A, A, kw.get("E", 256), kw.get("H", 7168), scale,
+                                       kw.get("cap", 1000), A, A + kw.get("t_off", 0), A, None, None)
+    assert rc == code
+
+
+def test_cast_transpose_t_bytes(lib):
+    assert ep.ep_cast_transpose_t_bytes(32768, 256, 7168) == 7168 * (32768 + 15 * 256)
+    assert ep.ep_cast_transpose_t_bytes(-1, 256, 7168) == 0
+
+
 def test_binding_rejects_host_tensors(lib):
     idx = torch.zeros(4, 2, dtype=torch.int32)
     with pytest.raises(ValueError):

@@ -109,6 +109,29 @@ class DispatchCombine:
             _lib.ep_combine_weighted(y, self.slot, w, self.out, self.status, stream)
         return self.out
 
+    def cast_transpose(self, scale: torch.Tensor, amax: torch.Tensor | None = None,
+                       stream=None):
+        """Expert-major order, bf16 dispatch: the FP8 cast of the received rows
+        (``recv_fp8`` [capacity_rows, H]) and their per-expert transposed cast
+        (``recv_fp8_t``, one [H][n_e rounded up to 16] block per expert) with
+        per-expert scales ``scale`` [E]; ``amax`` [E] (default: zeroed buffer
+        ``self.amax``) gets max(amax, max |x|).  Returns (recv_fp8, recv_fp8_t, amax)."""
+        if self.order != "expert" or self.quant != _lib.EP_QUANT_BF16:
+            raise ValueError("cast_transpose takes the bf16 rows of the expert-major layout")
+        if not hasattr(self, "recv_fp8"):
+            dev = self.recv_x.device
+            self.recv_fp8 = torch.empty(self.capacity_rows, self.H, dtype=torch.uint8, device=dev)
+            self.recv_fp8_t = torch.empty(
+                max(_lib.ep_cast_transpose_t_bytes(self.capacity_rows, self.E, self.H), 16),
+                dtype=torch.uint8, device=dev)
+            self.amax = torch.zeros(self.E, dtype=torch.float32, device=dev)
+        if amax is None:
+            amax = self.amax
+            amax.zero_()
+        _lib.ep_cast_transpose_experts(self.recv_x, self.expert_offset, scale, self.recv_fp8,
+                                       self.recv_fp8_t, amax, self.status, stream)
+        return self.recv_fp8, self.recv_fp8_t, amax
+
     def step(self, x, topk_idx, topk_w, y=None, stream=None) -> torch.Tensor:
         self.layout(topk_idx, stream)
         self.dispatch(x, topk_idx, topk_w, stream)

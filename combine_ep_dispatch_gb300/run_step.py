@@ -9,7 +9,8 @@ Combine reads the dispatched rows (identity experts; for the FP8 workload a
 bf16 dispatch of the same routing provides them).  --order expert runs the
 expert-major path (one row per (token, expert) pair, combine weighted by the
 gate weights); --fused uses the one-launch layout + dispatch (rank order,
-bf16, small batches).
+bf16, small batches); --cast-transpose adds the FP8 cast and transposed cast
+of the received rows (expert order).
 """
 from __future__ import annotations
 
@@ -30,6 +31,7 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--order", default="rank", choices=("rank", "expert"))
     ap.add_argument("--fused", action="store_true")
+    ap.add_argument("--cast-transpose", action="store_true")
     args = ap.parse_args(argv)
 
     inp = make_inputs(args.workload, seed=args.seed)
@@ -50,6 +52,7 @@ def main(argv=None):
     ident = dc if quant == _lib.EP_QUANT_BF16 else DispatchCombine(
         cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, capacity_rows=R, device=dev, order=order)
     weights = w if order == "expert" else None
+    scale = torch.full((cfg.E,), 112.0, dtype=torch.float32, device=dev)
     for _ in range(args.iters):
         if args.fused:
             dc.dispatch_fused(x, idx, w)
@@ -59,6 +62,8 @@ def main(argv=None):
         if ident is not dc:
             ident.layout(idx)
             ident.dispatch(x, idx, w)
+        if args.cast_transpose:
+            ident.cast_transpose(scale)
         dc.combine(ident.recv_x, weights)
     torch.cuda.synchronize()
     print(f"{args.workload} ({order}{', fused' if args.fused else ''}): T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} W={cfg.W} R={R} "

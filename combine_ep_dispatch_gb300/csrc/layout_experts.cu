@@ -19,7 +19,9 @@
 // Larger: chunks of kXPairs pairs and three kernels
 //   count:  per-chunk, per-expert pair counts;
 //   scan:   per expert, the pairs in earlier chunks (in place) and the total;
-//   assign: offsets by a block scan of the totals, then the slots.
+//   assign: offsets by a block scan of the totals, then the slots;
+// up to kXSelfScanMaxChunks chunks the assign CTAs do the scan's sums
+// themselves and the scan kernel is not launched.
 // Integer counts only: the layout is a pure function of topk_idx.
 #include "ep_device.cuh"
 
@@ -40,6 +42,10 @@ constexpr int kXSingleGroups = 8;
 constexpr int64_t kXSingleMax = EP_XSINGLE_MAX;  // <= kXSingleWarps * kXSingleGroups * 32
 static_assert(kXSingleMax <= kXSingleWarps * kXSingleGroups * 32, "one CTA holds 8192 pairs");
 constexpr int kXSingleMaxE = 1024;
+#ifndef EP_XSELF_SCAN_MAX_CHUNKS
+#define EP_XSELF_SCAN_MAX_CHUNKS 32
+#endif
+constexpr int64_t kXSelfScanMaxChunks = EP_XSELF_SCAN_MAX_CHUNKS;
 constexpr int kXMaxE = 4096;
 
 inline size_t a256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -295,14 +301,20 @@ __global__ void __launch_bounds__(kXWarps * 32)
 }
 
 // Chunk c: expert offsets from the totals, then the slots of its pairs.
+// SELF_SCAN (few chunks): the CTA sums the raw per-chunk counts itself (all
+// chunks for the totals, chunks before c for its base rows), in place of the
+// scan kernel; CTA 0 also writes num_tokens_per_expert.
+template <bool SELF_SCAN>
 __global__ void __launch_bounds__(kXWarps * 32)
     xlayout_assign_kernel(const int32_t* __restrict__ topk_idx, int64_t P, int E, int nbits, XWs ws,
+                          int64_t C, int32_t* __restrict__ num_tokens_per_expert,
                           int32_t* __restrict__ expert_offset, int32_t* __restrict__ slot) {
   pdl_wait();
   extern __shared__ int32_t s_dyn[];
   int32_t* s_cnt = s_dyn;                  // [kXWarps][E]
   int32_t* s_tot = s_cnt + kXWarps * E;    // [E]
-  int32_t* s_off = s_tot + E;              // [E + 1]
+  int32_t* s_bef = s_tot + E;              // [E]: pairs of each expert in chunks before c
+  int32_t* s_off = s_bef + E;              // [E + 1]
   __shared__ int32_t s_warp[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t c = blockIdx.x;
@@ -310,7 +322,23 @@ __global__ void __launch_bounds__(kXWarps * 32)
   int ids[kXGroups];
   bool valid[kXGroups];
   load_groups<kXGroups>(topk_idx, P, base, kXGroups, E, ids, valid);
-  for (int e = tid; e < E; e += blockDim.x) s_tot[e] = ws.tot[e];
+  for (int e = tid; e < E; e += blockDim.x) {
+    if constexpr (SELF_SCAN) {
+      int tot = 0, bef = 0;
+#pragma unroll 8
+      for (int64_t q = 0; q < C; ++q) {
+        const int v = ws.cnt[q * E + e];
+        tot += v;
+        bef += q < c ? v : 0;
+      }
+      s_tot[e] = tot;
+      s_bef[e] = bef;
+      if (c == 0) num_tokens_per_expert[e] = tot;
+    } else {
+      s_tot[e] = ws.tot[e];
+      s_bef[e] = ws.cnt[c * E + e];
+    }
+  }
   for (int i = tid; i < kXWarps * E; i += blockDim.x) s_cnt[i] = 0;
   __syncthreads();
   count_groups<kXGroups>(ids, valid, kXGroups, nbits, s_cnt + warp * E);
@@ -318,7 +346,7 @@ __global__ void __launch_bounds__(kXWarps * 32)
   if (c == 0)
     for (int e = tid; e <= E; e += blockDim.x) expert_offset[e] = s_off[e];
   for (int e = tid; e < E; e += blockDim.x) {
-    int run = s_off[e] + ws.cnt[c * E + e];
+    int run = s_off[e] + s_bef[e];
 #pragma unroll
     for (int w = 0; w < kXWarps; ++w) {
       const int v = s_cnt[w * E + e];
@@ -375,19 +403,26 @@ cudaError_t launch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int
   }
   const int64_t C = x_chunks(P);
   const XWs ws = x_carve(workspace, P, E);
-  static bool done[128];
-  const size_t most = sizeof(int32_t) * ((size_t)(kXWarps + 2) * kXMaxE + 1);
-  cudaError_t e = set_smem(reinterpret_cast<const void*>(xlayout_assign_kernel), most, done);
+  static bool done[128], done_self[128];
+  const size_t most = sizeof(int32_t) * ((size_t)(kXWarps + 3) * kXMaxE + 1);
+  cudaError_t e = set_smem(reinterpret_cast<const void*>(xlayout_assign_kernel<false>), most, done);
+  if (e != cudaSuccess) return e;
+  e = set_smem(reinterpret_cast<const void*>(xlayout_assign_kernel<true>), most, done_self);
   if (e != cudaSuccess) return e;
   e = launch_pdl(xlayout_count_kernel, dim3((unsigned)C), dim3(kXWarps * 32),
                  sizeof(int32_t) * (size_t)E, stream, topk_idx, P, E, ws, status);
   if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(int32_t) * ((size_t)(kXWarps + 3) * E + 1);
+  if (C <= kXSelfScanMaxChunks)  // each CTA reads all C x E counts: cheap for few chunks
+    return launch_pdl(xlayout_assign_kernel<true>, dim3((unsigned)C), dim3(kXWarps * 32), smem,
+                      stream, topk_idx, P, E, nbits, ws, C, num_tokens_per_expert, expert_offset,
+                      slot);
   e = launch_pdl(xlayout_scan_kernel, dim3((unsigned)((E + 31) / 32)), dim3(kXWarps * 32), 0,
                  stream, C, E, ws, num_tokens_per_expert);
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(int32_t) * ((size_t)(kXWarps + 2) * E + 1);
-  return launch_pdl(xlayout_assign_kernel, dim3((unsigned)C), dim3(kXWarps * 32), smem, stream,
-                    topk_idx, P, E, nbits, ws, expert_offset, slot);
+  return launch_pdl(xlayout_assign_kernel<false>, dim3((unsigned)C), dim3(kXWarps * 32), smem,
+                    stream, topk_idx, P, E, nbits, ws, C, num_tokens_per_expert, expert_offset,
+                    slot);
 }
 
 }  // namespace ep

@@ -82,6 +82,29 @@ __device__ __forceinline__ uint4 e4m3x16_of_quotients(const uint32_t (&w)[8], fl
                     c[6] | (c[7] << 16));
 }
 
+// Scale s = fl(m / 448) of a block and y = RN(1/s), the reciprocal the exact
+// quotient needs.  m is a bf16 value: m = M * 2^k with an 8-bit significand M,
+// so m / 448 = (M / 7) * 2^(k - 6) and, while everything stays normal,
+// s = fl(M / 7) * 2^(k - 6) and RN(1/s) = RN(1 / fl(M / 7)) * 2^(6 - k)
+// exactly: rounding commutes with scaling by a power of two.  q7[i] = fl(M/7)
+// and r7[i] = RN(1/q7[i]) for M = 128 + i are filled once per CTA by the IEEE
+// division and reciprocal; blocks whose scale would leave [2^-80, 2^100]
+// (biased exponent of m outside [56, 235]), or m = 0, take those operations
+// directly.
+__device__ __forceinline__ void block_scale(float m, const float* s_q7, const float* s_r7,
+                                            float& s, float& y) {
+  const uint32_t mb = __float_as_uint(m);
+  const uint32_t e8 = mb >> 23;
+  if (e8 >= 56u && e8 <= 235u) {
+    const int i = (int)((mb >> 16) & 0x7fu);
+    s = __fmul_rn(s_q7[i], __uint_as_float((e8 - 13u) << 23));   // * 2^(e8 - 140)
+    y = __fmul_rn(s_r7[i], __uint_as_float((267u - e8) << 23));  // * 2^(140 - e8)
+  } else {
+    s = __fdiv_rn(m, 448.0f);
+    y = s != 0.0f ? __frcp_rn(s) : 0.0f;
+  }
+}
+
 // FP8 payload.  A 128-column block is 256 bytes of bf16 = 8 lanes x 32 bytes,
 // so a warp covers four blocks per round (lanes 8b..8b+7 for block b).  Per
 // block: amax over the block (an 8-lane max reduction), scale = amax / 448
@@ -97,6 +120,13 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
                         float* __restrict__ recv_scale, int32_t* __restrict__ recv_topk_idx,
                         float* __restrict__ recv_topk_w, int32_t* __restrict__ recv_src,
                         int nseg, int per_seg, int32_t* __restrict__ status) {
+  __shared__ float s_q7[128], s_r7[128];
+  if (threadIdx.x < 128) {
+    const float q = __fdiv_rn((float)(128 + threadIdx.x), 7.0f);
+    s_q7[threadIdx.x] = q;
+    s_r7[threadIdx.x] = __frcp_rn(q);
+  }
+  __syncthreads();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int qb = lane >> 3, hl = lane & 7;  // block within the quad, lane within the block
@@ -184,9 +214,10 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
       float m = bf16x16_absmax(w);
 #pragma unroll
       for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-      const float sv = __fdiv_rn(m, 448.0f);
+      float sv, yv;
+      block_scale(m, s_q7, s_r7, sv, yv);
       sc[v] = sv;
-      codes[v] = sv != 0.0f ? e4m3x16_of_quotients(w, sv, __frcp_rn(sv)) : make_uint4(0u, 0u, 0u, 0u);
+      codes[v] = sv != 0.0f ? e4m3x16_of_quotients(w, sv, yv) : make_uint4(0u, 0u, 0u, 0u);
     }
     // the lane's byte offsets in a row, and whether each of its blocks exists
     bool has[U];

@@ -324,11 +324,8 @@ template <typename K1, typename KS>
 cudaError_t launch_combine_regs(K1 kern_rows, KS kern_seg, const void* y, const int32_t* slot,
                                 const float* w, int64_t T, int H, int W, int64_t capacity_rows,
                                 void* out, int32_t* status, cudaStream_t stream) {
-  int per_sm = 0;
-  auto kern = kern_seg;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCThreads, 0) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+  static int cache[128];
+  const int per_sm = occupancy_cached(kern_seg, kCThreads, cache);
   const int64_t most = (int64_t)device_sm_count() * per_sm;
   // Segments, when the batch has fewer tokens than the device has warp slots:
   // enough (token, segment) units for EP_COMBINE_SEG_F units per slot, each

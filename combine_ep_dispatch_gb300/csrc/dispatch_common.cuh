@@ -61,10 +61,8 @@ __device__ __forceinline__ void carry_metadata(const int32_t* __restrict__ topk_
 
 template <typename K>
 inline int grid_for(K kernel, int64_t T, int threads) {
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+  static int cache[128];
+  const int per_sm = occupancy_cached(kernel, threads, cache);
   const int64_t want = (T * 32 + threads - 1) / threads;  // one warp per token
   const int64_t cap = (int64_t)device_sm_count() * per_sm;
   int64_t g = want < cap ? want : cap;

@@ -269,10 +269,8 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
   // segments per token: enough (token, segment) units to give every resident warp
   // a few, but no more segments than block quadruples
   auto kern = dispatch_fp8_kernel<EP_FP8_U>;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDThreads, 0) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+  static int cache[128];
+  const int per_sm = occupancy_cached(kern, kDThreads, cache);
   const int64_t warps = (int64_t)device_sm_count() * per_sm * (kDThreads / 32);
   const int nquad = (H / 128 + 3) / 4;
   int nseg = (int)((2 * warps + T - 1) / T);

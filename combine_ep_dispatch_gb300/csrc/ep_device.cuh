@@ -206,6 +206,21 @@ __device__ __forceinline__ int nth_set_bit_of_lane(unsigned mask, int lane) {
 // ------------------------------------------------------------ launchers
 int device_sm_count();  // cached per device; 0 on error
 
+// Resident CTAs per SM of a kernel at a block size (no dynamic shared memory),
+// queried once per device and kept in the caller's cache (one per call site).
+template <typename K>
+int occupancy_cached(K kernel, int threads, int (&cache)[128]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) dev = -1;
+  if (dev >= 0 && cache[dev] > 0) return cache[dev];
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  if (dev >= 0) cache[dev] = per_sm;  // a race only repeats the query
+  return per_sm;
+}
+
 cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int W,
                           int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
                           int32_t* rank_offset, int32_t* slot, void* workspace, int32_t* status,

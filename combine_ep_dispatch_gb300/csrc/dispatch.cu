@@ -80,21 +80,16 @@ __global__ void __launch_bounds__(kDThreads)
 #ifndef EP_TMA_CTAS_PER_SM
 #define EP_TMA_CTAS_PER_SM 2
 #endif
-#ifndef EP_TMA_LANE_STORES
-#define EP_TMA_LANE_STORES 1
-#endif
 constexpr int kTmaStages = EP_TMA_STAGES;            // row buffers per warp
 constexpr int kTmaBarBytes = 1024;                   // barrier area ahead of the row buffers
 constexpr int kTmaSmemBudget = EP_TMA_SMEM_BUDGET;   // row buffers per CTA
 constexpr int kTmaMaxWarps = EP_TMA_MAX_WARPS;
-// L2 priority of the received rows (0: none, 1: evict_first, 2: evict_last).
-// evict_last keeps the rows just written in L2 for their consumer (the expert
-// GEMM reads them next) and moves part of their write-back out of this kernel:
-// measured on GB300 it shortens the layout + dispatch + combine step by 1.3 to
-// 2.5 us at T=4096 (H=7168) and T=8192 (H=4096); evict_first changed nothing.
-#ifndef EP_TMA_STORE_HINT
-#define EP_TMA_STORE_HINT 2
-#endif
+// The received rows are stored with an L2 evict_last policy: it keeps the
+// rows just written in L2 for their consumer (the expert GEMM reads them next)
+// and moves part of their write-back out of this kernel.  Measured on GB300 it
+// shortens the layout + dispatch + combine step by 1.3 to 2.5 us at T=4096
+// (H=7168) and T=8192 (H=4096); evict_first changed nothing.
+constexpr int kL2EvictLast = 2;
 constexpr int kTmaCtasPerSm = EP_TMA_CTAS_PER_SM;
 constexpr uint32_t kTmaMinRowBytes = 1024;  // smaller rows: 16-byte stores from registers
 
@@ -159,34 +154,16 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
     const int r = nth_set_bit_of_lane(dmask, lane);
     const int my_row = __shfl_sync(kFull, s_cur, r & 31);
 
-#if EP_TMA_LANE_STORES
     // every lane observes the row's arrival, lane q sends it to destination q
     const bool ok = mbar_wait_bounded(&full[st], parity);
     if (!__all_sync(kFull, ok)) {
       timed_out = true;
       break;
     }
-#if EP_TMA_STORE_HINT
     if (lane < nd)
       bulk_store_hint(recv_x + (int64_t)my_row * row_bytes, buf + st * stage_bytes, row_bytes,
-                      make_l2_policy<EP_TMA_STORE_HINT>());
-#else
-    if (lane < nd) bulk_store(recv_x + (int64_t)my_row * row_bytes, buf + st * stage_bytes, row_bytes);
-#endif
+                      make_l2_policy<kL2EvictLast>());
     bulk_commit();
-#else
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait_bounded(&full[st], parity);
-    if (!__shfl_sync(kFull, ok, 0)) {
-      timed_out = true;
-      break;
-    }
-    for (int q = 0; q < nd; ++q) {
-      const int row = __shfl_sync(kFull, my_row, q);
-      if (lane == 0) bulk_store(recv_x + (int64_t)row * row_bytes, buf + st * stage_bytes, row_bytes);
-    }
-    if (lane == 0) bulk_commit();
-#endif
     if (meta_lanes) {
       for (int q = 0; q < nd; ++q) {
         const int64_t row = __shfl_sync(kFull, my_row, q);
@@ -205,15 +182,13 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
       d.cap_err = false;
       carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
     }
-    // refill the previous token's buffer once the copies out of it have read it
-#if EP_TMA_LANE_STORES
+    // refill the previous token's buffer once the copies out of it (issued by
+    // several lanes) have read it
     if (j >= 1 && issued < n) {
       bulk_wait_read<1>();
       __syncwarp();
     }
-#endif
     if (lane == 0 && j >= 1 && issued < n) {
-      bulk_wait_read<1>();
       const int sp = (int)((j - 1) % kTmaStages);
       mbar_arrive_expect_tx(&full[sp], row_bytes);
       bulk_load(buf + sp * stage_bytes, x + (gw + issued * NW) * row_bytes, row_bytes, &full[sp]);

@@ -11,7 +11,7 @@
 // The (token, column) pairs are taken in their flat order p = t * k + j, which
 // is the order of topk_idx and of the slot table in memory.  A warp handles
 // groups of 32 consecutive pairs: within a group, the pairs before p with the
-// same expert are the lanes below p's in __match_any_sync(e), and the groups of
+// same expert are the lanes below p's that hold the same id, and the groups of
 // a warp are consecutive, so per warp a running count per expert completes the
 // rank.  Across warps and chunks the counts are scanned per expert.
 //
@@ -35,9 +35,6 @@ constexpr int kXSingleWarps = 32;
 constexpr int kXSingleGroups = 8;
 #ifndef EP_XSINGLE_MAX
 #define EP_XSINGLE_MAX 2048
-#endif
-#ifndef EP_XMATCH_BALLOT
-#define EP_XMATCH_BALLOT 1
 #endif
 constexpr int64_t kXSingleMax = EP_XSINGLE_MAX;  // <= kXSingleWarps * kXSingleGroups * 32
 static_assert(kXSingleMax <= kXSingleWarps * kXSingleGroups * 32, "one CTA holds 8192 pairs");
@@ -108,10 +105,10 @@ __device__ void block_exclusive_scan(const int32_t* s_val, int32_t* s_out, int n
 }
 
 // Lanes whose pair has the same expert as this lane's (valid pairs only; an
-// invalid pair matches nobody and its result is not used).  With ballots: one
-// per bit of the expert id, nbits = bits of E - 1.
+// invalid pair matches nobody and its result is not used): one ballot per bit
+// of the expert id, nbits = bits of E - 1.  Measured on GB300 this is 1.3 to
+// 1.7 times faster in these kernels than __match_any_sync.
 __device__ __forceinline__ unsigned peers_of(int e, bool valid, int nbits) {
-#if EP_XMATCH_BALLOT
   unsigned m = __ballot_sync(kFull, valid);
   for (int b = 0; b < nbits; ++b) {
     const bool bit = (e >> b) & 1;
@@ -119,10 +116,6 @@ __device__ __forceinline__ unsigned peers_of(int e, bool valid, int nbits) {
     m &= bit ? v : ~v;
   }
   return m;
-#else
-  (void)nbits;
-  return __match_any_sync(kFull, valid ? e : -1 - (int)(threadIdx.x & 31));
-#endif
 }
 
 // Ranks of a warp's pairs, in flat order, given s_run[e] = the first row of

@@ -95,6 +95,20 @@ def test_e4m3_matches_torch_cast_within_range():
     np.testing.assert_array_equal(oracle.e4m3_from_f32(a), _torch_e4m3_codes(a))
 
 
+def test_e4m3_every_nonnegative_pattern_up_to_448_matches_torch():
+    """Every fp32 bit pattern from +0 to 448 (1.14e9 values, in chunks)
+    against PyTorch's float8_e4m3fn cast; negative values on a stride-7
+    subsample of the same range (the sign only sets bit 7)."""
+    lim = int(np.float32(448.0).view(np.uint32))
+    chunk = 1 << 24
+    for start in range(0, lim + 1, chunk):
+        bits = np.arange(start, min(start + chunk, lim + 1), dtype=np.uint32)
+        a = bits.view(np.float32)
+        assert np.array_equal(oracle.e4m3_from_f32(a), _torch_e4m3_codes(a)), start
+        neg = (bits[::7] | np.uint32(0x80000000)).view(np.float32)
+        assert np.array_equal(oracle.e4m3_from_f32(neg), _torch_e4m3_codes(neg)), start
+
+
 def _e4m3_nearest_bruteforce(a: np.ndarray) -> np.ndarray:
     """Nearest finite e4m3 value by exhaustive search over the value table in
     float64; ties to the code with an even mantissa; magnitudes >= 448 saturate."""

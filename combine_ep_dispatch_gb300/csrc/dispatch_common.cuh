@@ -31,30 +31,47 @@ __device__ __forceinline__ Dests token_dests(const int32_t* __restrict__ slot, i
   return d;
 }
 
+// One 32-bit word, whatever its type.
+__device__ __forceinline__ void st_b32(void* p, uint32_t v) {
+  asm volatile("st.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Metadata of one token for all its destinations: per destination row, k ids,
 // k weights and the source index (2k+1 words), written by the whole warp at
 // once ("perf(ep): optimize IntraNode dispatch kernel for MI350X", Technical
-// Details 4).
+// Details 4).  Lane j takes word j of the token (id j, weight j - k, or the
+// source index at j = 2k), reads it once, and stores it to every destination
+// row with one multiply-add for the address: no division, no per-destination
+// reloads.
 __device__ __forceinline__ void carry_metadata(const int32_t* __restrict__ topk_idx,
                                                const float* __restrict__ topk_w, int64_t t, int k,
                                                const Dests& d, int32_t* __restrict__ recv_topk_idx,
                                                float* __restrict__ recv_topk_w,
                                                int32_t* __restrict__ recv_src, int lane) {
   const int per = 2 * k + 1;
-  const int total = d.nd * per;
-  for (int base = 0; base < total; base += 32) {
-    const int i = base + lane;
-    const int dd = i / per;
-    const int j = i - dd * per;
-    const int row = __shfl_sync(kFull, d.my_row, dd & 31);
-    if (i < total) {
-      if (j < k) {
-        if (recv_topk_idx) recv_topk_idx[(int64_t)row * k + j] = __ldg(topk_idx + t * k + j);
-      } else if (j < 2 * k) {
-        if (recv_topk_w) recv_topk_w[(int64_t)row * k + (j - k)] = __ldg(topk_w + t * k + (j - k));
-      } else if (recv_src) {
-        recv_src[row] = (int32_t)t;
+  for (int w0 = 0; w0 < per; w0 += 32) {
+    const int j = w0 + lane;
+    uint32_t* col = nullptr;  // the word's address in receive row 0
+    uint32_t stride = 1, val = 0;
+    if (j < k) {
+      if (recv_topk_idx != nullptr) {
+        col = reinterpret_cast<uint32_t*>(recv_topk_idx) + j;
+        stride = (uint32_t)k;
+        val = (uint32_t)__ldg(topk_idx + t * k + j);
       }
+    } else if (j < 2 * k) {
+      if (recv_topk_w != nullptr) {
+        col = reinterpret_cast<uint32_t*>(recv_topk_w) + (j - k);
+        stride = (uint32_t)k;
+        val = __float_as_uint(__ldg(topk_w + t * k + (j - k)));
+      }
+    } else if (j == 2 * k && recv_src != nullptr) {
+      col = reinterpret_cast<uint32_t*>(recv_src);
+      val = (uint32_t)t;
+    }
+    for (int qq = 0; qq < d.nd; ++qq) {
+      const uint32_t row = (uint32_t)__shfl_sync(kFull, d.my_row, qq);
+      if (col != nullptr) st_b32(col + (uint64_t)row * stride, val);
     }
   }
 }

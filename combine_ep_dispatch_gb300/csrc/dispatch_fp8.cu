@@ -42,20 +42,23 @@ __device__ __forceinline__ float bf16x16_absmax(const uint32_t (&w)[8]) {
 }
 
 // fl(v / s), the IEEE quotient rounded to nearest even, from y = RN(1/s)
-// with fused multiply-adds: a first quotient q0 = RN(v y) lies within 1.5 ulp
-// of v / s, one correction q1 = RN(q0 + (v - s q0) y) brings it within one
-// ulp, and a second correction of q1 is the correctly rounded quotient by
-// Markstein's theorem (P. Markstein, IBM J. Res. Dev. 34(1), 1990: with y
-// within half an ulp of 1/s and q within one ulp of v/s, the residual
-// v - s q is exact and RN(q + (v - s q) y) = RN(v / s)).  The residual is
-// formed as s q - v and subtracted, which keeps the sign of a zero quotient.
-// Valid while nothing underflows or overflows: 2^-80 <= s <= 2^100 (a quotient
-// too small for that has an e4m3 code of zero either way).
+// with fused multiply-adds: q0 = RN(v y), then one correction
+// q1 = RN(q0 - (s q0 - v) y) (P. Markstein, IBM J. Res. Dev. 34(1), 1990).
+// For arbitrary fp32 operands a second correction is needed; here it is not.
+// v is a bf16 value (significand V, at most 8 bits) and s = fl(M/7) * 2^j for
+// the 8-bit significand M of the block's amax (block_scale), and every step
+// commutes with scaling by a power of two while q0, q1 stay normal: q0 and q1
+// are near v / s, and the residual s q0 - v is a multiple of 2^-137 for the
+// scales allowed here, so it is exact even when subnormal.  The 255 x 128
+// pairs (V, M) are then all the cases there are, and for each of them q1 is
+// fl(V / S), checked exhaustively in exact rational arithmetic
+// (tests/test_fp8_quotient.py).  q0 alone is wrong for a quarter of them.
+// The residual is formed as s q - v and subtracted, which keeps the sign of a
+// zero quotient.  Valid for 2^-80 <= s <= 2^100; a quotient below 2^-10, where
+// q1 may underflow, has an e4m3 code of zero (with its sign) either way.
 __device__ __forceinline__ float quotient_rn(float v, float s, float y) {
-  float q = __fmul_rn(v, y);
-  float r = __fmaf_rn(s, q, -v);
-  q = __fmaf_rn(-r, y, q);
-  r = __fmaf_rn(s, q, -v);
+  const float q = __fmul_rn(v, y);
+  const float r = __fmaf_rn(s, q, -v);
   return __fmaf_rn(-r, y, q);
 }
 
@@ -121,6 +124,7 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
                         float* __restrict__ recv_topk_w, int32_t* __restrict__ recv_src,
                         int nseg, int per_seg, int32_t* __restrict__ status) {
   __shared__ float s_q7[128], s_r7[128];
+  __shared__ int32_t s_dst[kDThreads / 32][32];  // per warp: rows of the unit's destinations
   if (threadIdx.x < 128) {
     const float q = __fdiv_rn((float)(128 + threadIdx.x), 7.0f);
     s_q7[threadIdx.x] = q;
@@ -129,6 +133,8 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
   __syncthreads();
   pdl_wait();
   const int lane = threadIdx.x & 31;
+  int32_t* const my_dst = s_dst[threadIdx.x >> 5];
+  const unsigned below = (1u << lane) - 1u;  // lanes under this one
   const int qb = lane >> 3, hl = lane & 7;  // block within the quad, lane within the block
   const int nb = H >> 7;
   const int n16 = H >> 3;
@@ -173,6 +179,7 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
   Dests d;
   d.nd = 0;
   d.my_row = -1;
+  int sc_row = -1;  // lane (qb, hl): row of destination hl, which receives block qb's scale
   while (u < units) {
     // the next step, and its loads
     int64_t u2 = u, t2 = t;
@@ -196,11 +203,14 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
       const bool keep = s_raw >= 0 && (int64_t)s_raw < cap;
       const bool over = s_raw >= 0 && (int64_t)s_raw >= cap;
       const unsigned dmask = __ballot_sync(kFull, keep);
-      const int r = nth_set_bit_of_lane(dmask, lane);
-      const int rowv = __shfl_sync(kFull, s_raw, r & 31);
+      // compact the destinations: lane i gets the row of the i-th one
+      __syncwarp();  // the previous unit's rows have been read
+      if (keep) my_dst[__popc(dmask & below)] = s_raw;
+      __syncwarp();
       d.nd = __popc(dmask);
-      d.my_row = r >= 0 ? rowv : -1;
+      d.my_row = lane < d.nd ? my_dst[lane] : -1;
       d.cap_err = __any_sync(kFull, over);
+      sc_row = hl < d.nd ? my_dst[hl] : -1;
       if (seg == 0) {
         cap_err |= d.cap_err;
         carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
@@ -219,26 +229,24 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
       sc[v] = sv;
       codes[v] = sv != 0.0f ? e4m3x16_of_quotients(w, sv, yv) : make_uint4(0u, 0u, 0u, 0u);
     }
-    // the lane's byte offsets in a row, and whether each of its blocks exists
-    bool has[U];
-    int boff[U];
+    // Codes: every destination gets the lane's 16 bytes of each of its
+    // blocks.  Scales: lane (qb, hl) writes block qb's scale to destinations
+    // hl, hl + 8, ... (one store per step while there are at most 8).
 #pragma unroll
     for (int v = 0; v < U; ++v) {
+      if (q0 + v >= q_end) continue;  // warp-uniform
       const int b = (q0 + v) * 4 + qb;
-      has[v] = q0 + v < q_end && b < nb;
-      boff[v] = b * 128 + hl * 16;
-    }
+      const bool has = b < nb;          // the last quadruple may be partial
+      uint8_t* const xb = recv_x + b * 128 + hl * 16;
 #pragma unroll 1
-    for (int qq = 0; qq < d.nd; ++qq) {  // the token's destinations only
-      const int64_t row = __shfl_sync(kFull, d.my_row, qq);
-      uint8_t* dst = recv_x + row * H;
-      float* dsc = recv_scale + row * nb;
-#pragma unroll
-      for (int v = 0; v < U; ++v) {
-        if (has[v]) {
-          st_v4(reinterpret_cast<uint4*>(dst + boff[v]), codes[v]);
-          if (hl == 0) dsc[(q0 + v) * 4 + qb] = sc[v];
-        }
+      for (int qq = 0; qq < d.nd; ++qq) {
+        const uint32_t row = (uint32_t)__shfl_sync(kFull, d.my_row, qq);
+        if (has) st_v4(reinterpret_cast<uint4*>(xb + (uint64_t)row * (uint32_t)H), codes[v]);
+      }
+      if (has) {
+        if (sc_row >= 0) recv_scale[(uint64_t)(uint32_t)sc_row * (uint32_t)nb + b] = sc[v];
+        for (int j = hl + 8; j < d.nd; j += 8)
+          recv_scale[(uint64_t)(uint32_t)my_dst[j] * (uint32_t)nb + b] = sc[v];
       }
     }
 #pragma unroll

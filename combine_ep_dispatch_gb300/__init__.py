@@ -12,7 +12,8 @@ from ._lib import (EP_ERR_CUDA, EP_ERR_INVALID_ARG, EP_ERR_MISALIGNED, EP_ERR_UN
                    ep_dispatch_layout, ep_dispatch_layout_noalloc, ep_layout_workspace_bytes, ep_max_recv_rows,
                    ep_status_string, load_library, ep_layout_experts_workspace_bytes,
                    ep_dispatch_layout_experts, ep_combine_weighted, ep_selftest_wait_timeout,
-                   EP_STATUS_TIMEOUT, ep_cast_transpose_t_bytes, ep_cast_transpose_experts)
+                   EP_STATUS_TIMEOUT, ep_cast_transpose_t_bytes, ep_cast_transpose_experts,
+                   ep_dispatch_with_layout, ep_dispatch_with_layout_launches)
 from .pipeline import DispatchCombine
 
 __all__ = [
@@ -23,5 +24,6 @@ __all__ = [
     "DispatchCombine", "ep_dispatch_fused", "EP_FUSED_MAX_TOKENS", "ep_localize_expert_ids",
     "ep_layout_experts_workspace_bytes", "ep_dispatch_layout_experts", "ep_combine_weighted",
     "ep_selftest_wait_timeout", "EP_STATUS_TIMEOUT", "ep_cast_transpose_t_bytes",
-    "ep_cast_transpose_experts",
+    "ep_cast_transpose_experts", "ep_dispatch_with_layout",
+    "ep_dispatch_with_layout_launches",
 ]

@@ -45,10 +45,12 @@ int64_t ep_max_recv_rows(int64_t T, int k, int W) {
   return T * min64(k, W);
 }
 
-int ep_dispatch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int W,
-                       int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
-                       int32_t* rank_offset, int32_t* slot, void* workspace,
-                       size_t workspace_bytes, int32_t* status, ep_stream_t stream) {
+namespace {
+
+int check_layout(const int32_t* topk_idx, int64_t T, int k, int E, int W,
+                 const int32_t* num_tokens_per_expert, const int32_t* num_tokens_per_rank,
+                 const int32_t* rank_offset, const int32_t* slot, const void* workspace,
+                 size_t workspace_bytes, const int32_t* status) {
   if (T < 0 || k < 1 || W < 1 || W > 32 || E < 1 || E > 8192 || E % W != 0)
     return EP_ERR_INVALID_ARG;
   if (T * min64(k, W) > kMaxRows || T > kMaxRows / W) return EP_ERR_UNSUPPORTED;
@@ -60,15 +62,13 @@ int ep_dispatch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int W,
       !aligned(num_tokens_per_rank, 4) || !aligned(rank_offset, 4) || !aligned(slot, 4) ||
       !aligned(workspace, 16) || !aligned(status, 4))
     return EP_ERR_MISALIGNED;
-  return from_cuda(ep::launch_layout(topk_idx, T, k, E, W, num_tokens_per_expert,
-                                     num_tokens_per_rank, rank_offset, slot, workspace, status,
-                                     reinterpret_cast<cudaStream_t>(stream)));
+  return EP_OK;
 }
 
-int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T, int H,
-                int k, int W, const int32_t* slot, int64_t capacity_rows, int quant, void* recv_x,
-                float* recv_scale, int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
-                int32_t* status, ep_stream_t stream) {
+int check_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T, int H,
+                   int k, int W, const int32_t* slot, int64_t capacity_rows, int quant,
+                   const void* recv_x, const float* recv_scale, const int32_t* recv_topk_idx,
+                   const float* recv_topk_w, const int32_t* recv_src, const int32_t* status) {
   if (T < 0 || H < 1 || k < 1 || W < 1 || W > 32 || capacity_rows < 0 || capacity_rows > kMaxRows)
     return EP_ERR_INVALID_ARG;
   if (quant != EP_QUANT_BF16 && quant != EP_QUANT_FP8_E4M3_B128) return EP_ERR_INVALID_ARG;
@@ -83,9 +83,59 @@ int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w, int
       !aligned(slot, 4) || !aligned(recv_scale, 4) || !aligned(recv_topk_idx, 4) ||
       !aligned(recv_topk_w, 4) || !aligned(recv_src, 4) || !aligned(status, 4))
     return EP_ERR_MISALIGNED;
+  return EP_OK;
+}
+
+}  // namespace
+
+int ep_dispatch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int W,
+                       int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                       int32_t* rank_offset, int32_t* slot, void* workspace,
+                       size_t workspace_bytes, int32_t* status, ep_stream_t stream) {
+  const int rc = check_layout(topk_idx, T, k, E, W, num_tokens_per_expert, num_tokens_per_rank,
+                              rank_offset, slot, workspace, workspace_bytes, status);
+  if (rc != EP_OK) return rc;
+  return from_cuda(ep::launch_layout(topk_idx, T, k, E, W, num_tokens_per_expert,
+                                     num_tokens_per_rank, rank_offset, slot, workspace, status,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T, int H,
+                int k, int W, const int32_t* slot, int64_t capacity_rows, int quant, void* recv_x,
+                float* recv_scale, int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
+                int32_t* status, ep_stream_t stream) {
+  const int rc = check_dispatch(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, quant,
+                                recv_x, recv_scale, recv_topk_idx, recv_topk_w, recv_src, status);
+  if (rc != EP_OK) return rc;
   return from_cuda(ep::launch_dispatch(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, quant,
                                        recv_x, recv_scale, recv_topk_idx, recv_topk_w, recv_src,
                                        status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ep_dispatch_with_layout_launches(int64_t T, int H, int W, int quant) {
+  if (T < 0 || H < 1 || W < 1 || W > 32) return -1;
+  if (quant != EP_QUANT_BF16 && quant != EP_QUANT_FP8_E4M3_B128) return -1;
+  return ep::dispatch_with_layout_launches(T, H, W, quant);
+}
+
+int ep_dispatch_with_layout(const void* x, const int32_t* topk_idx, const float* topk_w,
+                            int64_t T, int H, int k, int E, int W,
+                            int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                            int32_t* rank_offset, int32_t* slot, void* workspace,
+                            size_t workspace_bytes, int64_t capacity_rows, int quant,
+                            void* recv_x, float* recv_scale, int32_t* recv_topk_idx,
+                            float* recv_topk_w, int32_t* recv_src, int32_t* status,
+                            ep_stream_t stream) {
+  int rc = check_layout(topk_idx, T, k, E, W, num_tokens_per_expert, num_tokens_per_rank,
+                        rank_offset, slot, workspace, workspace_bytes, status);
+  if (rc != EP_OK) return rc;
+  rc = check_dispatch(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, quant, recv_x,
+                      recv_scale, recv_topk_idx, recv_topk_w, recv_src, status);
+  if (rc != EP_OK) return rc;
+  return from_cuda(ep::launch_dispatch_with_layout(
+      x, topk_idx, topk_w, T, H, k, E, W, num_tokens_per_expert, num_tokens_per_rank, rank_offset,
+      slot, workspace, capacity_rows, quant, recv_x, recv_scale, recv_topk_idx, recv_topk_w,
+      recv_src, status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int ep_dispatch_fused(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T,

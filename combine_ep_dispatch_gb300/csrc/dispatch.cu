@@ -93,18 +93,41 @@ constexpr int kL2EvictLast = 2;
 constexpr int kTmaCtasPerSm = EP_TMA_CTAS_PER_SM;
 constexpr uint32_t kTmaMinRowBytes = 1024;  // smaller rows: 16-byte stores from registers
 
-__device__ __forceinline__ int load_slot(const int32_t* __restrict__ slot, int64_t t, int W,
-                                         int lane, int64_t T) {
-  return (t < T && lane < W) ? __ldg(slot + t * W + lane) : -1;
+// A plain load: with a Finalize the kernel also writes the slot table (each
+// entry by the warp that read it, after reading it).
+__device__ __forceinline__ int load_slot(const int32_t* slot, int64_t t, int W, int lane,
+                                         int64_t T) {
+  return (t < T && lane < W) ? slot[t * W + lane] : -1;
 }
+
+// Finishing the layout inside the dispatch (ep_dispatch_with_layout): the slot
+// table holds each (t, r)'s position inside its chunk of 2^shift tokens, and
+// chunk_rank the chunks' per-rank counts.  Every CTA scans the counts over the
+// chunks per rank in shared memory (base row of chunk c on rank r =
+// rank_offset[r] + rows of r in chunks before c), each warp turns its tokens'
+// positions into receive rows and writes them back, CTA 0 writes the per-rank
+// totals and offsets, and the per-expert totals are summed across the grid.
+// chunk_rank == nullptr: the slot table is final (ordinary dispatch).
+struct Finalize {
+  const int32_t* chunk_rank;  // [C][W]
+  const int32_t* chunk_exp;   // [C][E]
+  int64_t C;
+  int shift;
+  int E;
+  int32_t* num_tokens_per_expert;
+  int32_t* num_tokens_per_rank;
+  int32_t* rank_offset;
+};
+constexpr int kFinMaxBytes = 16384;  // shared memory for the chunk table (C * W ints)
 
 __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
     dispatch_bf16_tma_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
                              const float* __restrict__ topk_w, int64_t T, uint32_t row_bytes,
-                             uint32_t stage_bytes, int k, int W, const int32_t* __restrict__ slot,
+                             uint32_t stage_bytes, int k, int W, int32_t* slot,
                              int64_t cap, uint8_t* __restrict__ recv_x,
                              int32_t* __restrict__ recv_topk_idx, float* __restrict__ recv_topk_w,
-                             int32_t* __restrict__ recv_src, int32_t* __restrict__ status) {
+                             int32_t* __restrict__ recv_src, int32_t* __restrict__ status,
+                             int x_early, Finalize fin) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta_warps = blockDim.x >> 5;
@@ -115,22 +138,82 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
     fence_barrier_init();
   }
   __syncwarp();
-  pdl_wait();
 
   const int64_t gw = (int64_t)blockIdx.x * cta_warps + warp;
   const int64_t NW = (int64_t)gridDim.x * cta_warps;
   const int64_t n = gw < T ? (T - 1 - gw) / NW + 1 : 0;  // tokens gw, gw+NW, ...
   int64_t issued = 0;                                      // tokens whose row load was issued
-  if (lane == 0) {
-    for (; issued < n && issued < kTmaStages; ++issued) {
-      mbar_arrive_expect_tx(&full[issued], row_bytes);
-      bulk_load(buf + issued * stage_bytes, x + (gw + issued * NW) * row_bytes, row_bytes,
-                &full[issued]);
+  // The first rows depend on x only.  With x_early (set only when this launch
+  // directly follows the layout kernels, whose own wait already covered x's
+  // producer) they are loaded while the layout still runs; otherwise after
+  // the wait, like every other access.
+  auto first_loads = [&](int64_t upto) {
+    if (lane == 0) {
+      for (; issued < n && issued < upto; ++issued) {
+        mbar_arrive_expect_tx(&full[issued], row_bytes);
+        bulk_load(buf + issued * stage_bytes, x + (gw + issued * NW) * row_bytes, row_bytes,
+                  &full[issued]);
+      }
+    }
+  };
+  if (x_early) first_loads(kTmaStages);
+  pdl_wait();
+  first_loads(kTmaStages);
+
+  const bool fin_mode = fin.chunk_rank != nullptr;  // uniform over the grid
+  __shared__ int32_t s_tot[32], s_off[33];
+  int32_t* const s_base =
+      reinterpret_cast<int32_t*>(smem + kTmaBarBytes + (size_t)cta_warps * kTmaStages * stage_bytes);
+  if (fin_mode) {
+    const int64_t n_ent = fin.C * W;
+    for (int64_t i = threadIdx.x; i < n_ent; i += blockDim.x) s_base[i] = fin.chunk_rank[i];
+    __syncthreads();
+    for (int r = warp; r < W; r += cta_warps) {  // exclusive scan of rank r over the chunks
+      int carry = 0;
+      for (int64_t c0 = 0; c0 < fin.C; c0 += 32) {
+        const int64_t c = c0 + lane;
+        const int v = c < fin.C ? s_base[c * W + r] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += u;
+        }
+        if (c < fin.C) s_base[c * W + r] = carry + incl - v;
+        carry += __shfl_sync(kFull, incl, 31);
+      }
+      if (lane == 0) s_tot[r] = carry;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int off = 0;
+      for (int r = 0; r < W; ++r) {
+        s_off[r] = off;
+        off += s_tot[r];
+      }
+      s_off[W] = off;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+      for (int i = threadIdx.x; i <= W; i += blockDim.x) {
+        fin.rank_offset[i] = s_off[i];
+        if (i < W) fin.num_tokens_per_rank[i] = s_tot[i];
+      }
     }
   }
+  // the receive row of (tt, lane) from its position inside the chunk, written
+  // back to the slot table
+  auto finalize = [&](int s_loc, int64_t tt) -> int {
+    if (!fin_mode || lane >= W || tt >= T) return s_loc;
+    const int s_fin =
+        s_loc >= 0 ? s_off[lane] + s_base[(tt >> fin.shift) * W + lane] + s_loc : -1;
+    slot[tt * W + lane] = s_fin;
+    return s_fin;
+  };
+
   const bool meta_lanes = 2 * k + 1 <= 32;
   bool cap_err = false, timed_out = false;
-  int s_cur = load_slot(slot, gw, W, lane, T);
+  int s_cur = finalize(load_slot(slot, gw, W, lane, T), gw);
   int64_t j = 0;
   for (; j < n; ++j) {
     const int64_t t = gw + j * NW;
@@ -195,7 +278,16 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
       ++issued;
     }
     issued = __shfl_sync(kFull, issued, 0);
-    s_cur = s_next;
+    s_cur = finalize(s_next, t + NW);
+  }
+  if (fin_mode) {  // per-expert totals: a warp per expert, the chunks over its lanes
+    for (int64_t e = blockIdx.x + (int64_t)warp * gridDim.x; e < fin.E;
+         e += (int64_t)cta_warps * gridDim.x) {
+      int sum = 0;
+      for (int64_t c = lane; c < fin.C; c += 32) sum += fin.chunk_exp[c * fin.E + e];
+      sum = warp_sum(sum);
+      if (lane == 0) fin.num_tokens_per_expert[e] = sum;
+    }
   }
   if (lane == 0) {
     // never leave with a bulk copy still using this CTA's shared memory
@@ -217,40 +309,68 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
                                 int64_t T, int H, int k, int W, const int32_t* slot,
                                 int64_t capacity_rows, void* recv_x, float* recv_scale,
                                 int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
-                                int32_t* status, cudaStream_t stream);
+                                int32_t* status, cudaStream_t stream, int x_early);
+
+namespace {
+
+// Launch shape of the bulk-copy kernel for rows of H bf16 values; false when
+// the register kernel serves this row size.
+struct TmaShape {
+  uint32_t row_bytes, stage_bytes;
+  int cta_warps;
+};
+bool tma_shape(int H, TmaShape* sh) {
+  sh->row_bytes = (uint32_t)H * 2u;
+  sh->stage_bytes = (sh->row_bytes + 127u) & ~127u;
+  const int fit = (int)(kTmaSmemBudget / ((size_t)kTmaStages * sh->stage_bytes));
+  sh->cta_warps = fit < kTmaMaxWarps ? fit : kTmaMaxWarps;
+  return !EP_FORCE_LSU && sh->row_bytes >= kTmaMinRowBytes && fit >= 1;
+}
+
+cudaError_t launch_tma(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T,
+                       int k, int W, int32_t* slot, int64_t capacity_rows, void* recv_x,
+                       int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
+                       int32_t* status, cudaStream_t stream, int x_early, const TmaShape& sh,
+                       const Finalize& fin) {
+  size_t smem = kTmaBarBytes + (size_t)sh.cta_warps * kTmaStages * sh.stage_bytes;
+  if (fin.chunk_rank != nullptr) smem += ((size_t)(fin.C * W) * sizeof(int32_t) + 15) & ~size_t(15);
+  static bool attr_set[128];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 128 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(dispatch_bf16_tma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTmaBarBytes + kTmaSmemBudget + kFinMaxBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int64_t want = (T + sh.cta_warps - 1) / sh.cta_warps;
+  const int64_t sms = (int64_t)device_sm_count() * kTmaCtasPerSm;
+  const int grid = (int)(want < sms ? want : sms);
+  return launch_pdl(dispatch_bf16_tma_kernel, dim3(grid < 1 ? 1 : grid), dim3(sh.cta_warps * 32),
+                    smem, stream, static_cast<const uint8_t*>(x), topk_idx, topk_w, T,
+                    sh.row_bytes, sh.stage_bytes, k, W, slot, capacity_rows,
+                    static_cast<uint8_t*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status,
+                    x_early, fin);
+}
+
+}  // namespace
 
 cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w,
                             int64_t T, int H, int k, int W, const int32_t* slot,
                             int64_t capacity_rows, int quant, void* recv_x, float* recv_scale,
                             int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
-                            int32_t* status, cudaStream_t stream) {
+                            int32_t* status, cudaStream_t stream, int x_early) {
   if (T == 0) return cudaSuccess;
   const uint4* x4 = static_cast<const uint4*>(x);
   if (quant == EP_QUANT_BF16) {
-    const uint32_t row_bytes = (uint32_t)H * 2u;
-    const uint32_t stage_bytes = (row_bytes + 127u) & ~127u;
-    const int cta_warps_fit = (int)(kTmaSmemBudget / ((size_t)kTmaStages * stage_bytes));
-    if (!EP_FORCE_LSU && row_bytes >= kTmaMinRowBytes && cta_warps_fit >= 1) {
-      const int cta_warps = cta_warps_fit < kTmaMaxWarps ? cta_warps_fit : kTmaMaxWarps;
-      const size_t smem = kTmaBarBytes + (size_t)cta_warps * kTmaStages * stage_bytes;
-      static bool attr_set[128];
-      int dev = 0;
-      cudaGetDevice(&dev);
-      if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(dispatch_bf16_tma_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kTmaBarBytes + kTmaSmemBudget);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-      }
-      const int64_t want = (T + cta_warps - 1) / cta_warps;
-      const int64_t sms = (int64_t)device_sm_count() * kTmaCtasPerSm;
-      const int grid = (int)(want < sms ? want : sms);
-      return launch_pdl(dispatch_bf16_tma_kernel, dim3(grid < 1 ? 1 : grid), dim3(cta_warps * 32),
-                        smem, stream, static_cast<const uint8_t*>(x), topk_idx, topk_w, T,
-                        row_bytes, stage_bytes, k, W, slot, capacity_rows,
-                        static_cast<uint8_t*>(recv_x), recv_topk_idx, recv_topk_w, recv_src,
-                        status);
+    TmaShape sh;
+    if (tma_shape(H, &sh)) {
+      Finalize none{};
+      // the kernel writes the slot table only with a Finalize
+      return launch_tma(x, topk_idx, topk_w, T, k, W, const_cast<int32_t*>(slot), capacity_rows,
+                        recv_x, recv_topk_idx, recv_topk_w, recv_src, status, stream, x_early,
+                        sh, none);
     }
     const int n16 = H / 8;
     if (n16 % (32 * 7) == 0) {
@@ -265,7 +385,51 @@ cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float*
                       static_cast<uint4*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status);
   }
   return launch_dispatch_fp8(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, recv_x,
-                            recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream);
+                            recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream,
+                            x_early);
+}
+
+namespace {
+bool finalize_applies(int64_t T, int H, int W, int quant, TmaShape* sh) {
+  return quant == EP_QUANT_BF16 && T > kLayoutSingleMaxT && tma_shape(H, sh) &&
+         layout_num_chunks(T) * W * (int64_t)sizeof(int32_t) <= kFinMaxBytes;
+}
+}  // namespace
+
+int dispatch_with_layout_launches(int64_t T, int H, int W, int quant) {
+  TmaShape sh;
+  if (finalize_applies(T, H, W, quant, &sh)) return 2;      // count, dispatch
+  const int layout = T <= kLayoutSingleMaxT ? 1 : 2;       // one CTA, or count + scan
+  return layout + (T > 0 ? 1 : 0);
+}
+
+cudaError_t launch_dispatch_with_layout(const void* x, const int32_t* topk_idx, const float* topk_w,
+                                        int64_t T, int H, int k, int E, int W,
+                                        int32_t* num_tokens_per_expert,
+                                        int32_t* num_tokens_per_rank, int32_t* rank_offset,
+                                        int32_t* slot, void* workspace, int64_t capacity_rows,
+                                        int quant, void* recv_x, float* recv_scale,
+                                        int32_t* recv_topk_idx, float* recv_topk_w,
+                                        int32_t* recv_src, int32_t* status, cudaStream_t stream) {
+  TmaShape sh;
+  if (finalize_applies(T, H, W, quant, &sh)) {
+    // count kernel (positions inside chunks) -> dispatch that finishes the layout
+    LayoutChunks ch;
+    cudaError_t e = launch_layout_count(topk_idx, T, k, E, W, workspace, slot, status, stream, &ch);
+    if (e != cudaSuccess) return e;
+    Finalize fin{ch.chunk_rank, ch.chunk_exp, ch.C, ch.shift, E, num_tokens_per_expert,
+                 num_tokens_per_rank, rank_offset};
+    return launch_tma(x, topk_idx, topk_w, T, k, W, slot, capacity_rows, recv_x, recv_topk_idx,
+                      recv_topk_w, recv_src, status, stream, /*x_early=*/1, sh, fin);
+  }
+  // the whole layout, then the dispatch, which loads its first rows of x while
+  // the layout kernels run
+  cudaError_t e = launch_layout(topk_idx, T, k, E, W, num_tokens_per_expert, num_tokens_per_rank,
+                                rank_offset, slot, workspace, status, stream);
+  if (e != cudaSuccess) return e;
+  return launch_dispatch(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, quant, recv_x,
+                         recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream,
+                         /*x_early=*/1);
 }
 
 }  // namespace ep

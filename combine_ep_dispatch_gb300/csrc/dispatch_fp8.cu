@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
                         const int32_t* __restrict__ slot, int64_t cap, uint8_t* __restrict__ recv_x,
                         float* __restrict__ recv_scale, int32_t* __restrict__ recv_topk_idx,
                         float* __restrict__ recv_topk_w, int32_t* __restrict__ recv_src,
-                        int nseg, int per_seg, int32_t* __restrict__ status) {
+                        int nseg, int per_seg, int32_t* __restrict__ status, int x_early) {
   __shared__ float s_q7[128], s_r7[128];
   __shared__ int32_t s_dst[kDThreads / 32][32];  // per warp: rows of the unit's destinations
   if (threadIdx.x < 128) {
@@ -131,7 +131,6 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
     s_r7[threadIdx.x] = __frcp_rn(q);
   }
   __syncthreads();
-  pdl_wait();
   const int lane = threadIdx.x & 31;
   int32_t* const my_dst = s_dst[threadIdx.x >> 5];
   const unsigned below = (1u << lane) - 1u;  // lanes under this one
@@ -171,9 +170,16 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
   int seg = 0, q0 = 0, q_end = 0;
   uint4 A[U], C[U];
   int s_raw = -1;  // the current unit's slot entry of this lane
+  // the first step's rows depend on x only: with x_early (this launch
+  // directly follows the layout kernels, whose wait covered x's producer) they
+  // are loaded before the wait
   if (u < units) {
     split(u, t, seg, q0, q_end);
-    load_step(t, q0, q_end, A, C);
+    if (x_early) load_step(t, q0, q_end, A, C);
+  }
+  pdl_wait();
+  if (u < units) {
+    if (!x_early) load_step(t, q0, q_end, A, C);
     s_raw = lane < W ? __ldg(slot + t * W + lane) : -1;
   }
   Dests d;
@@ -271,7 +277,7 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
                                 int64_t T, int H, int k, int W, const int32_t* slot,
                                 int64_t capacity_rows, void* recv_x, float* recv_scale,
                                 int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
-                                int32_t* status, cudaStream_t stream) {
+                                int32_t* status, cudaStream_t stream, int x_early) {
   if (T == 0) return cudaSuccess;
   const uint4* x4 = static_cast<const uint4*>(x);
   // segments per token: enough (token, segment) units to give every resident warp
@@ -294,7 +300,7 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
   return launch_pdl(kern, dim3((unsigned)(grid < 1 ? 1 : grid)), dim3(kDThreads), 0, stream, x4,
                     topk_idx, topk_w, T, H, k, W, slot, capacity_rows,
                     static_cast<uint8_t*>(recv_x), recv_scale, recv_topk_idx, recv_topk_w, recv_src,
-                    nseg, per_seg, status);
+                    nseg, per_seg, status, x_early);
 }
 
 }  // namespace ep

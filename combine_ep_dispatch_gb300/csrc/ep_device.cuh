@@ -205,11 +205,40 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
                           cudaStream_t stream);
 size_t layout_workspace_bytes(int64_t T, int W, int E);
 
+// Per-chunk counts the layout's count kernel leaves in its workspace: chunk c
+// holds tokens [c << shift, (c + 1) << shift).
+struct LayoutChunks {
+  const int32_t* chunk_rank;  // [C][W]  tokens of chunk c with r in D(t)
+  const int32_t* chunk_exp;   // [C][E]  (t, j) entries of chunk c with expert e
+  int64_t C;
+  int shift;
+};
+// The count kernel alone; with local_slot non-null it also writes each
+// (t, r)'s position inside its chunk there (-1 when r is not in D(t)).
+cudaError_t launch_layout_count(const int32_t* topk_idx, int64_t T, int k, int E, int W,
+                                void* workspace, int32_t* local_slot, int32_t* status,
+                                cudaStream_t stream, LayoutChunks* chunks);
+// T up to which launch_layout uses its one-CTA kernel.
+constexpr int64_t kLayoutSingleMaxT = 1024;
+int64_t layout_num_chunks(int64_t T);
+int dispatch_with_layout_launches(int64_t T, int H, int W, int quant);
+// ep_dispatch_with_layout: the layout, then the dispatch, launched so that the
+// dispatch overlaps the layout (and, for bf16 rows of 1 KB or more, finishes
+// the layout itself in place of the scan kernel).
+cudaError_t launch_dispatch_with_layout(const void* x, const int32_t* topk_idx, const float* topk_w,
+                                        int64_t T, int H, int k, int E, int W,
+                                        int32_t* num_tokens_per_expert,
+                                        int32_t* num_tokens_per_rank, int32_t* rank_offset,
+                                        int32_t* slot, void* workspace, int64_t capacity_rows,
+                                        int quant, void* recv_x, float* recv_scale,
+                                        int32_t* recv_topk_idx, float* recv_topk_w,
+                                        int32_t* recv_src, int32_t* status, cudaStream_t stream);
+
 cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w,
                             int64_t T, int H, int k, int W, const int32_t* slot,
                             int64_t capacity_rows, int quant, void* recv_x, float* recv_scale,
                             int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
-                            int32_t* status, cudaStream_t stream);
+                            int32_t* status, cudaStream_t stream, int x_early = 0);
 
 cudaError_t launch_localize_ids(int32_t* recv_topk_idx, const int32_t* rank_offset, int64_t cap,
                                 int k, int E, int W, cudaStream_t stream);

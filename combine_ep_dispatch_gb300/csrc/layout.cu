@@ -20,7 +20,8 @@ namespace {
 #ifndef EP_LAYOUT_SINGLE
 #define EP_LAYOUT_SINGLE 1
 #endif
-constexpr int kLT = 128;  // tokens per CTA, one per thread
+constexpr int kLTShift = 7;
+constexpr int kLT = 1 << kLTShift;  // tokens per CTA, one per thread
 constexpr int kLWarps = kLT / 32;
 
 inline size_t a256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -74,7 +75,8 @@ __device__ __forceinline__ void load_row(const int32_t* __restrict__ row, int k,
 template <int KV, bool VEC>
 __global__ void __launch_bounds__(kLT)
     layout_count_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k, int E, int W,
-                        int Er, LayoutWs ws, int32_t* __restrict__ status) {
+                        int Er, LayoutWs ws, int32_t* __restrict__ status,
+                        int32_t* __restrict__ local_slot) {
   pdl_wait();
   pdl_launch_dependents();
   extern __shared__ int32_t s_hist[];  // [E]
@@ -124,6 +126,21 @@ __global__ void __launch_bounds__(kLT)
     ws.chunk_rank[(int64_t)blockIdx.x * W + tid] = s;
   }
   for (int e = tid; e < E; e += kLT) ws.chunk_exp[(int64_t)blockIdx.x * E + e] = s_hist[e];
+
+  // Optionally the position of (t, r) inside the chunk: rows of r in earlier
+  // warps of the chunk plus rows of r in earlier lanes of this warp (-1 when r
+  // is not a destination).  A later kernel adds the chunk's base row.
+  if (local_slot != nullptr) {
+    const unsigned lt = lanemask_lt();
+    int32_t* srow = local_slot + (live ? t * W : 0);
+    for (int r = 0; r < W; ++r) {
+      const unsigned in_r = (m >> r) & 1u;
+      const unsigned b = __ballot_sync(kFull, in_r);
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += s_warp_rank[w][r];
+      if (live) srow[r] = in_r ? before + __popc(b & lt) : -1;
+    }
+  }
 }
 
 // Stable exclusive scan and slots.  The receive rows of rank r are
@@ -138,6 +155,7 @@ __global__ void __launch_bounds__(kLT)
                        int32_t* __restrict__ num_tokens_per_rank, int32_t* __restrict__ rank_offset,
                        int32_t* __restrict__ slot) {
   pdl_wait();
+  pdl_launch_dependents();  // the next kernel may become resident (its own wait still holds)
   __shared__ int32_t s_total[32], s_before[32];
   __shared__ int32_t s_warp_cnt[kLWarps][32];
   __shared__ int32_t s_base[kLWarps][32];
@@ -223,7 +241,6 @@ __global__ void __launch_bounds__(kLT)
       num_tokens_per_expert[e] = s;
     }
   }
-  pdl_launch_dependents();
 }
 
 // Whole layout in one CTA, for T <= kSingleMaxT: no workspace traffic and one
@@ -240,7 +257,7 @@ __global__ void __launch_bounds__(kLT)
 // the earlier lanes of its warp (ballot + popc).
 constexpr int kSingleThreads = 1024;
 constexpr int kSingleWarps = kSingleThreads / 32;
-constexpr int kSingleMaxT = 1024;
+constexpr int kSingleMaxT = (int)kLayoutSingleMaxT;
 constexpr int kSingleMaxBatches = kSingleMaxT / kSingleThreads;
 
 template <int KV, bool VEC>
@@ -251,6 +268,7 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
                          int32_t* __restrict__ rank_offset, int32_t* __restrict__ slot,
                          int32_t* __restrict__ status) {
   pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ int32_t s_dyn[];
   int32_t* s_hist = s_dyn;                                   // [E]
   uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_dyn + E);  // [T]
@@ -353,15 +371,40 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
     }
   }
   for (int e = tid; e < E; e += kSingleThreads) num_tokens_per_expert[e] = s_hist[e];
-  pdl_launch_dependents();
 }
 
 }  // namespace
+
+int64_t layout_num_chunks(int64_t T) { return num_chunks(T); }
 
 size_t layout_workspace_bytes(int64_t T, int W, int E) {
   const int64_t C = num_chunks(T);
   return a256(sizeof(uint32_t) * (size_t)T) + a256(sizeof(int32_t) * (size_t)(C * W)) +
          a256(sizeof(int32_t) * (size_t)(C * E));
+}
+
+cudaError_t launch_layout_count(const int32_t* topk_idx, int64_t T, int k, int E, int W,
+                                void* workspace, int32_t* local_slot, int32_t* status,
+                                cudaStream_t stream, LayoutChunks* chunks) {
+  const bool vec = (reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0;
+  const int64_t C = num_chunks(T);
+  const LayoutWs ws = carve(workspace, T, W);
+  chunks->chunk_rank = ws.chunk_rank;
+  chunks->chunk_exp = ws.chunk_exp;
+  chunks->C = C;
+  chunks->shift = kLTShift;
+  const size_t smem = sizeof(int32_t) * (size_t)E;
+  if (k == 8 && vec)
+    return launch_pdl(layout_count_kernel<8, true>, dim3((unsigned)C), dim3(kLT), smem, stream,
+                      topk_idx, T, k, E, W, E / W, ws, status, local_slot);
+  if (k == 4 && vec)
+    return launch_pdl(layout_count_kernel<4, true>, dim3((unsigned)C), dim3(kLT), smem, stream,
+                      topk_idx, T, k, E, W, E / W, ws, status, local_slot);
+  if (k <= 16)
+    return launch_pdl(layout_count_kernel<16, false>, dim3((unsigned)C), dim3(kLT), smem, stream,
+                      topk_idx, T, k, E, W, E / W, ws, status, local_slot);
+  return launch_pdl(layout_count_kernel<0, false>, dim3((unsigned)C), dim3(kLT), smem, stream,
+                    topk_idx, T, k, E, W, E / W, ws, status, local_slot);
 }
 
 cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int W,
@@ -411,16 +454,16 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
   cudaError_t err;
   if (k == 8 && vec)
     err = launch_pdl(layout_count_kernel<8, true>, dim3((unsigned)C), dim3(kLT), smem, stream,
-                     topk_idx, T, k, E, W, E / W, ws, status);
+                     topk_idx, T, k, E, W, E / W, ws, status, nullptr);
   else if (k == 4 && vec)
     err = launch_pdl(layout_count_kernel<4, true>, dim3((unsigned)C), dim3(kLT), smem, stream,
-                     topk_idx, T, k, E, W, E / W, ws, status);
+                     topk_idx, T, k, E, W, E / W, ws, status, nullptr);
   else if (k <= 16)
     err = launch_pdl(layout_count_kernel<16, false>, dim3((unsigned)C), dim3(kLT), smem, stream,
-                     topk_idx, T, k, E, W, E / W, ws, status);
+                     topk_idx, T, k, E, W, E / W, ws, status, nullptr);
   else
     err = launch_pdl(layout_count_kernel<0, false>, dim3((unsigned)C), dim3(kLT), smem, stream,
-                     topk_idx, T, k, E, W, E / W, ws, status);
+                     topk_idx, T, k, E, W, E / W, ws, status, nullptr);
   if (err != cudaSuccess) return err;
   return launch_pdl(layout_scan_kernel, dim3((unsigned)C), dim3(kLT), 0, stream, T, E, W, C, ws,
                     num_tokens_per_expert, num_tokens_per_rank, rank_offset, slot);

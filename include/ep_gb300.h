@@ -144,6 +144,41 @@ EP_API int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk
                 int32_t* status, ep_stream_t stream);
 
 /*
+ * Layout and dispatch in one call: ep_dispatch_layout followed by ep_dispatch
+ * on the same stream, with the same arguments, limits, results and errors as
+ * those two calls.  The layout's counts and slots are written as by
+ * ep_dispatch_layout.  What one call allows that two do not: the dispatch
+ * kernel is known to follow the layout kernels directly, so it becomes resident
+ * while they run and starts loading its first rows of x before the slots
+ * exist (x must be complete in stream order before this call, as it must
+ * before ep_dispatch).  For bf16 rows of at least 1 KB and T > 1024 the
+ * dispatch also finishes the layout: the count kernel numbers each token
+ * inside its chunk of 128 and the dispatch adds the chunk's base row, so the
+ * scan kernel is not launched (ep_dispatch_with_layout_launches).  The layout
+ * is the one of "perf(ep): optimize IntraNode dispatch kernel for MI350X",
+ * Technical Details 1; the dispatch follows the same page's Technical Details
+ * 1, 3 and 4.
+ */
+EP_API int ep_dispatch_with_layout(const void* x, const int32_t* topk_idx, const float* topk_w,
+                                   int64_t T, int H, int k, int E, int W,
+                                   int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                                   int32_t* rank_offset, int32_t* slot, void* workspace,
+                                   size_t workspace_bytes, int64_t capacity_rows, int quant,
+                                   void* recv_x, float* recv_scale, int32_t* recv_topk_idx,
+                                   float* recv_topk_w, int32_t* recv_src, int32_t* status,
+                                   ep_stream_t stream);
+
+/*
+ * Number of kernels one ep_dispatch_with_layout call with these sizes
+ * launches (for callers that count launches, e.g. to size a CUDA graph):
+ * 2 when the dispatch finishes the layout itself (bf16 rows of at least 1 KB,
+ * T > 1024, and a chunk table (ceil(T / 128) * W ints) of at most 16 KB), else
+ * the layout's kernels (1 for T <= 1024, else 2) plus 1 for the dispatch when
+ * T > 0.  Returns -1 for invalid arguments.  Host only.
+ */
+EP_API int ep_dispatch_with_layout_launches(int64_t T, int H, int W, int quant);
+
+/*
  * Local expert ids, in place, after ep_dispatch on the same stream: in receive
  * row s of rank r (rank_offset[r] <= s < rank_offset[r+1], s < capacity_rows)
  * each of the k ids e in recv_topk_idx[s] becomes e - r * (E / W) when e is a

@@ -95,3 +95,42 @@ def assert_rows_equal(got: np.ndarray, want: np.ndarray, what: str):
         j = np.nonzero(g[i] != w[i])[0][:8]
         raise AssertionError(f"{what}: {bad.size} rows differ, first row {i} cols {j}: "
                              f"got {g[i][j]} want {w[i][j]}")
+
+
+def run_with_layout(x: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, E: int, W: int,
+                    cap: int, quant: int, dev="cuda") -> dict:
+    """ep_dispatch_with_layout on sentinel-filled buffers: layout and dispatch
+    outputs of one call."""
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    i32 = dict(dtype=torch.int32, device=dev)
+    xd = to_dev_bf16(x, dev)
+    idx = torch.from_numpy(np.ascontiguousarray(topk_idx, np.int32)).to(dev)
+    w = torch.from_numpy(np.ascontiguousarray(topk_w, np.float32)).to(dev)
+    ne = torch.full((E,), SENT_I32, **i32)
+    nr = torch.full((W,), SENT_I32, **i32)
+    off = torch.full((W + 1,), SENT_I32, **i32)
+    slot = torch.full((T, W), SENT_I32, **i32)
+    ws = torch.full((max(ep.ep_layout_workspace_bytes(T, W, E), 16),), 0x5A, dtype=torch.uint8,
+                    device=dev)
+    if quant == ep.EP_QUANT_BF16:
+        rx = torch.full((cap, H), SENT_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+        rs = None
+    else:
+        rx = torch.full((cap, H), SENT_U8, dtype=torch.uint8, device=dev)
+        rs = torch.full((cap, H // 128), -7.0, dtype=torch.float32, device=dev)
+    ri = torch.full((cap, k), SENT_I32, **i32)
+    rw = torch.full((cap, k), -3.0, dtype=torch.float32, device=dev)
+    rsrc = torch.full((cap,), SENT_I32, **i32)
+    st = torch.zeros(1, **i32)
+    ep.ep_dispatch_with_layout(xd, idx, w, E, W, ne, nr, off, slot, ws, rx, ri, rw, rsrc, rs, quant,
+                               st)
+    torch.cuda.synchronize()
+    out = {"num_tokens_per_expert": ne.cpu().numpy(), "num_tokens_per_rank": nr.cpu().numpy(),
+           "rank_offset": off.cpu().numpy(), "slot": slot.cpu().numpy(),
+           "recv_x": u16(rx) if quant == ep.EP_QUANT_BF16 else rx.cpu().numpy(),
+           "recv_topk_idx": ri.cpu().numpy(), "recv_topk_w": rw.cpu().numpy(),
+           "recv_src": rsrc.cpu().numpy(), "status": int(st.item())}
+    if rs is not None:
+        out["recv_scale"] = rs.cpu().numpy()
+    return out

@@ -54,6 +54,14 @@ def test_size_queries(lib):
     assert ep.ep_layout_workspace_bytes(10, 33, 66) == 0
     for code in range(6):
         assert ep.ep_status_string(code).startswith("EP_")
+    # kernels per ep_dispatch_with_layout call
+    assert ep.ep_dispatch_with_layout_launches(4096, 7168, 8) == 2     # count + finishing dispatch
+    assert ep.ep_dispatch_with_layout_launches(4096, 7168, 8, 1) == 3  # FP8: count + scan + dispatch
+    assert ep.ep_dispatch_with_layout_launches(4096, 256, 8) == 3      # rows under 1 KB
+    assert ep.ep_dispatch_with_layout_launches(1024, 7168, 8) == 2     # one-CTA layout + dispatch
+    assert ep.ep_dispatch_with_layout_launches(0, 7168, 8) == 1
+    assert ep.ep_dispatch_with_layout_launches(300000, 7168, 8) == 3   # chunk table over 16 KB
+    assert ep.ep_dispatch_with_layout_launches(4096, 7168, 33) == -1
 
 
 # The calls below pass made-up device addresses that each violate one rule, so
@@ -116,6 +124,27 @@ def test_combine_rejects(lib, kw, code):
     out = None if kw.get("out_null") else A + kw.get("out_off", 0)
     rc = lib.ep_combine(A + kw.get("y_off", 0), A, 100, kw.get("H", 256), kw.get("W", 8), 800, out,
                         None, None)
+    assert rc == code
+
+
+@cpu_only
+@pytest.mark.parametrize("kw,code", [
+    (dict(W=33), _lib.EP_ERR_INVALID_ARG),                      # layout's check
+    (dict(E=100), _lib.EP_ERR_INVALID_ARG),                     # E % W != 0
+    (dict(ws=64), _lib.EP_ERR_WORKSPACE),                       # layout workspace too small
+    (dict(slot_off=2), _lib.EP_ERR_MISALIGNED),
+    (dict(H=12), _lib.EP_ERR_UNSUPPORTED),                      # dispatch's check: H % 8
+    (dict(H=200, quant=1), _lib.EP_ERR_UNSUPPORTED),            # FP8 needs H % 128
+    (dict(quant=7), _lib.EP_ERR_INVALID_ARG),
+    (dict(x_off=8), _lib.EP_ERR_MISALIGNED),
+    (dict(scale_null=True, quant=1), _lib.EP_ERR_INVALID_ARG),  # FP8 without recv_scale
+])
+def test_dispatch_with_layout_rejects(lib, kw, code):
+    scale = None if kw.get("scale_null") else A
+    rc = lib.ep_dispatch_with_layout(
+        A + kw.get("x_off", 0), A, A, 256, kw.get("H", 256), 8, kw.get("E", 256), kw.get("W", 8),
+        A, A, A, A + kw.get("slot_off", 0), A, kw.get("ws", 1 << 20), 2048, kw.get("quant", 0), A,
+        scale, A, A, A, None, None)
     assert rc == code
 
 

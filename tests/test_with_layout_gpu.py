@@ -1,0 +1,119 @@
+"""GPU parity of ep_dispatch_with_layout (layout and dispatch in one call,
+the dispatch loading x while the layout kernels run): every output against the
+oracle's layout and dispatch, bit for bit, on both layout paths (one CTA up to
+1024 tokens, count + scan above), both payloads, both dispatch kernels (bulk
+copies for rows of 1 KB and more, registers below)."""
+import numpy as np
+import pytest
+import torch
+
+import combine_ep_dispatch_gb300 as ep
+import oracle
+from combine_ep_dispatch_gb300.inputs import make_bf16, make_inputs, make_routing
+from gpu_util import SENT_BF16, SENT_I32, SENT_U8, assert_rows_equal, run_with_layout
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _check(x, idx, w, E, W, cap, quant):
+    lay = oracle.layout(idx, E, W)
+    want = oracle.dispatch(x, idx, w, lay["slot"], cap, quant)
+    got = run_with_layout(x, idx, w, E, W, cap, quant)
+    for key in ("num_tokens_per_expert", "num_tokens_per_rank", "rank_offset", "slot"):
+        assert_rows_equal(got[key], lay[key], key)
+    assert got["status"] == (lay["status"] | want["status"])
+    R = min(int(lay["rank_offset"][-1]), cap)
+    assert_rows_equal(got["recv_x"][:R], want["recv_x"][:R], "recv_x")
+    if quant == ep.EP_QUANT_FP8_E4M3_B128:
+        assert_rows_equal(got["recv_scale"][:R].view(np.uint32),
+                          want["recv_scale"][:R].view(np.uint32), "recv_scale")
+    assert_rows_equal(got["recv_topk_idx"][:R], want["recv_topk_idx"][:R], "recv_topk_idx")
+    assert_rows_equal(got["recv_topk_w"][:R].view(np.uint32),
+                      want["recv_topk_w"][:R].view(np.uint32), "recv_topk_w")
+    assert_rows_equal(got["recv_src"][:R], want["recv_src"][:R], "recv_src")
+    sent = SENT_BF16 if quant == ep.EP_QUANT_BF16 else SENT_U8
+    assert np.all(got["recv_x"][R:] == sent)
+    assert np.all(got["recv_src"][R:] == SENT_I32)
+    return got
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "dsv3", "dsv3_zipf_fp8", "qwen"])
+def test_workloads(name):
+    inp = make_inputs(name, seed=3)
+    cfg = inp["cfg"]
+    quant = ep.EP_QUANT_FP8_E4M3_B128 if cfg.quant == "fp8" else ep.EP_QUANT_BF16
+    _check(inp["x"], inp["topk_idx"], inp["topk_w"], cfg.E, cfg.W,
+           ep.ep_max_recv_rows(cfg.T, cfg.k, cfg.W), quant)
+
+
+@pytest.mark.parametrize("quant", [0, 1])
+@pytest.mark.parametrize("T,H,E,k,W", [
+    (1, 7168, 256, 8, 8),       # one token
+    (1024, 7168, 256, 8, 8),    # largest one-CTA layout
+    (1025, 7168, 256, 8, 8),    # smallest count + scan layout
+    (3001, 2048, 64, 6, 8),     # ragged chunks
+    (700, 256, 32, 4, 4),       # rows under 1 KB: the register dispatch kernel
+    (513, 1536, 96, 3, 6),
+])
+def test_shapes(T, H, E, k, W, quant):
+    if quant == ep.EP_QUANT_FP8_E4M3_B128 and H % 128:
+        pytest.skip("FP8 needs H % 128 == 0")
+    rng = np.random.default_rng(T * 7 + H + quant)
+    x = make_bf16(rng, (T, H))
+    idx = make_routing(rng, T, E, k, "uniform")
+    w = rng.random((T, k), dtype=np.float32)
+    _check(x, idx, w, E, W, ep.ep_max_recv_rows(T, k, W), quant)
+
+
+def test_empty_batch():
+    x = np.zeros((0, 7168), np.uint16)
+    idx = np.zeros((0, 8), np.int32)
+    w = np.zeros((0, 8), np.float32)
+    got = run_with_layout(x, idx, w, 256, 8, 16, ep.EP_QUANT_BF16)
+    assert np.all(got["num_tokens_per_rank"] == 0) and np.all(got["rank_offset"] == 0)
+    assert np.all(got["num_tokens_per_expert"] == 0) and got["status"] == 0
+
+
+def test_capacity_and_bad_ids_flagged():
+    rng = np.random.default_rng(5)
+    T, H, E, k, W = 2000, 1024, 64, 4, 8
+    x = make_bf16(rng, (T, H))
+    idx = make_routing(rng, T, E, k, "zipf")
+    idx[::17, 1] = E + 3   # invalid ids: ignored and flagged
+    idx[::29, 2] = -1
+    w = rng.random((T, k), dtype=np.float32)
+    got = _check(x, idx, w, E, W, 1500, ep.EP_QUANT_BF16)
+    assert got["status"] == ep.EP_STATUS_BAD_EXPERT | ep.EP_STATUS_CAPACITY
+
+
+def test_back_to_back_calls_match_separate_calls():
+    """Several steps in a row on one stream (each call's dispatch overlapping
+    its own layout, and the next call's layout following the dispatch): the
+    receive buffers after the last call equal the layout + dispatch calls'."""
+    dev = "cuda"
+    inps = [make_inputs("dsv3", seed=s) for s in (11, 12, 13)]
+    cfg = inps[0]["cfg"]
+    a = ep.DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, device=dev)
+    b = ep.DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, device=dev)
+    for inp in inps:
+        x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+        idx = torch.from_numpy(inp["topk_idx"]).to(dev)
+        w = torch.from_numpy(inp["topk_w"]).to(dev)
+        for _ in range(3):
+            a.layout_dispatch(x, idx, w)
+        b.layout(idx)
+        b.dispatch(x, idx, w)
+        torch.cuda.synchronize()
+        R = int(b.rank_offset[cfg.W].item())
+        assert torch.equal(a.slot, b.slot) and torch.equal(a.rank_offset, b.rank_offset)
+        assert torch.equal(a.recv_x[:R].view(torch.int16), b.recv_x[:R].view(torch.int16))
+        assert torch.equal(a.recv_src[:R], b.recv_src[:R])
+        assert int(a.status.item()) == 0

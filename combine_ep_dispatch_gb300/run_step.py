@@ -9,8 +9,9 @@ Combine reads the dispatched rows (identity experts; for the FP8 workload a
 bf16 dispatch of the same routing provides them).  --order expert runs the
 expert-major path (one row per (token, expert) pair, combine weighted by the
 gate weights); --fused uses the one-launch layout + dispatch (rank order,
-bf16, small batches); --cast-transpose adds the FP8 cast and transposed cast
-of the received rows (expert order).
+bf16, small batches); --with-layout uses the single layout + dispatch call
+(rank order); --cast-transpose adds the FP8 cast and transposed cast of the
+received rows (expert order).
 """
 from __future__ import annotations
 
@@ -31,6 +32,7 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--order", default="rank", choices=("rank", "expert"))
     ap.add_argument("--fused", action="store_true")
+    ap.add_argument("--with-layout", action="store_true")
     ap.add_argument("--cast-transpose", action="store_true")
     args = ap.parse_args(argv)
 
@@ -56,6 +58,8 @@ def main(argv=None):
     for _ in range(args.iters):
         if args.fused:
             dc.dispatch_fused(x, idx, w)
+        elif args.with_layout:
+            dc.layout_dispatch(x, idx, w)
         else:
             dc.layout(idx)
             dc.dispatch(x, idx, w)
@@ -66,7 +70,8 @@ def main(argv=None):
             ident.cast_transpose(scale)
         dc.combine(ident.recv_x, weights)
     torch.cuda.synchronize()
-    print(f"{args.workload} ({order}{', fused' if args.fused else ''}): T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} W={cfg.W} R={R} "
+    mode = ", fused" if args.fused else (", with layout" if args.with_layout else "")
+    print(f"{args.workload} ({order}{mode}): T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} W={cfg.W} R={R} "
           f"iters={args.iters} status={int(dc.status.item())}")
 
 

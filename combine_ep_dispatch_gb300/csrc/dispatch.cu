@@ -100,25 +100,6 @@ __device__ __forceinline__ int load_slot(const int32_t* slot, int64_t t, int W, 
   return (t < T && lane < W) ? slot[t * W + lane] : -1;
 }
 
-// Finishing the layout inside the dispatch (ep_dispatch_with_layout): the slot
-// table holds each (t, r)'s position inside its chunk of 2^shift tokens, and
-// chunk_rank the chunks' per-rank counts.  Every CTA scans the counts over the
-// chunks per rank in shared memory (base row of chunk c on rank r =
-// rank_offset[r] + rows of r in chunks before c), each warp turns its tokens'
-// positions into receive rows and writes them back, CTA 0 writes the per-rank
-// totals and offsets, and the per-expert totals are summed across the grid.
-// chunk_rank == nullptr: the slot table is final (ordinary dispatch).
-struct Finalize {
-  const int32_t* chunk_rank;  // [C][W]
-  const int32_t* chunk_exp;   // [C][E]
-  int64_t C;
-  int shift;
-  int E;
-  int32_t* num_tokens_per_expert;
-  int32_t* num_tokens_per_rank;
-  int32_t* rank_offset;
-};
-constexpr int kFinMaxBytes = 16384;  // shared memory for the chunk table (C * W ints)
 
 __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
     dispatch_bf16_tma_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
@@ -164,49 +145,12 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
   __shared__ int32_t s_tot[32], s_off[33];
   int32_t* const s_base =
       reinterpret_cast<int32_t*>(smem + kTmaBarBytes + (size_t)cta_warps * kTmaStages * stage_bytes);
-  if (fin_mode) {
-    const int64_t n_ent = fin.C * W;
-    for (int64_t i = threadIdx.x; i < n_ent; i += blockDim.x) s_base[i] = fin.chunk_rank[i];
-    __syncthreads();
-    for (int r = warp; r < W; r += cta_warps) {  // exclusive scan of rank r over the chunks
-      int carry = 0;
-      for (int64_t c0 = 0; c0 < fin.C; c0 += 32) {
-        const int64_t c = c0 + lane;
-        const int v = c < fin.C ? s_base[c * W + r] : 0;
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int u = __shfl_up_sync(kFull, incl, o);
-          if (lane >= o) incl += u;
-        }
-        if (c < fin.C) s_base[c * W + r] = carry + incl - v;
-        carry += __shfl_sync(kFull, incl, 31);
-      }
-      if (lane == 0) s_tot[r] = carry;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int off = 0;
-      for (int r = 0; r < W; ++r) {
-        s_off[r] = off;
-        off += s_tot[r];
-      }
-      s_off[W] = off;
-    }
-    __syncthreads();
-    if (blockIdx.x == 0) {
-      for (int i = threadIdx.x; i <= W; i += blockDim.x) {
-        fin.rank_offset[i] = s_off[i];
-        if (i < W) fin.num_tokens_per_rank[i] = s_tot[i];
-      }
-    }
-  }
-  // the receive row of (tt, lane) from its position inside the chunk, written
-  // back to the slot table
+  if (fin_mode) build_chunk_base(fin, W, s_base, s_tot, s_off);
+  // the receive row of (tt, lane), written back to the slot table (the warp
+  // owns token tt's entries)
   auto finalize = [&](int s_loc, int64_t tt) -> int {
     if (!fin_mode || lane >= W || tt >= T) return s_loc;
-    const int s_fin =
-        s_loc >= 0 ? s_off[lane] + s_base[(tt >> fin.shift) * W + lane] + s_loc : -1;
+    const int s_fin = final_slot(s_loc, tt, lane, W, fin.shift, s_base, s_off);
     slot[tt * W + lane] = s_fin;
     return s_fin;
   };
@@ -280,15 +224,7 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
     issued = __shfl_sync(kFull, issued, 0);
     s_cur = finalize(s_next, t + NW);
   }
-  if (fin_mode) {  // per-expert totals: a warp per expert, the chunks over its lanes
-    for (int64_t e = blockIdx.x + (int64_t)warp * gridDim.x; e < fin.E;
-         e += (int64_t)cta_warps * gridDim.x) {
-      int sum = 0;
-      for (int64_t c = lane; c < fin.C; c += 32) sum += fin.chunk_exp[c * fin.E + e];
-      sum = warp_sum(sum);
-      if (lane == 0) fin.num_tokens_per_expert[e] = sum;
-    }
-  }
+  if (fin_mode) finish_expert_totals(fin);
   if (lane == 0) {
     // never leave with a bulk copy still using this CTA's shared memory
     for (int64_t q = j; q < issued; ++q)
@@ -309,7 +245,8 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
                                 int64_t T, int H, int k, int W, const int32_t* slot,
                                 int64_t capacity_rows, void* recv_x, float* recv_scale,
                                 int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
-                                int32_t* status, cudaStream_t stream, int x_early);
+                                int32_t* status, cudaStream_t stream, int x_early,
+                                const Finalize& fin);
 
 namespace {
 
@@ -384,15 +321,21 @@ cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float*
                       topk_idx, topk_w, T, n16, k, W, slot, capacity_rows,
                       static_cast<uint4*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status);
   }
+  Finalize none{};
   return launch_dispatch_fp8(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, recv_x,
                             recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream,
-                            x_early);
+                            x_early, none);
 }
 
 namespace {
+// The dispatch finishes the layout (count kernel + dispatch, no scan kernel):
+// FP8 rows, or bf16 rows that take the bulk-copy kernel, beyond the one-CTA
+// layout's batches, with a chunk table that fits kFinMaxBytes.
 bool finalize_applies(int64_t T, int H, int W, int quant, TmaShape* sh) {
-  return quant == EP_QUANT_BF16 && T > kLayoutSingleMaxT && tma_shape(H, sh) &&
-         layout_num_chunks(T) * W * (int64_t)sizeof(int32_t) <= kFinMaxBytes;
+  if (T <= kLayoutSingleMaxT || layout_num_chunks(T) * W * (int64_t)sizeof(int32_t) > kFinMaxBytes)
+    return false;
+  if (quant == EP_QUANT_FP8_E4M3_B128) return true;
+  return quant == EP_QUANT_BF16 && tma_shape(H, sh);
 }
 }  // namespace
 
@@ -419,6 +362,10 @@ cudaError_t launch_dispatch_with_layout(const void* x, const int32_t* topk_idx, 
     if (e != cudaSuccess) return e;
     Finalize fin{ch.chunk_rank, ch.chunk_exp, ch.C, ch.shift, E, num_tokens_per_expert,
                  num_tokens_per_rank, rank_offset};
+    if (quant == EP_QUANT_FP8_E4M3_B128)
+      return launch_dispatch_fp8(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, recv_x,
+                                 recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream,
+                                 /*x_early=*/1, fin);
     return launch_tma(x, topk_idx, topk_w, T, k, W, slot, capacity_rows, recv_x, recv_topk_idx,
                       recv_topk_w, recv_src, status, stream, /*x_early=*/1, sh, fin);
   }

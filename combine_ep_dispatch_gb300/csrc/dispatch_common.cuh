@@ -76,6 +76,88 @@ __device__ __forceinline__ void carry_metadata(const int32_t* __restrict__ topk_
   }
 }
 
+// Finishing the layout inside a dispatch kernel (ep_dispatch_with_layout):
+// the slot table holds, for each kept (t, r), its position p inside its chunk
+// of 2^shift tokens encoded as -2 - p, and chunk_rank the chunks' per-rank
+// counts.  Every CTA scans the counts per rank over the chunks in shared
+// memory (build_chunk_base); a token's receive row on rank r is then
+// rank_offset[r] + rows of r in earlier chunks + p (final_slot).  Values >= -1
+// are final already, so a reader may meet either form.  chunk_rank ==
+// nullptr: the slot table is final (ordinary dispatch).
+struct Finalize {
+  const int32_t* chunk_rank;  // [C][W]
+  const int32_t* chunk_exp;   // [C][E]
+  int64_t C;
+  int shift;
+  int E;
+  int32_t* num_tokens_per_expert;
+  int32_t* num_tokens_per_rank;
+  int32_t* rank_offset;
+};
+constexpr int kFinMaxBytes = 16384;  // shared memory for the chunk table (C * W ints)
+
+// s_base[c * W + r] = rows of r in chunks before c; s_tot[r] = rows of r;
+// s_off[r] = rank_offset[r] (s_off[W] = R).  CTA 0 writes the per-rank totals
+// and offsets.  Every thread of the CTA must call it.
+__device__ __forceinline__ void build_chunk_base(const Finalize& fin, int W, int32_t* s_base,
+                                                 int32_t* s_tot, int32_t* s_off) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int64_t n_ent = fin.C * W;
+  for (int64_t i = threadIdx.x; i < n_ent; i += blockDim.x) s_base[i] = fin.chunk_rank[i];
+  __syncthreads();
+  for (int r = warp; r < W; r += nwarps) {  // exclusive scan of rank r over the chunks
+    int carry = 0;
+    for (int64_t c0 = 0; c0 < fin.C; c0 += 32) {
+      const int64_t c = c0 + lane;
+      const int v = c < fin.C ? s_base[c * W + r] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (c < fin.C) s_base[c * W + r] = carry + incl - v;
+      carry += __shfl_sync(kFull, incl, 31);
+    }
+    if (lane == 0) s_tot[r] = carry;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int off = 0;
+    for (int r = 0; r < W; ++r) {
+      s_off[r] = off;
+      off += s_tot[r];
+    }
+    s_off[W] = off;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i <= W; i += blockDim.x) {
+      fin.rank_offset[i] = s_off[i];
+      if (i < W) fin.num_tokens_per_rank[i] = s_tot[i];
+    }
+  }
+}
+
+// The receive row of (t, r) from an entry of the slot table.
+__device__ __forceinline__ int final_slot(int v, int64_t t, int r, int W, int shift,
+                                          const int32_t* s_base, const int32_t* s_off) {
+  return v <= -2 ? s_off[r] + s_base[(t >> shift) * W + r] + (-2 - v) : v;
+}
+
+// Per-expert totals over the chunks: a warp per expert, the chunks over its
+// lanes, the experts spread over the grid's warps.
+__device__ __forceinline__ void finish_expert_totals(const Finalize& fin) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int64_t e = blockIdx.x + (int64_t)warp * gridDim.x; e < fin.E;
+       e += (int64_t)nwarps * gridDim.x) {
+    int sum = 0;
+    for (int64_t c = lane; c < fin.C; c += 32) sum += fin.chunk_exp[c * fin.E + e];
+    sum = warp_sum(sum);
+    if (lane == 0) fin.num_tokens_per_expert[e] = sum;
+  }
+}
+
 template <typename K>
 inline int grid_for(K kernel, int64_t T, int threads) {
   static int cache[128];

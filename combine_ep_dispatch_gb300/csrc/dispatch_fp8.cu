@@ -119,10 +119,11 @@ template <int U>
 __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
     dispatch_fp8_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ topk_idx,
                         const float* __restrict__ topk_w, int64_t T, int H, int k, int W,
-                        const int32_t* __restrict__ slot, int64_t cap, uint8_t* __restrict__ recv_x,
+                        int32_t* slot, int64_t cap, uint8_t* __restrict__ recv_x,
                         float* __restrict__ recv_scale, int32_t* __restrict__ recv_topk_idx,
                         float* __restrict__ recv_topk_w, int32_t* __restrict__ recv_src,
-                        int nseg, int per_seg, int32_t* __restrict__ status, int x_early) {
+                        int nseg, int per_seg, int32_t* __restrict__ status, int x_early,
+                        Finalize fin) {
   __shared__ float s_q7[128], s_r7[128];
   __shared__ int32_t s_dst[kDThreads / 32][32];  // per warp: rows of the unit's destinations
   if (threadIdx.x < 128) {
@@ -178,9 +179,18 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
     if (x_early) load_step(t, q0, q_end, A, C);
   }
   pdl_wait();
+  // With a Finalize the slot table holds in-chunk positions: every CTA scans
+  // the chunk counts first; the warp taking a token's first segment writes
+  // its receive rows back (other segments may read either form).
+  extern __shared__ int32_t s_base[];  // [C][W] with a Finalize
+  __shared__ int32_t s_tot[32], s_off[33];
+  const bool fin_mode = fin.chunk_rank != nullptr;  // uniform over the grid
+  if (fin_mode) build_chunk_base(fin, W, s_base, s_tot, s_off);
+  // plain loads: with a Finalize the table is also written during the kernel
+  auto slot_entry = [&](int64_t tt) { return lane < W ? slot[tt * W + lane] : -1; };
   if (u < units) {
     if (!x_early) load_step(t, q0, q_end, A, C);
-    s_raw = lane < W ? __ldg(slot + t * W + lane) : -1;
+    s_raw = slot_entry(t);
   }
   Dests d;
   d.nd = 0;
@@ -195,7 +205,7 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
       u2 = u + nwarps;
       if (u2 < units) {
         split(u2, t2, seg2, q2, qe2);
-        s_raw2 = lane < W ? __ldg(slot + t2 * W + lane) : -1;
+        s_raw2 = slot_entry(t2);
       }
     }
     uint4 A2[U], C2[U];
@@ -206,6 +216,10 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
       for (int v = 0; v < U; ++v) A2[v] = C2[v] = make_uint4(0u, 0u, 0u, 0u);
     }
     if (q0 == seg * per_seg) {  // a unit's first step: its destinations and metadata
+      if (fin_mode && lane < W) {
+        s_raw = final_slot(s_raw, t, lane, W, fin.shift, s_base, s_off);
+        if (seg == 0) slot[t * W + lane] = s_raw;
+      }
       const bool keep = s_raw >= 0 && (int64_t)s_raw < cap;
       const bool over = s_raw >= 0 && (int64_t)s_raw >= cap;
       const unsigned dmask = __ballot_sync(kFull, keep);
@@ -267,6 +281,7 @@ __global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
     q_end = qe2;
     s_raw = s_raw2;
   }
+  if (fin_mode) finish_expert_totals(fin);
   pdl_launch_dependents();
   if (cap_err && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_CAPACITY);
 }
@@ -277,7 +292,8 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
                                 int64_t T, int H, int k, int W, const int32_t* slot,
                                 int64_t capacity_rows, void* recv_x, float* recv_scale,
                                 int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
-                                int32_t* status, cudaStream_t stream, int x_early) {
+                                int32_t* status, cudaStream_t stream, int x_early,
+                                const Finalize& fin) {
   if (T == 0) return cudaSuccess;
   const uint4* x4 = static_cast<const uint4*>(x);
   // segments per token: enough (token, segment) units to give every resident warp
@@ -297,10 +313,13 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
   const int64_t grid = (units * 32 + kDThreads - 1) / kDThreads < device_sm_count() * per_sm
                            ? (units * 32 + kDThreads - 1) / kDThreads
                            : (int64_t)device_sm_count() * per_sm;
-  return launch_pdl(kern, dim3((unsigned)(grid < 1 ? 1 : grid)), dim3(kDThreads), 0, stream, x4,
-                    topk_idx, topk_w, T, H, k, W, slot, capacity_rows,
+  const size_t smem =
+      fin.chunk_rank != nullptr ? ((size_t)(fin.C * W) * sizeof(int32_t) + 15) & ~size_t(15) : 0;
+  // the kernel writes the slot table only with a Finalize
+  return launch_pdl(kern, dim3((unsigned)(grid < 1 ? 1 : grid)), dim3(kDThreads), smem, stream, x4,
+                    topk_idx, topk_w, T, H, k, W, const_cast<int32_t*>(slot), capacity_rows,
                     static_cast<uint8_t*>(recv_x), recv_scale, recv_topk_idx, recv_topk_w, recv_src,
-                    nseg, per_seg, status, x_early);
+                    nseg, per_seg, status, x_early, fin);
 }
 
 }  // namespace ep

@@ -214,7 +214,8 @@ struct LayoutChunks {
   int shift;
 };
 // The count kernel alone; with local_slot non-null it also writes each
-// (t, r)'s position inside its chunk there (-1 when r is not in D(t)).
+// (t, r)'s position p inside its chunk there as -2 - p (-1 when r is not in
+// D(t)).
 cudaError_t launch_layout_count(const int32_t* topk_idx, int64_t T, int k, int E, int W,
                                 void* workspace, int32_t* local_slot, int32_t* status,
                                 cudaStream_t stream, LayoutChunks* chunks);

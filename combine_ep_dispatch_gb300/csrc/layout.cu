@@ -127,9 +127,10 @@ __global__ void __launch_bounds__(kLT)
   }
   for (int e = tid; e < E; e += kLT) ws.chunk_exp[(int64_t)blockIdx.x * E + e] = s_hist[e];
 
-  // Optionally the position of (t, r) inside the chunk: rows of r in earlier
-  // warps of the chunk plus rows of r in earlier lanes of this warp (-1 when r
-  // is not a destination).  A later kernel adds the chunk's base row.
+  // Optionally the position p of (t, r) inside the chunk (rows of r in earlier
+  // warps of the chunk plus rows of r in earlier lanes of this warp), stored
+  // as -2 - p so that it can never be mistaken for a receive row (>= 0) or for
+  // "not a destination" (-1).  A later kernel adds the chunk's base row.
   if (local_slot != nullptr) {
     const unsigned lt = lanemask_lt();
     int32_t* srow = local_slot + (live ? t * W : 0);
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(kLT)
       const unsigned b = __ballot_sync(kFull, in_r);
       int before = 0;
       for (int w = 0; w < warp; ++w) before += s_warp_rank[w][r];
-      if (live) srow[r] = in_r ? before + __popc(b & lt) : -1;
+      if (live) srow[r] = in_r ? -2 - (before + __popc(b & lt)) : -1;
     }
   }
 }

@@ -56,7 +56,8 @@ def test_size_queries(lib):
         assert ep.ep_status_string(code).startswith("EP_")
     # kernels per ep_dispatch_with_layout call
     assert ep.ep_dispatch_with_layout_launches(4096, 7168, 8) == 2     # count + finishing dispatch
-    assert ep.ep_dispatch_with_layout_launches(4096, 7168, 8, 1) == 3  # FP8: count + scan + dispatch
+    assert ep.ep_dispatch_with_layout_launches(4096, 7168, 8, 1) == 2  # FP8: count + finishing dispatch
+    assert ep.ep_dispatch_with_layout_launches(1024, 7168, 8, 1) == 2  # one-CTA layout + FP8 dispatch
     assert ep.ep_dispatch_with_layout_launches(4096, 256, 8) == 3      # rows under 1 KB
     assert ep.ep_dispatch_with_layout_launches(1024, 7168, 8) == 2     # one-CTA layout + dispatch
     assert ep.ep_dispatch_with_layout_launches(0, 7168, 8) == 1

@@ -383,6 +383,12 @@ def run_ours(args) -> dict | None:
                    "T": T, "H": H, "E": E, "k": k, "W": W, "R": R, "seed": args.seed,
                    "l2": "flushed before every step, outside the timed events: a 256 MiB write, then a 512 MiB read that evicts the write's dirty lines",
                    "parallelism": f"replicas x{world}"},
+        # this rank's timed steps (value and ms_per_step use the mean, max over ranks)
+        "step_stats_us": {"mean": round(statistics.fmean(step_ms) * 1e3, 2),
+                          "std": round(statistics.pstdev(step_ms) * 1e3, 2),
+                          "best": round(min(step_ms) * 1e3, 2),
+                          "median": round(statistics.median(step_ms) * 1e3, 2),
+                          "n": len(step_ms)},
         # per-kernel figures come from separate calls with events in between
         "us": {"step": round(s_ms * 1e3, 2), "layout": round(l_ms * 1e3, 2),
                "dispatch": round(d_ms * 1e3, 2), "combine": round(c_ms * 1e3, 2)},
@@ -390,6 +396,9 @@ def run_ours(args) -> dict | None:
                 "layout": round(gbs(nbytes["layout"], l_ms), 1),
                 "dispatch": round(gbs(nbytes["dispatch"], d_ms), 1),
                 "combine": round(gbs(nbytes["combine"], c_ms), 1),
+                "frac_of_nominal_8tbs": {"step": round(gbs(nbytes["step"], s_ms) / 8000.0, 4),
+                                         "dispatch": round(gbs(nbytes["dispatch"], d_ms) / 8000.0, 4),
+                                         "combine": round(gbs(nbytes["combine"], c_ms) / 8000.0, 4)},
                 "frac_of_peak": {"dispatch": round(gbs(nbytes["dispatch"], d_ms) / peak, 4),
                                  "combine": round(gbs(nbytes["combine"], c_ms) / peak, 4)},
                 "pages_convention": {"dispatch": round(pages_convention_gbs(R, H, 2, d_ms * 1e-3), 1),
@@ -551,16 +560,27 @@ def cpu_baseline(args, min_seconds: float = 10.0) -> dict:
 
     inp = make_inputs(WORKLOAD, seed=args.seed)
     T = inp["cfg"].T
-    total_b, total_s, n = 0, 0.0, 0
-    while total_s < min_seconds or n < 1:
-        t = time.perf_counter()
-        total_b += _oracle_run(inp, 0, T)
-        total_s += time.perf_counter() - t
-        n += 1
-    return {"value": round(total_b / total_s / 1e9, 3), "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"{n} whole steps of the workload (T={T}), layout+dispatch+combine, "
-                      f"{total_s:.1f} s on one host thread",
+    # one host thread pinned to one core (restored afterwards); at least 3
+    # whole steps, the median step reported
+    prev = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    core = min(prev) if prev else None
+    rates, total_s = [], 0.0
+    try:
+        if prev:
+            os.sched_setaffinity(0, {core})
+        while total_s < min_seconds or len(rates) < 3:
+            t = time.perf_counter()
+            b = _oracle_run(inp, 0, T)
+            dt = time.perf_counter() - t
+            rates.append(b / dt)
+            total_s += dt
+    finally:
+        if prev:
+            os.sched_setaffinity(0, prev)
+    return {"value": round(statistics.median(rates) / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "pinned_core": core,
+            "sample": f"{len(rates)} whole steps of the workload (T={T}), layout+dispatch+combine, "
+                      f"median step, {total_s:.1f} s on one host thread pinned to one core",
             **host_cpu()}
 
 

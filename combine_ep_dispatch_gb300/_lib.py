@@ -33,7 +33,7 @@ EXPORTED = ("ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_dispatch_layout
             "ep_localize_expert_ids", "ep_layout_experts_workspace_bytes",
             "ep_dispatch_layout_experts", "ep_combine_weighted", "ep_selftest_wait_timeout",
             "ep_cast_transpose_t_bytes", "ep_cast_transpose_experts", "ep_dispatch_with_layout",
-            "ep_dispatch_with_layout_launches")
+            "ep_dispatch_with_layout_launches", "ep_dispatch_experts_with_layout")
 
 # Largest batch ep_dispatch_fused takes.
 EP_FUSED_MAX_TOKENS = 1024
@@ -77,6 +77,10 @@ def load_library() -> ctypes.CDLL:
     lib.ep_dispatch_with_layout.argtypes = [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                                             ctypes.c_size_t, _I64, _I, _P, _P, _P, _P, _P, _P, _P]
     lib.ep_dispatch_with_layout.restype = _I
+    lib.ep_dispatch_experts_with_layout.argtypes = [_P, _P, _P, _I64, _I, _I, _I, _P, _P, _P, _P,
+                                                    ctypes.c_size_t, _I64, _I, _P, _P, _P, _P, _P,
+                                                    _P, _P]
+    lib.ep_dispatch_experts_with_layout.restype = _I
     lib.ep_dispatch_with_layout_launches.argtypes = [_I64, _I, _I, _I]
     lib.ep_dispatch_with_layout_launches.restype = _I
     lib.ep_combine.argtypes = [_P, _P, _I64, _I, _I, _I64, _P, _P, _P]
@@ -233,6 +237,41 @@ def ep_dispatch_with_layout(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: tor
         _ptr(recv_scale), _ptr(recv_topk_idx), _ptr(recv_topk_w), _ptr(recv_src), _ptr(status),
         _stream(stream))
     _raise("ep_dispatch_with_layout", rc)
+
+
+def ep_dispatch_experts_with_layout(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                                    E: int, num_tokens_per_expert: torch.Tensor,
+                                    expert_offset: torch.Tensor, slot: torch.Tensor,
+                                    workspace: torch.Tensor, recv_x: torch.Tensor,
+                                    recv_topk_idx: torch.Tensor | None = None,
+                                    recv_topk_w: torch.Tensor | None = None,
+                                    recv_src: torch.Tensor | None = None,
+                                    recv_scale: torch.Tensor | None = None,
+                                    quant: int = EP_QUANT_BF16, status: torch.Tensor | None = None,
+                                    stream=None) -> None:
+    """ep_dispatch_layout_experts + ep_dispatch (W = k) in one call (the
+    dispatch starts loading x while the layout runs)."""
+    for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
+                 ("expert_offset", expert_offset), ("slot", slot)):
+        _check_cuda(n, t, torch.int32)
+    _check_cuda("workspace", workspace)
+    _check_cuda("x", x, torch.bfloat16)
+    _check_cuda("topk_w", topk_w, torch.float32)
+    _check_cuda("recv_x", recv_x, torch.bfloat16 if quant == EP_QUANT_BF16 else torch.uint8)
+    _check_cuda("recv_topk_idx", recv_topk_idx, torch.int32, optional=True)
+    _check_cuda("recv_topk_w", recv_topk_w, torch.float32, optional=True)
+    _check_cuda("recv_src", recv_src, torch.int32, optional=True)
+    _check_cuda("recv_scale", recv_scale, torch.float32, optional=quant == EP_QUANT_BF16)
+    _check_cuda("status", status, torch.int32, optional=True)
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    rc = load_library().ep_dispatch_experts_with_layout(
+        _ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, E, _ptr(num_tokens_per_expert),
+        _ptr(expert_offset), _ptr(slot), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), recv_x.shape[0], quant, _ptr(recv_x),
+        _ptr(recv_scale), _ptr(recv_topk_idx), _ptr(recv_topk_w), _ptr(recv_src), _ptr(status),
+        _stream(stream))
+    _raise("ep_dispatch_experts_with_layout", rc)
 
 
 def ep_dispatch_with_layout_launches(T: int, H: int, W: int, quant: int = EP_QUANT_BF16) -> int:

@@ -193,10 +193,11 @@ size_t ep_layout_experts_workspace_bytes(int64_t T, int k, int E) {
   return ep::layout_experts_workspace_bytes(T, k, E);
 }
 
-int ep_dispatch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,
-                               int32_t* num_tokens_per_expert, int32_t* expert_offset,
-                               int32_t* slot, void* workspace, size_t workspace_bytes,
-                               int32_t* status, ep_stream_t stream) {
+namespace {
+int check_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,
+                         const int32_t* num_tokens_per_expert, const int32_t* expert_offset,
+                         const int32_t* slot, const void* workspace, size_t workspace_bytes,
+                         const int32_t* status) {
   if (T < 0 || k < 1 || E < 1 || E > ep::layout_experts_max_experts()) return EP_ERR_INVALID_ARG;
   if (T > kMaxRows / k) return EP_ERR_UNSUPPORTED;
   if (!num_tokens_per_expert || !expert_offset || !workspace) return EP_ERR_INVALID_ARG;
@@ -205,9 +206,46 @@ int ep_dispatch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,
   if (!aligned(topk_idx, 4) || !aligned(num_tokens_per_expert, 4) || !aligned(expert_offset, 4) ||
       !aligned(slot, 4) || !aligned(workspace, 16) || !aligned(status, 4))
     return EP_ERR_MISALIGNED;
+  return EP_OK;
+}
+}  // namespace
+
+int ep_dispatch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,
+                               int32_t* num_tokens_per_expert, int32_t* expert_offset,
+                               int32_t* slot, void* workspace, size_t workspace_bytes,
+                               int32_t* status, ep_stream_t stream) {
+  const int rc = check_layout_experts(topk_idx, T, k, E, num_tokens_per_expert, expert_offset,
+                                      slot, workspace, workspace_bytes, status);
+  if (rc != EP_OK) return rc;
   return from_cuda(ep::launch_layout_experts(topk_idx, T, k, E, num_tokens_per_expert,
                                              expert_offset, slot, workspace, status,
                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ep_dispatch_experts_with_layout(const void* x, const int32_t* topk_idx, const float* topk_w,
+                                    int64_t T, int H, int k, int E,
+                                    int32_t* num_tokens_per_expert, int32_t* expert_offset,
+                                    int32_t* slot, void* workspace, size_t workspace_bytes,
+                                    int64_t capacity_rows, int quant, void* recv_x,
+                                    float* recv_scale, int32_t* recv_topk_idx, float* recv_topk_w,
+                                    int32_t* recv_src, int32_t* status, ep_stream_t stream) {
+  int rc = check_layout_experts(topk_idx, T, k, E, num_tokens_per_expert, expert_offset, slot,
+                                workspace, workspace_bytes, status);
+  if (rc != EP_OK) return rc;
+  // the dispatch of the [T, k] slot table: W = k columns
+  if (k > 32) return EP_ERR_UNSUPPORTED;
+  rc = check_dispatch(x, topk_idx, topk_w, T, H, k, k, slot, capacity_rows, quant, recv_x,
+                      recv_scale, recv_topk_idx, recv_topk_w, recv_src, status);
+  if (rc != EP_OK) return rc;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = from_cuda(ep::launch_layout_experts(topk_idx, T, k, E, num_tokens_per_expert, expert_offset,
+                                           slot, workspace, status, s));
+  if (rc != EP_OK) return rc;
+  // the dispatch follows the layout kernels directly: its first rows of x are
+  // loaded while they run
+  return from_cuda(ep::launch_dispatch(x, topk_idx, topk_w, T, H, k, k, slot, capacity_rows, quant,
+                                       recv_x, recv_scale, recv_topk_idx, recv_topk_w, recv_src,
+                                       status, s, /*x_early=*/1));
 }
 
 int ep_combine_weighted(const void* y, const int32_t* slot, const float* w, int64_t T, int H,

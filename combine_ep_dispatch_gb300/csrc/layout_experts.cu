@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(kXSingleWarps * 32, 1)
                           int32_t* __restrict__ expert_offset, int32_t* __restrict__ slot,
                           int32_t* __restrict__ status) {
   pdl_wait();
+  pdl_launch_dependents();  // the next kernel may become resident (its own wait still holds)
   extern __shared__ int32_t s_dyn[];
   int32_t* s_cnt = s_dyn;                          // [32][E]
   int32_t* s_tot = s_cnt + kXSingleWarps * E;      // [E]
@@ -222,7 +223,6 @@ __global__ void __launch_bounds__(kXSingleWarps * 32, 1)
     const int64_t p = base + (int64_t)i * 32 + lane;
     if (i < ng && p < P) slot[p] = row[i];
   }
-  pdl_launch_dependents();
 }
 
 // Chunk c: per-expert counts of its kXPairs pairs.
@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(kXWarps * 32)
 __global__ void __launch_bounds__(kXWarps * 32)
     xlayout_scan_kernel(int64_t C, int E, XWs ws, int32_t* __restrict__ num_tokens_per_expert) {
   pdl_wait();
+  pdl_launch_dependents();
   __shared__ int32_t s_part[kXWarps][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x * 32 + lane;
@@ -290,7 +291,6 @@ __global__ void __launch_bounds__(kXWarps * 32)
       num_tokens_per_expert[e] = total;
     }
   }
-  pdl_launch_dependents();
 }
 
 // Chunk c: expert offsets from the totals, then the slots of its pairs.
@@ -303,6 +303,7 @@ __global__ void __launch_bounds__(kXWarps * 32)
                           int64_t C, int32_t* __restrict__ num_tokens_per_expert,
                           int32_t* __restrict__ expert_offset, int32_t* __restrict__ slot) {
   pdl_wait();
+  pdl_launch_dependents();  // the next kernel may become resident (its own wait still holds)
   extern __shared__ int32_t s_dyn[];
   int32_t* s_cnt = s_dyn;                  // [kXWarps][E]
   int32_t* s_tot = s_cnt + kXWarps * E;    // [E]
@@ -355,7 +356,6 @@ __global__ void __launch_bounds__(kXWarps * 32)
     const int64_t p = base + (int64_t)i * 32 + lane;
     if (p < P) slot[p] = row[i];
   }
-  pdl_launch_dependents();
 }
 
 cudaError_t set_smem(const void* fn, size_t bytes, bool* done) {

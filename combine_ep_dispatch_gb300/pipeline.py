@@ -82,10 +82,14 @@ class DispatchCombine:
 
     def layout_dispatch(self, x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
                         stream=None) -> None:
-        """layout() then dispatch() in one library call (rank order): the same
-        results, with the dispatch loading x while the layout kernels run."""
-        if self.order != "rank":
-            raise ValueError("layout_dispatch builds the rank-major layout")
+        """layout() then dispatch() in one library call: the same results, with
+        the dispatch loading x while the layout kernels run."""
+        if self.order == "expert":
+            _lib.ep_dispatch_experts_with_layout(
+                x, topk_idx, topk_w, self.E, self.num_tokens_per_expert, self.expert_offset,
+                self.slot, self.workspace, self.recv_x, self.recv_topk_idx, self.recv_topk_w,
+                self.recv_src, self.recv_scale, self.quant, self.status, stream)
+            return
         _lib.ep_dispatch_with_layout(x, topk_idx, topk_w, self.E, self.W,
                                      self.num_tokens_per_expert, self.num_tokens_per_rank,
                                      self.rank_offset, self.slot, self.workspace, self.recv_x,
@@ -145,9 +149,5 @@ class DispatchCombine:
         return self.recv_fp8, self.recv_fp8_t, amax
 
     def step(self, x, topk_idx, topk_w, y=None, stream=None) -> torch.Tensor:
-        if self.order == "rank":
-            self.layout_dispatch(x, topk_idx, topk_w, stream)
-        else:
-            self.layout(topk_idx, stream)
-            self.dispatch(x, topk_idx, topk_w, stream)
+        self.layout_dispatch(x, topk_idx, topk_w, stream)
         return self.combine(y, topk_w if self.order == "expert" else None, stream)

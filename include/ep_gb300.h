@@ -294,6 +294,24 @@ EP_API int ep_dispatch_layout_experts(const int32_t* topk_idx, int64_t T, int k,
                                       int32_t* status, ep_stream_t stream);
 
 /*
+ * Expert-major layout and dispatch in one call: ep_dispatch_layout_experts
+ * followed by ep_dispatch of its [T, k] slot table (W = k) on the same stream,
+ * with the same arguments, limits (also k <= 32), results and errors.  The
+ * dispatch becomes resident while the layout kernels run and loads its first
+ * rows of x before the slots exist (x must be complete in stream order before
+ * this call).
+ */
+EP_API int ep_dispatch_experts_with_layout(const void* x, const int32_t* topk_idx,
+                                           const float* topk_w, int64_t T, int H, int k, int E,
+                                           int32_t* num_tokens_per_expert,
+                                           int32_t* expert_offset, int32_t* slot, void* workspace,
+                                           size_t workspace_bytes, int64_t capacity_rows,
+                                           int quant, void* recv_x, float* recv_scale,
+                                           int32_t* recv_topk_idx, float* recv_topk_w,
+                                           int32_t* recv_src, int32_t* status,
+                                           ep_stream_t stream);
+
+/*
  * Weighted combine over a slot table of C columns:
  *   out[t] = bf16_rne( fma(w[t][c_n], y[s_n], ... fma(w[t][c_1], y[s_1], +0)) )
  * over the columns c with s = slot[t][c] >= 0 in ascending order, each step one

@@ -151,6 +151,22 @@ def test_dispatch_with_layout_rejects(lib, kw, code):
 
 @cpu_only
 @pytest.mark.parametrize("kw,code", [
+    (dict(E=5000), _lib.EP_ERR_INVALID_ARG),                    # expert layout's check
+    (dict(ws=64), _lib.EP_ERR_WORKSPACE),
+    (dict(k=40), _lib.EP_ERR_UNSUPPORTED),                      # k slot columns > 32
+    (dict(H=12), _lib.EP_ERR_UNSUPPORTED),                      # dispatch's check
+    (dict(x_off=8), _lib.EP_ERR_MISALIGNED),
+    (dict(quant=5), _lib.EP_ERR_INVALID_ARG),
+])
+def test_experts_with_layout_rejects(lib, kw, code):
+    rc = lib.ep_dispatch_experts_with_layout(
+        A + kw.get("x_off", 0), A, A, 256, kw.get("H", 256), kw.get("k", 8), kw.get("E", 256), A, A,
+        A, A, kw.get("ws", 1 << 20), 2048, kw.get("quant", 0), A, A, A, A, A, None, None)
+    assert rc == code
+
+
+@cpu_only
+@pytest.mark.parametrize("kw,code", [
     (dict(T=1025), _lib.EP_ERR_UNSUPPORTED),                    # beyond EP_FUSED_MAX_TOKENS
     (dict(k=17), _lib.EP_ERR_UNSUPPORTED),
     (dict(H=12), _lib.EP_ERR_UNSUPPORTED),

@@ -117,3 +117,68 @@ def test_back_to_back_calls_match_separate_calls():
         assert torch.equal(a.recv_x[:R].view(torch.int16), b.recv_x[:R].view(torch.int16))
         assert torch.equal(a.recv_src[:R], b.recv_src[:R])
         assert int(a.status.item()) == 0
+
+
+# ------------------------------------------------------------ expert-major
+
+def _run_experts_with_layout(x, idx, w, E, cap, quant):
+    T, H = x.shape
+    k = idx.shape[1]
+    i32 = dict(dtype=torch.int32, device="cuda")
+    from gpu_util import to_dev_bf16, u16
+    ne = torch.full((E,), SENT_I32, **i32)
+    off = torch.full((E + 1,), SENT_I32, **i32)
+    slot = torch.full((T, k), SENT_I32, **i32)
+    ws = torch.full((max(ep.ep_layout_experts_workspace_bytes(T, k, E), 16),), 0x5A,
+                    dtype=torch.uint8, device="cuda")
+    if quant == ep.EP_QUANT_BF16:
+        rx = torch.full((cap, H), SENT_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        rs = None
+    else:
+        rx = torch.full((cap, H), SENT_U8, dtype=torch.uint8, device="cuda")
+        rs = torch.full((cap, H // 128), -7.0, dtype=torch.float32, device="cuda")
+    ri = torch.full((cap, k), SENT_I32, **i32)
+    rw = torch.full((cap, k), -3.0, dtype=torch.float32, device="cuda")
+    rsrc = torch.full((cap,), SENT_I32, **i32)
+    st = torch.zeros(1, **i32)
+    ep.ep_dispatch_experts_with_layout(
+        to_dev_bf16(x), torch.from_numpy(np.ascontiguousarray(idx, np.int32)).cuda(),
+        torch.from_numpy(np.ascontiguousarray(w, np.float32)).cuda(), E, ne, off, slot, ws, rx,
+        ri, rw, rsrc, rs, quant, st)
+    torch.cuda.synchronize()
+    out = {"num_tokens_per_expert": ne.cpu().numpy(), "expert_offset": off.cpu().numpy(),
+           "slot": slot.cpu().numpy(),
+           "recv_x": u16(rx) if quant == ep.EP_QUANT_BF16 else rx.cpu().numpy(),
+           "recv_topk_idx": ri.cpu().numpy(), "recv_topk_w": rw.cpu().numpy(),
+           "recv_src": rsrc.cpu().numpy(), "status": int(st.item())}
+    if rs is not None:
+        out["recv_scale"] = rs.cpu().numpy()
+    return out
+
+
+@pytest.mark.parametrize("quant", [0, 1])
+@pytest.mark.parametrize("T,H,E,k", [
+    (200, 1024, 64, 8),       # one-CTA expert layout (<= 2048 pairs)
+    (4096, 7168, 256, 8),     # dsv3 shape: count + assign kernels
+    (3001, 512, 48, 6),       # ragged; rows under 1 KB take the register kernel (bf16)
+])
+def test_experts_with_layout(T, H, E, k, quant):
+    rng = np.random.default_rng(T + H + quant)
+    x = make_bf16(rng, (T, H))
+    idx = make_routing(rng, T, E, k, "zipf")
+    w = rng.random((T, k), dtype=np.float32)
+    lay = oracle.layout_experts(idx, E)
+    R = int(lay["expert_offset"][-1])
+    want = oracle.dispatch(x, idx, w, lay["slot"], R, quant)
+    got = _run_experts_with_layout(x, idx, w, E, R, quant)
+    for key in ("num_tokens_per_expert", "expert_offset", "slot"):
+        assert_rows_equal(got[key], lay[key], key)
+    assert got["status"] == (lay["status"] | want["status"]) == 0
+    assert_rows_equal(got["recv_x"], want["recv_x"], "recv_x")
+    if quant == ep.EP_QUANT_FP8_E4M3_B128:
+        assert_rows_equal(got["recv_scale"].view(np.uint32), want["recv_scale"].view(np.uint32),
+                          "recv_scale")
+    assert_rows_equal(got["recv_topk_idx"], want["recv_topk_idx"], "recv_topk_idx")
+    assert_rows_equal(got["recv_topk_w"].view(np.uint32), want["recv_topk_w"].view(np.uint32),
+                      "recv_topk_w")
+    assert_rows_equal(got["recv_src"], want["recv_src"], "recv_src")

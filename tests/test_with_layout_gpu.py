@@ -73,6 +73,21 @@ def test_shapes(T, H, E, k, W, quant):
     _check(x, idx, w, E, W, ep.ep_max_recv_rows(T, k, W), quant)
 
 
+@pytest.mark.parametrize("T,H,E,k,W,launches", [
+    (16384, 512, 64, 4, 32, 2),    # chunk table exactly 16 KB (128 chunks x 32 ranks)
+    (16385, 512, 64, 4, 32, 3),    # one chunk more: count + scan + dispatch
+    (65536, 512, 64, 2, 8, 2),     # 512 chunks x 8 ranks, exactly 16 KB
+    (5000, 1024, 48, 5, 6, 2),     # W not a multiple of 4
+])
+def test_finalize_limits(T, H, E, k, W, launches):
+    assert ep.ep_dispatch_with_layout_launches(T, H, W) == launches
+    rng = np.random.default_rng(T + W)
+    x = make_bf16(rng, (T, H))
+    idx = make_routing(rng, T, E, k, "uniform")
+    w = rng.random((T, k), dtype=np.float32)
+    _check(x, idx, w, E, W, ep.ep_max_recv_rows(T, k, W), ep.EP_QUANT_BF16)
+
+
 def test_empty_batch():
     x = np.zeros((0, 7168), np.uint16)
     idx = np.zeros((0, 8), np.int32)

@@ -422,7 +422,7 @@ def run_ours(args) -> dict | None:
                  "mode": "CUDA graph of 20 steps replayed back to back, no L2 flush (warm caches)"},
         "idle_check": idle,
         # timed steps only: layout + dispatch in one call, then combine
-        "gpu_launches": (ep.ep_dispatch_with_layout_launches(T, H, W) + 1) * args.steps,
+        "gpu_launches": (ep.ep_dispatch_with_layout_launches(T, H, k, W) + 1) * args.steps,
         "clocks": clocks,
     }
 

@@ -81,7 +81,7 @@ def load_library() -> ctypes.CDLL:
                                                     ctypes.c_size_t, _I64, _I, _P, _P, _P, _P, _P,
                                                     _P, _P]
     lib.ep_dispatch_experts_with_layout.restype = _I
-    lib.ep_dispatch_with_layout_launches.argtypes = [_I64, _I, _I, _I]
+    lib.ep_dispatch_with_layout_launches.argtypes = [_I64, _I, _I, _I, _I]
     lib.ep_dispatch_with_layout_launches.restype = _I
     lib.ep_combine.argtypes = [_P, _P, _I64, _I, _I, _I64, _P, _P, _P]
     lib.ep_combine.restype = _I
@@ -274,8 +274,9 @@ def ep_dispatch_experts_with_layout(x: torch.Tensor, topk_idx: torch.Tensor, top
     _raise("ep_dispatch_experts_with_layout", rc)
 
 
-def ep_dispatch_with_layout_launches(T: int, H: int, W: int, quant: int = EP_QUANT_BF16) -> int:
-    return int(load_library().ep_dispatch_with_layout_launches(T, H, W, quant))
+def ep_dispatch_with_layout_launches(T: int, H: int, k: int, W: int,
+                                     quant: int = EP_QUANT_BF16) -> int:
+    return int(load_library().ep_dispatch_with_layout_launches(T, H, k, W, quant))
 
 
 def ep_combine(y: torch.Tensor, slot: torch.Tensor, out: torch.Tensor,

@@ -112,10 +112,10 @@ int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk_w, int
                                        status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int ep_dispatch_with_layout_launches(int64_t T, int H, int W, int quant) {
-  if (T < 0 || H < 1 || W < 1 || W > 32) return -1;
+int ep_dispatch_with_layout_launches(int64_t T, int H, int k, int W, int quant) {
+  if (T < 0 || H < 1 || k < 1 || W < 1 || W > 32) return -1;
   if (quant != EP_QUANT_BF16 && quant != EP_QUANT_FP8_E4M3_B128) return -1;
-  return ep::dispatch_with_layout_launches(T, H, W, quant);
+  return ep::dispatch_with_layout_launches(T, H, k, W, quant);
 }
 
 int ep_dispatch_with_layout(const void* x, const int32_t* topk_idx, const float* topk_w,

@@ -339,8 +339,17 @@ bool finalize_applies(int64_t T, int H, int W, int quant, TmaShape* sh) {
 }
 }  // namespace
 
-int dispatch_with_layout_launches(int64_t T, int H, int W, int quant) {
+// Small bf16 batches: the one-launch dispatch (every CTA recomputes the
+// layout) is the fastest step up to this many tokens (GB300, decode shapes).
+constexpr int64_t kPreferFusedMaxT = 512;
+bool prefer_fused(int64_t T, int H, int k, int quant) {
+  return quant == EP_QUANT_BF16 && T > 0 && T <= kPreferFusedMaxT && T <= fused_max_tokens() &&
+         k <= 16 && H % 8 == 0;
+}
+
+int dispatch_with_layout_launches(int64_t T, int H, int k, int W, int quant) {
   TmaShape sh;
+  if (prefer_fused(T, H, k, quant)) return 1;               // layout + dispatch in one kernel
   if (finalize_applies(T, H, W, quant, &sh)) return 2;      // count, dispatch
   const int layout = T <= kLayoutSingleMaxT ? 1 : 2;       // one CTA, or count + scan
   return layout + (T > 0 ? 1 : 0);
@@ -354,6 +363,10 @@ cudaError_t launch_dispatch_with_layout(const void* x, const int32_t* topk_idx, 
                                         int quant, void* recv_x, float* recv_scale,
                                         int32_t* recv_topk_idx, float* recv_topk_w,
                                         int32_t* recv_src, int32_t* status, cudaStream_t stream) {
+  if (prefer_fused(T, H, k, quant))
+    return launch_dispatch_fused(x, topk_idx, topk_w, T, H, k, E, W, num_tokens_per_expert,
+                                 num_tokens_per_rank, rank_offset, slot, capacity_rows, recv_x,
+                                 recv_topk_idx, recv_topk_w, recv_src, status, stream);
   TmaShape sh;
   if (finalize_applies(T, H, W, quant, &sh)) {
     // count kernel (positions inside chunks) -> dispatch that finishes the layout

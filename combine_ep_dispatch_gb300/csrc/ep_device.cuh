@@ -222,10 +222,11 @@ cudaError_t launch_layout_count(const int32_t* topk_idx, int64_t T, int k, int E
 // T up to which launch_layout uses its one-CTA kernel.
 constexpr int64_t kLayoutSingleMaxT = 1024;
 int64_t layout_num_chunks(int64_t T);
-int dispatch_with_layout_launches(int64_t T, int H, int W, int quant);
+int dispatch_with_layout_launches(int64_t T, int H, int k, int W, int quant);
 // ep_dispatch_with_layout: the layout, then the dispatch, launched so that the
-// dispatch overlaps the layout (and, for bf16 rows of 1 KB or more, finishes
-// the layout itself in place of the scan kernel).
+// dispatch overlaps the layout (and, beyond 1024 tokens, finishes the layout
+// itself in place of the scan kernel); small bf16 batches take the one-launch
+// dispatch.
 cudaError_t launch_dispatch_with_layout(const void* x, const int32_t* topk_idx, const float* topk_w,
                                         int64_t T, int H, int k, int E, int W,
                                         int32_t* num_tokens_per_expert,

@@ -154,7 +154,9 @@ EP_API int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk
  * before ep_dispatch).  For T > 1024 (FP8 rows, or bf16 rows of at least
  * 1 KB) the dispatch also finishes the layout: the count kernel numbers each
  * token inside its chunk of 128 and the dispatch adds the chunk's base row, so
- * the scan kernel is not launched (ep_dispatch_with_layout_launches).  The layout
+ * the scan kernel is not launched.  bf16 batches of up to 512 tokens (k <= 16)
+ * take the one-launch kernel of ep_dispatch_fused, the fastest there
+ * (ep_dispatch_with_layout_launches).  The layout
  * is the one of "perf(ep): optimize IntraNode dispatch kernel for MI350X",
  * Technical Details 1; the dispatch follows the same page's Technical Details
  * 1, 3 and 4.
@@ -171,12 +173,14 @@ EP_API int ep_dispatch_with_layout(const void* x, const int32_t* topk_idx, const
 /*
  * Number of kernels one ep_dispatch_with_layout call with these sizes
  * launches (for callers that count launches, e.g. to size a CUDA graph):
- * 2 when the dispatch finishes the layout itself (T > 1024, FP8 rows or bf16
- * rows of at least 1 KB, and a chunk table (ceil(T / 128) * W ints) of at most
- * 16 KB), else the layout's kernels (1 for T <= 1024, else 2) plus 1 for the
- * dispatch when T > 0.  Returns -1 for invalid arguments.  Host only.
+ * 1 for bf16 batches of 1 to 512 tokens with k <= 16 (the one-launch dispatch
+ * of ep_dispatch_fused); 2 when the dispatch finishes the layout itself
+ * (T > 1024, FP8 rows or bf16 rows of at least 1 KB, and a chunk table
+ * (ceil(T / 128) * W ints) of at most 16 KB); else the layout's kernels (1 for
+ * T <= 1024, else 2) plus 1 for the dispatch when T > 0.  Returns -1 for
+ * invalid arguments.  Host only.
  */
-EP_API int ep_dispatch_with_layout_launches(int64_t T, int H, int W, int quant);
+EP_API int ep_dispatch_with_layout_launches(int64_t T, int H, int k, int W, int quant);
 
 /*
  * Local expert ids, in place, after ep_dispatch on the same stream: in receive

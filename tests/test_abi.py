@@ -55,14 +55,18 @@ def test_size_queries(lib):
     for code in range(6):
         assert ep.ep_status_string(code).startswith("EP_")
     # kernels per ep_dispatch_with_layout call
-    assert ep.ep_dispatch_with_layout_launches(4096, 7168, 8) == 2     # count + finishing dispatch
-    assert ep.ep_dispatch_with_layout_launches(4096, 7168, 8, 1) == 2  # FP8: count + finishing dispatch
-    assert ep.ep_dispatch_with_layout_launches(1024, 7168, 8, 1) == 2  # one-CTA layout + FP8 dispatch
-    assert ep.ep_dispatch_with_layout_launches(4096, 256, 8) == 3      # rows under 1 KB
-    assert ep.ep_dispatch_with_layout_launches(1024, 7168, 8) == 2     # one-CTA layout + dispatch
-    assert ep.ep_dispatch_with_layout_launches(0, 7168, 8) == 1
-    assert ep.ep_dispatch_with_layout_launches(300000, 7168, 8) == 3   # chunk table over 16 KB
-    assert ep.ep_dispatch_with_layout_launches(4096, 7168, 33) == -1
+    L = ep.ep_dispatch_with_layout_launches
+    assert L(4096, 7168, 8, 8) == 2      # count + finishing dispatch
+    assert L(4096, 7168, 8, 8, 1) == 2   # FP8: count + finishing dispatch
+    assert L(1024, 7168, 8, 8, 1) == 2   # one-CTA layout + FP8 dispatch
+    assert L(4096, 256, 8, 8) == 3       # rows under 1 KB: count + scan + dispatch
+    assert L(1024, 7168, 8, 8) == 2      # one-CTA layout + dispatch
+    assert L(512, 7168, 8, 8) == 1       # one-launch dispatch
+    assert L(256, 7168, 20, 8) == 2      # k > 16: one-CTA layout + dispatch
+    assert L(256, 7168, 8, 8, 1) == 2    # FP8 never takes the one-launch kernel
+    assert L(0, 7168, 8, 8) == 1
+    assert L(300000, 7168, 8, 8) == 3    # chunk table over 16 KB
+    assert L(4096, 7168, 8, 33) == -1
 
 
 # The calls below pass made-up device addresses that each violate one rule, so

@@ -80,7 +80,7 @@ def test_shapes(T, H, E, k, W, quant):
     (5000, 1024, 48, 5, 6, 2),     # W not a multiple of 4
 ])
 def test_finalize_limits(T, H, E, k, W, launches):
-    assert ep.ep_dispatch_with_layout_launches(T, H, W) == launches
+    assert ep.ep_dispatch_with_layout_launches(T, H, k, W) == launches
     rng = np.random.default_rng(T + W)
     x = make_bf16(rng, (T, H))
     idx = make_routing(rng, T, E, k, "uniform")

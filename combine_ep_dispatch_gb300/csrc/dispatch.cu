@@ -100,7 +100,6 @@ __device__ __forceinline__ int load_slot(const int32_t* slot, int64_t t, int W, 
   return (t < T && lane < W) ? slot[t * W + lane] : -1;
 }
 
-
 __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
     dispatch_bf16_tma_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
                              const float* __restrict__ topk_w, int64_t T, uint32_t row_bytes,

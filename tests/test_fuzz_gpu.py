@@ -1,7 +1,8 @@
 """Seeded random shapes through every entry point, against the oracle, bit
 for bit: rank-major layout, dispatch (bf16 and FP8) and combine (plain and
-weighted); expert-major layout, dispatch and weighted combine; the one-launch
-dispatch where the batch allows it; local ids; FP8 cast and transposed cast.
+weighted); the single layout + dispatch call (rank-major, both payloads);
+expert-major layout, dispatch and weighted combine; the one-launch dispatch
+where the batch allows it; local ids; FP8 cast and transposed cast.
 Each case draws T, H, E, k, W, the routing (uniform or Zipf, with invalid ids
 and repeated experts) and the capacity from its own seed."""
 import numpy as np
@@ -11,7 +12,8 @@ import torch
 import combine_ep_dispatch_gb300 as ep
 import oracle
 from combine_ep_dispatch_gb300.inputs import make_bf16, make_routing
-from gpu_util import assert_rows_equal, run_combine, run_dispatch, run_layout, to_dev_bf16, u16
+from gpu_util import (assert_rows_equal, run_combine, run_dispatch, run_layout, run_with_layout,
+                      to_dev_bf16, u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -64,6 +66,19 @@ def test_fuzz_rank_major(seed):
                               "recv_scale")
         for key in ("recv_topk_idx", "recv_src"):
             assert_rows_equal(g[key][:n], want[key][:n], key)
+        # the same through the single layout + dispatch call (whichever of its
+        # paths this size takes)
+        if quant == ep.EP_QUANT_BF16 or H % 128 == 0:
+            gw = run_with_layout(x, idx, w, E, W, cap, quant)
+            for key in ("num_tokens_per_expert", "num_tokens_per_rank", "rank_offset", "slot"):
+                assert_rows_equal(gw[key], lay[key], "with_layout " + key)
+            assert gw["status"] == lay["status"] | want["status"]
+            assert_rows_equal(gw["recv_x"][:n], want["recv_x"][:n], "with_layout recv_x")
+            if quant == ep.EP_QUANT_FP8_E4M3_B128:
+                assert_rows_equal(gw["recv_scale"][:n].view(np.uint32),
+                                  want["recv_scale"][:n].view(np.uint32), "with_layout recv_scale")
+            for key in ("recv_topk_idx", "recv_src"):
+                assert_rows_equal(gw[key][:n], want[key][:n], "with_layout " + key)
         if quant == ep.EP_QUANT_BF16 and cap >= R and T:
             local = oracle.localize_ids(want["recv_topk_idx"], E, W, lay["rank_offset"])
             ri = torch.from_numpy(np.ascontiguousarray(g["recv_topk_idx"])).cuda()

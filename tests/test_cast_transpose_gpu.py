@@ -73,6 +73,22 @@ def test_cast_transpose_matches_oracle(sizes, H):
     _check(y if R else np.zeros((1, H), np.uint16)[:0], off, scale, amax0)
 
 
+def test_cast_transpose_8192_experts():
+    """The largest expert count the call takes: 8192 per-expert prefixes in
+    shared memory, most experts empty, a few with ragged row counts."""
+    rng = np.random.default_rng(8192)
+    E, H = 8192, 256
+    n = np.zeros(E, np.int64)
+    hot = rng.choice(E, 40, replace=False)
+    n[hot] = rng.integers(1, 150, hot.size)
+    n[E - 1] = 65                                                     # the last expert too
+    off = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    R = int(off[-1])
+    y = make_bf16(rng, (R, H), scale=2.0)
+    scale = (2.0 ** rng.uniform(-3, 6, size=E)).astype(np.float32)
+    _check(y, off, scale, np.zeros(E, np.float32))
+
+
 def test_cast_transpose_expert_major_dsv3_step():
     """Dispatch the DeepSeek-V3 batch into the expert-major layout, then cast
     and transpose the received rows with per-expert scales."""

@@ -88,6 +88,30 @@ def test_finalize_limits(T, H, E, k, W, launches):
     _check(x, idx, w, E, W, ep.ep_max_recv_rows(T, k, W), ep.EP_QUANT_BF16)
 
 
+@pytest.mark.parametrize("T", [700, 3000])
+@pytest.mark.parametrize("quant", [0, 1])
+def test_max_experts_and_ranks(T, quant):
+    """E = 8192 experts (the rank layout's limit: an 8192-entry histogram in
+    shared memory) over W = 32 ranks, one-CTA and chunked layouts, both
+    payloads, through both the separate calls and the single call."""
+    from gpu_util import run_dispatch, run_layout
+    rng = np.random.default_rng(T + quant)
+    E, W, k, H = 8192, 32, 8, 1024
+    x = make_bf16(rng, (T, H))
+    idx = make_routing(rng, T, E, k, "zipf" if quant else "uniform")
+    w = rng.random((T, k), dtype=np.float32)
+    lay = oracle.layout(idx, E, W)
+    got = run_layout(idx, E, W)
+    for key in ("num_tokens_per_expert", "num_tokens_per_rank", "rank_offset", "slot"):
+        assert_rows_equal(got[key], lay[key], key)
+    cap = ep.ep_max_recv_rows(T, k, W)
+    want = oracle.dispatch(x, idx, w, lay["slot"], cap, quant)
+    R = int(lay["rank_offset"][-1])
+    g = run_dispatch(x, idx, w, lay["slot"], cap, quant)
+    assert_rows_equal(g["recv_x"][:R], want["recv_x"][:R], "recv_x")
+    _check(x, idx, w, E, W, cap, quant)
+
+
 def test_empty_batch():
     x = np.zeros((0, 7168), np.uint16)
     idx = np.zeros((0, 8), np.int32)
@@ -173,6 +197,7 @@ def _run_experts_with_layout(x, idx, w, E, cap, quant):
 
 @pytest.mark.parametrize("quant", [0, 1])
 @pytest.mark.parametrize("T,H,E,k", [
+    (600, 1024, 4096, 8),     # the expert layout's limit: 4096 experts, chunked kernels
     (200, 1024, 64, 8),       # one-CTA expert layout (<= 2048 pairs)
     (4096, 7168, 256, 8),     # dsv3 shape: count + assign kernels
     (3001, 512, 48, 6),       # ragged; rows under 1 KB take the register kernel (bf16)

@@ -40,21 +40,27 @@ def _capture(dc, x, idx, w, fused):
     return g
 
 
-@pytest.mark.parametrize("order,fused", [("rank", False), ("rank", True), ("expert", False)])
-def test_graph_replays_match_oracle(order, fused):
-    cfg = make_inputs("decode", seed=0)["cfg"]
+@pytest.mark.parametrize("order,fused,workload,T_", [
+    ("rank", False, "decode", None),    # the single call takes the one-launch kernel
+    ("rank", True, "decode", None),
+    ("expert", False, "decode", None),
+    ("rank", False, "dsv3", 2048),      # count kernel + dispatch finishing the layout
+    ("expert", False, "dsv3", 2048),    # expert layout kernels + dispatch
+])
+def test_graph_replays_match_oracle(order, fused, workload, T_):
+    cfg = make_inputs(workload, seed=0, T=T_)["cfg"]
     T, H, E, k, W = cfg.T, cfg.H, cfg.E, cfg.k, cfg.W
     dc = ep.DispatchCombine(T, H, E, k, W, order=order)
     x = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
     idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
     w = torch.empty(T, k, dtype=torch.float32, device="cuda")
-    first = make_inputs("decode", seed=100)
+    first = make_inputs(workload, seed=100, T=T_)
     x.copy_(to_dev_bf16(first["x"]))
     idx.copy_(torch.from_numpy(first["topk_idx"]))
     w.copy_(torch.from_numpy(first["topk_w"]))
     g = _capture(dc, x, idx, w, fused)
     for seed in (1, 2, 3):
-        inp = make_inputs("decode", seed=seed)
+        inp = make_inputs(workload, seed=seed, T=T_)
         x.copy_(to_dev_bf16(inp["x"]))
         idx.copy_(torch.from_numpy(inp["topk_idx"]))
         w.copy_(torch.from_numpy(inp["topk_w"]))

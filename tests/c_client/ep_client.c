@@ -1,0 +1,142 @@
+/*
+ * A plain C client of libep_gb300: no Python and no PyTorch in the process,
+ * only include/ep_gb300.h and the shared library.
+ *
+ *   query mode (no GPU): size queries, status strings, and host-side argument
+ *     checks that reject a call before anything reaches a GPU;
+ *   gpu mode (built with -DEP_CLIENT_GPU): a small batch through
+ *     ep_dispatch_with_layout and ep_combine with identity experts (the
+ *     combine reads the dispatched rows back).  Every output row must then be
+ *     d_t * x_t exactly, with d_t the number of distinct destination ranks of
+ *     token t: small integer inputs make the fp32 sum and the bf16 rounding
+ *     exact, so this closed form needs no reference implementation.
+ */
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "ep_gb300.h"
+#ifdef EP_CLIENT_GPU
+#include <cuda_runtime.h>
+#endif
+
+static int fail(const char* what) {
+  fprintf(stderr, "FAIL: %s\n", what);
+  return 1;
+}
+
+static int query_mode(void) {
+  if (ep_max_recv_rows(4096, 8, 8) != 32768) return fail("ep_max_recv_rows");
+  if (ep_layout_workspace_bytes(4096, 8, 256) < 4096 * 4) return fail("ep_layout_workspace_bytes");
+  if (strncmp(ep_status_string(EP_OK), "EP_OK", 5) != 0) return fail("ep_status_string");
+  if (ep_dispatch_with_layout_launches(4096, 7168, 8, 8, EP_QUANT_BF16) != 2)
+    return fail("ep_dispatch_with_layout_launches");
+  /* rejected on the host: more than 32 ranks, E not a multiple of W, H % 8 */
+  if (ep_dispatch_layout(NULL, 10, 8, 256, 33, NULL, NULL, NULL, NULL, NULL, 0, NULL, NULL) !=
+      EP_ERR_INVALID_ARG)
+    return fail("reject W = 33");
+  if (ep_dispatch_layout(NULL, 10, 8, 100, 8, NULL, NULL, NULL, NULL, NULL, 0, NULL, NULL) !=
+      EP_ERR_INVALID_ARG)
+    return fail("reject E % W");
+  if (ep_dispatch(NULL, NULL, NULL, 10, 12, 8, 8, NULL, 80, EP_QUANT_BF16, NULL, NULL, NULL, NULL,
+                  NULL, NULL, NULL) != EP_ERR_UNSUPPORTED)
+    return fail("reject H = 12");
+  printf("query mode ok\n");
+  return 0;
+}
+
+#ifdef EP_CLIENT_GPU
+/* bf16 bits of a small integer (exact: at most 8 significant bits) */
+static uint16_t bf16_of_int(int v) {
+  float f = (float)v;
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)(u >> 16);
+}
+
+#define CK(call)                                              \
+  do {                                                        \
+    if ((call) != cudaSuccess) return fail(#call);            \
+  } while (0)
+
+static int gpu_mode(void) {
+  enum { T = 300, H = 256, E = 64, K = 4, W = 8 };
+  const int Er = E / W;
+  static int32_t idx[T * K];
+  static float wts[T * K];
+  static uint16_t x[T * H], out[T * H];
+  int d[T];
+  uint32_t lcg = 12345u;
+  for (int t = 0; t < T; ++t) { /* k distinct experts per token */
+    for (int j = 0; j < K; ++j) {
+      int e, dup;
+      do {
+        lcg = lcg * 1664525u + 1013904223u;
+        e = (int)((lcg >> 8) % E);
+        dup = 0;
+        for (int i = 0; i < j; ++i) dup |= idx[t * K + i] == e;
+      } while (dup);
+      idx[t * K + j] = e;
+      wts[t * K + j] = 1.0f / K;
+    }
+    unsigned ranks = 0;
+    for (int j = 0; j < K; ++j) ranks |= 1u << (idx[t * K + j] / Er);
+    d[t] = __builtin_popcount(ranks);
+    for (int h = 0; h < H; ++h) x[t * H + h] = bf16_of_int((t * 7 + h * 3) % 17 - 8);
+  }
+  const int64_t cap = ep_max_recv_rows(T, K, W);
+  const size_t ws_bytes = ep_layout_workspace_bytes(T, W, E);
+  void *dx, *dy, *dout, *dws;
+  int32_t *didx, *dne, *dnr, *doff, *dslot, *dri, *dsrc, *dst;
+  float *dw, *drw;
+  CK(cudaMalloc((void**)&dx, sizeof x));
+  CK(cudaMalloc((void**)&didx, sizeof idx));
+  CK(cudaMalloc((void**)&dw, sizeof wts));
+  CK(cudaMalloc((void**)&dne, E * 4));
+  CK(cudaMalloc((void**)&dnr, W * 4));
+  CK(cudaMalloc((void**)&doff, (W + 1) * 4));
+  CK(cudaMalloc((void**)&dslot, T * W * 4));
+  CK(cudaMalloc((void**)&dws, ws_bytes));
+  CK(cudaMalloc((void**)&dy, (size_t)cap * H * 2));
+  CK(cudaMalloc((void**)&dri, (size_t)cap * K * 4));
+  CK(cudaMalloc((void**)&drw, (size_t)cap * K * 4));
+  CK(cudaMalloc((void**)&dsrc, (size_t)cap * 4));
+  CK(cudaMalloc((void**)&dout, sizeof out));
+  CK(cudaMalloc((void**)&dst, 4));
+  CK(cudaMemset(dst, 0, 4));
+  CK(cudaMemcpy(dx, x, sizeof x, cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(didx, idx, sizeof idx, cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(dw, wts, sizeof wts, cudaMemcpyHostToDevice));
+  int rc = ep_dispatch_with_layout(dx, didx, dw, T, H, K, E, W, dne, dnr, doff, dslot, dws,
+                                   ws_bytes, cap, EP_QUANT_BF16, dy, NULL, dri, drw, dsrc, dst,
+                                   NULL);
+  if (rc != EP_OK) return fail(ep_status_string(rc));
+  rc = ep_combine(dy, dslot, T, H, W, cap, dout, dst, NULL);
+  if (rc != EP_OK) return fail(ep_status_string(rc));
+  CK(cudaDeviceSynchronize());
+  int32_t off[W + 1], status = -1;
+  CK(cudaMemcpy(out, dout, sizeof out, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(off, doff, sizeof off, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(&status, dst, 4, cudaMemcpyDeviceToHost));
+  if (status != 0) return fail("status word");
+  int R = 0;
+  for (int t = 0; t < T; ++t) R += d[t];
+  if (off[W] != R) return fail("rank_offset[W] != sum of d_t");
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h)
+      if (out[t * H + h] != bf16_of_int(d[t] * ((t * 7 + h * 3) % 17 - 8))) {
+        fprintf(stderr, "token %d column %d\n", t, h);
+        return fail("combine(dispatch(x)) != d_t * x");
+      }
+  printf("gpu mode ok: T=%d H=%d E=%d k=%d W=%d R=%d\n", T, H, E, K, W, R);
+  return 0;
+}
+#endif
+
+int main(void) {
+  if (query_mode()) return 1;
+#ifdef EP_CLIENT_GPU
+  if (gpu_mode()) return 1;
+#endif
+  return 0;
+}

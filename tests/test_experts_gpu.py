@@ -195,3 +195,29 @@ def test_combine_weighted_empty_batch():
     got = run_combine_weighted(make_bf16(np.random.default_rng(0), (4, 64)),
                                np.zeros((0, 8), np.int32), np.zeros((0, 8), np.float32), 64)
     assert got["out"].shape == (0, 64) and got["status"] == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3"])
+def test_combine_weighted_rank_scaled_experts_closed_form(name):
+    """The fused expert epilogue of the pages' combine test (rank r's rows
+    scaled by 1 + r) as a weighted rank-major combine of identity experts:
+    out[t] = bf16(S_t * x[t]) with S_t = sum over r in D(t) of (1 + r).  x has
+    8 significant bits and S_t at most 6, so every product and sum is exact in
+    fp32 and the only rounding is the final bf16 one, taken here from
+    PyTorch's cast (the dsv3 inputs hold a -0, which the sum from +0 turns
+    into +0)."""
+    inp = make_inputs(name, seed=4)
+    cfg = inp["cfg"]
+    dc = ep.DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W)
+    x = to_dev_bf16(inp["x"])
+    idx = torch.from_numpy(inp["topk_idx"]).cuda()
+    dc.layout_dispatch(x, idx, torch.from_numpy(inp["topk_w"]).cuda())
+    slot = dc.slot
+    wr = (torch.arange(cfg.W, dtype=torch.float32, device="cuda") + 1.0).expand(cfg.T, cfg.W).contiguous()
+    out = dc.combine(dc.recv_x, wr)
+    torch.cuda.synchronize()
+    S = ((slot >= 0).float() * wr).sum(dim=1, keepdim=True)
+    # the sum starts from +0, so a -0 input gives +0 (the combine's reading of signed zero)
+    want = (0.0 + x.float() * S).cpu().to(torch.bfloat16)
+    assert torch.equal(out.cpu().view(torch.int16), want.view(torch.int16))
+    assert int(dc.status.item()) == 0

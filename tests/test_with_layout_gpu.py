@@ -222,3 +222,20 @@ def test_experts_with_layout(T, H, E, k, quant):
     assert_rows_equal(got["recv_topk_w"].view(np.uint32), want["recv_topk_w"].view(np.uint32),
                       "recv_topk_w")
     assert_rows_equal(got["recv_src"], want["recv_src"], "recv_src")
+
+
+@pytest.mark.parametrize("T", [300, 2000])
+def test_zero_capacity(T):
+    """capacity_rows = 0 with recv buffers of zero rows: the layout is still
+    complete, nothing is written, and EP_STATUS_CAPACITY is set (the one-launch
+    kernel at T = 300, the finishing dispatch at T = 2000)."""
+    rng = np.random.default_rng(T)
+    H, E, k, W = 1024, 64, 4, 8
+    x = make_bf16(rng, (T, H))
+    idx = make_routing(rng, T, E, k, "uniform")
+    w = rng.random((T, k), dtype=np.float32)
+    got = run_with_layout(x, idx, w, E, W, 0, ep.EP_QUANT_BF16)
+    lay = oracle.layout(idx, E, W)
+    for key in ("num_tokens_per_expert", "num_tokens_per_rank", "rank_offset", "slot"):
+        assert_rows_equal(got[key], lay[key], key)
+    assert got["status"] == ep.EP_STATUS_CAPACITY

@@ -239,3 +239,31 @@ def test_zero_capacity(T):
     for key in ("num_tokens_per_expert", "num_tokens_per_rank", "rank_offset", "slot"):
         assert_rows_equal(got[key], lay[key], key)
     assert got["status"] == ep.EP_STATUS_CAPACITY
+
+
+def test_two_streams_do_not_interfere():
+    """The library keeps no state between calls: two pipelines with their own
+    buffers, interleaved on two streams (one taking the one-launch kernel, one
+    the count kernel + finishing dispatch), give the results each gives alone."""
+    dev = "cuda"
+    setups = []
+    for name, T_, seed in (("decode", None, 31), ("dsv3", 2048, 32)):
+        inp = make_inputs(name, seed=seed, T=T_)
+        cfg = inp["cfg"]
+        dc = ep.DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, device=dev)
+        x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+        idx = torch.from_numpy(inp["topk_idx"]).to(dev)
+        w = torch.from_numpy(inp["topk_w"]).to(dev)
+        dc.step(x, idx, w)  # alone, on the current stream
+        torch.cuda.synchronize()
+        ref = (dc.slot.clone(), dc.out.clone())
+        setups.append((dc, x, idx, w, ref, torch.cuda.Stream(device=dev)))
+    for _ in range(5):
+        for dc, x, idx, w, _ref, s in setups:
+            with torch.cuda.stream(s):
+                dc.step(x, idx, w, stream=s)
+    torch.cuda.synchronize()
+    for dc, _x, _idx, _w, (slot, out), _s in setups:
+        assert torch.equal(dc.slot, slot)
+        assert torch.equal(dc.out.view(torch.int16), out.view(torch.int16))
+        assert int(dc.status.item()) == 0

@@ -43,6 +43,7 @@ EP_LAYOUT_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 class EPError(RuntimeError):
+    """A host-side EP_ERR_* code returned by a library call (``code``)."""
     def __init__(self, fn: str, code: int, text: str):
         super().__init__(f"{fn} failed with code {code}: {text}")
         self.code = code
@@ -151,14 +152,17 @@ def _raise(fn: str, code: int):
 
 
 def ep_status_string(code: int) -> str:
+    """Name and meaning of an EP_OK / EP_ERR_* code."""
     return load_library().ep_status_string(int(code)).decode()
 
 
 def ep_layout_workspace_bytes(T: int, W: int, E: int) -> int:
+    """Bytes of workspace ep_dispatch_layout needs for these sizes (0: invalid)."""
     return int(load_library().ep_layout_workspace_bytes(T, W, E))
 
 
 def ep_max_recv_rows(T: int, k: int, W: int) -> int:
+    """Worst-case receive rows, T * min(k, W): a capacity that never overflows."""
     return int(load_library().ep_max_recv_rows(T, k, W))
 
 
@@ -166,6 +170,9 @@ def ep_dispatch_layout(topk_idx: torch.Tensor, E: int, W: int,
                        num_tokens_per_expert: torch.Tensor, num_tokens_per_rank: torch.Tensor,
                        rank_offset: torch.Tensor, slot: torch.Tensor, workspace: torch.Tensor,
                        status: torch.Tensor | None = None, stream=None) -> None:
+    """ep_dispatch_layout: per-expert and per-rank counts, rank_offset and the
+    slot of every (token, rank) pair for topk_idx [T, k] (int32 CUDA tensors;
+    workspace of ep_layout_workspace_bytes(T, W, E) bytes)."""
     for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
                  ("num_tokens_per_rank", num_tokens_per_rank), ("rank_offset", rank_offset),
                  ("slot", slot)):
@@ -185,6 +192,9 @@ def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor, W
                 recv_topk_w: torch.Tensor | None = None, recv_src: torch.Tensor | None = None,
                 recv_scale: torch.Tensor | None = None, quant: int = EP_QUANT_BF16,
                 status: torch.Tensor | None = None, stream=None) -> None:
+    """ep_dispatch: rows of x [T, H] bf16 to their receive rows (bf16, or FP8
+    codes with recv_scale for EP_QUANT_FP8_E4M3_B128) with the metadata; the
+    capacity is recv_x.shape[0]."""
     _check_cuda("x", x, torch.bfloat16)
     _check_cuda("topk_idx", topk_idx, torch.int32)
     _check_cuda("topk_w", topk_w, torch.float32)
@@ -276,11 +286,14 @@ def ep_dispatch_experts_with_layout(x: torch.Tensor, topk_idx: torch.Tensor, top
 
 def ep_dispatch_with_layout_launches(T: int, H: int, k: int, W: int,
                                      quant: int = EP_QUANT_BF16) -> int:
+    """Kernels one ep_dispatch_with_layout call with these sizes launches."""
     return int(load_library().ep_dispatch_with_layout_launches(T, H, k, W, quant))
 
 
 def ep_combine(y: torch.Tensor, slot: torch.Tensor, out: torch.Tensor,
                status: torch.Tensor | None = None, stream=None) -> None:
+    """ep_combine: out[t] = bf16 of the fp32 sum, in ascending rank order from
+    +0, of the rows y[slot[t][r]] (y [capacity_rows, H] bf16)."""
     _check_cuda("y", y, torch.bfloat16)
     _check_cuda("slot", slot, torch.int32)
     _check_cuda("out", out, torch.bfloat16)
@@ -354,6 +367,7 @@ def ep_localize_expert_ids(recv_topk_idx: torch.Tensor, rank_offset: torch.Tenso
 
 
 def ep_layout_experts_workspace_bytes(T: int, k: int, E: int) -> int:
+    """Bytes of workspace ep_dispatch_layout_experts needs for these sizes."""
     return int(load_library().ep_layout_experts_workspace_bytes(T, k, E))
 
 
@@ -407,6 +421,7 @@ def ep_selftest_wait_timeout(status: torch.Tensor, stream=None) -> None:
 
 
 def ep_cast_transpose_t_bytes(capacity_rows: int, E: int, H: int) -> int:
+    """Bytes of the transposed FP8 output of ep_cast_transpose_experts."""
     return int(load_library().ep_cast_transpose_t_bytes(capacity_rows, E, H))
 
 

@@ -65,6 +65,7 @@ class DispatchCombine:
         self.status = torch.zeros(1, **i32)
 
     def layout(self, topk_idx: torch.Tensor, stream=None) -> None:
+        """The layout of topk_idx [T, k] into this object's counts, offsets and slot."""
         if self.order == "rank":
             _lib.ep_dispatch_layout(topk_idx, self.E, self.W, self.num_tokens_per_expert,
                                     self.num_tokens_per_rank, self.rank_offset, self.slot,
@@ -76,6 +77,8 @@ class DispatchCombine:
 
     def dispatch(self, x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
                  stream=None) -> None:
+        """Rows of x [T, H] bf16 into recv_x (and recv_scale for FP8) with the
+        metadata, by the slots of the last layout."""
         _lib.ep_dispatch(x, topk_idx, topk_w, self.slot.shape[1], self.slot, self.recv_x,
                          self.recv_topk_idx, self.recv_topk_w, self.recv_src, self.recv_scale,
                          self.quant, self.status, stream)
@@ -149,5 +152,7 @@ class DispatchCombine:
         return self.recv_fp8, self.recv_fp8_t, amax
 
     def step(self, x, topk_idx, topk_w, y=None, stream=None) -> torch.Tensor:
+        """layout_dispatch() then combine(y) (y defaults to the dispatched rows,
+        i.e. identity experts); returns self.out."""
         self.layout_dispatch(x, topk_idx, topk_w, stream)
         return self.combine(y, topk_w if self.order == "expert" else None, stream)

@@ -172,6 +172,56 @@ def test_dispatch_fp8_golden_block():
     np.testing.assert_array_equal(dis["recv_x"][0], want)
 
 
+def test_dispatch_fp8_quotient_golden_block():
+    """A block whose scale is not a power of two: the IEEE quotient x/scale
+    lands exactly on e4m3 midpoints (ties to even), while x times the rounded
+    reciprocal of the scale lands one fp32 ulp above them and rounds up."""
+    g = _golden("fp8_quotient_block.json")
+    H = g["H"]
+    xs = np.zeros(H, np.float32)
+    for i, v in g["x"].items():
+        xs[int(i)] = v
+    x = _bf16(xs).reshape(1, H)
+    assert np.array_equal(f32_from_bf16_bits(x)[0], xs)    # fixture values exact in bf16
+    dis = oracle.dispatch(x, np.array([[0]], np.int32), np.ones((1, 1), np.float32),
+                          np.array([[0]], np.int32), 1, oracle.QUANT_FP8)
+    assert hex(int(dis["recv_scale"][0, 0:1].view(np.uint32)[0])) == g["scale_bits"]
+    want = np.zeros(H, np.uint8)
+    for i, c in g["codes"].items():
+        want[int(i)] = c
+    np.testing.assert_array_equal(dis["recv_x"][0], want)
+    # the fixture tells the two quotients apart: the reciprocal form's codes differ
+    assert any(g["codes"][i] != g["codes_if_reciprocal_multiply"][i] for i in g["codes"])
+
+
+def test_dispatch_fp8_codes_match_library_cast_of_ieee_quotient():
+    """1M values in blocks of N(0,1) * 2^j (non-power-of-two scales): the
+    oracle's scales equal numpy's fp32 amax / 448 bit for bit, and its codes
+    equal PyTorch's float8_e4m3fn cast of numpy's fp32 quotient x / scale,
+    saturated at +-448 (the library cast does not saturate).  About 0.1% of the
+    codes change when the quotient is taken as x * (1 / scale)."""
+    rng = np.random.default_rng(2024)
+    T, H = 128, 8192
+    nb = H // 128
+    xs = rng.standard_normal((T, H)).astype(np.float32)
+    xs *= np.repeat(2.0 ** rng.integers(-24, 24, (T, nb)), 128, axis=1).astype(np.float32)
+    x = _bf16(xs)
+    xf = f32_from_bf16_bits(x)
+    slot = np.arange(T, dtype=np.int32).reshape(T, 1)
+    dis = oracle.dispatch(x, np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32), slot, T,
+                          oracle.QUANT_FP8)
+    amax = np.abs(xf.reshape(T, nb, 128)).max(axis=2)
+    scale = (amax / np.float32(448.0)).astype(np.float32)
+    np.testing.assert_array_equal(dis["recv_scale"].view(np.uint32), scale.view(np.uint32))
+    assert np.all(scale > 0)
+    q = (xf / np.repeat(scale, 128, axis=1)).astype(np.float32)
+    want = torch.from_numpy(np.clip(q, -448.0, 448.0)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(dis["recv_x"], want)
+    rcp = (xf * np.repeat((np.float32(1.0) / scale).astype(np.float32), 128, axis=1)).astype(np.float32)
+    other = torch.from_numpy(np.clip(rcp, -448.0, 448.0)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.count_nonzero(other != want) > 100    # the sweep separates the two readings
+
+
 def test_dispatch_fp8_closed_forms():
     rng = np.random.default_rng(11)
     T, H = 6, 512

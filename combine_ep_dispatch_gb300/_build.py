@@ -48,12 +48,11 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build_library(force: bool = False, verbose: bool = False, defines=(), out: str | None = None,
+def build_library(force: bool = False, verbose: bool = False, out: str | None = None,
                   build_dir: str | None = None) -> str:
-    """Compile and link the library.  ``defines`` (e.g. ["EP_TMA_STAGES=4"])
-    override compile-time tuning constants; with ``out`` the result goes to that
-    path instead of the package's libep_gb300.so."""
-    if not force and not defines and out is None and up_to_date():
+    """Compile and link the library; with ``out`` the result goes to that path
+    instead of the package's libep_gb300.so."""
+    if not force and out is None and up_to_date():
         return LIB
     lib_path = out or LIB
     build = build_dir or BUILD
@@ -62,11 +61,10 @@ def build_library(force: bool = False, verbose: bool = False, defines=(), out: s
         nvcc = "nvcc"
     os.makedirs(build, exist_ok=True)
     srcs = _sources()
-    dflags = [f"-D{d}" for d in defines]
 
     def compile_one(src):
         obj = os.path.join(build, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *dflags, "-I", os.path.join(ROOT, "include"), "-c", src,
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", src,
                "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

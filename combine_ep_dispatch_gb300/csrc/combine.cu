@@ -5,14 +5,9 @@
 namespace ep {
 namespace {
 
-#ifndef EP_COMBINE_U
-#define EP_COMBINE_U 2
-#endif
-#ifndef EP_COMBINE_SEG_F
-#define EP_COMBINE_SEG_F 4.0
-#endif
-
 constexpr int kCThreads = 256;
+constexpr int kCU = 2;             // 16-byte chunks per lane and row in one round
+constexpr double kCSegUnits = 4.0;  // (token, segment) units per warp slot for small batches
 
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   uint32_t r;
@@ -150,32 +145,16 @@ __global__ void __launch_bounds__(kCThreads)
 // order, a stage is handed back as soon as it has been added, and no token has
 // to sit in shared memory whole: the ring only holds bytes in flight.
 // Whole-row copies and several issuing lanes keep the copy engine streaming.
-// Used for EP_COMBINE_TMA_MIN_T <= T <= EP_COMBINE_TMA_MAX_T: measured on
+// Used for kCTmaMinT <= T <= kCTmaMaxT: measured on
 // GB300 (H=7168, top-8, W=8) it beats the register kernel at T=1024 (26 us
 // against 27-28 us) and loses at T=4096 (71 us against 66 us); below T=768 the
 // register kernel with row segments keeps more loads in flight (T=256: 12 us
 // against 14.8 us).
-#ifndef EP_COMBINE_TMA
-#define EP_COMBINE_TMA 1
-#endif
-#ifndef EP_COMBINE_TMA_MAX_T
-#define EP_COMBINE_TMA_MAX_T 1024
-#endif
-#ifndef EP_COMBINE_TMA_MIN_T
-#define EP_COMBINE_TMA_MIN_T 768
-#endif
-#ifndef EP_COMBINE_WARPS
-#define EP_COMBINE_WARPS 8
-#endif
-#ifndef EP_COMBINE_STAGE
-#define EP_COMBINE_STAGE 16384
-#endif
-#ifndef EP_COMBINE_SMEM_BUDGET
-#define EP_COMBINE_SMEM_BUDGET (208 * 1024)
-#endif
-constexpr int kCWarps = EP_COMBINE_WARPS;                        // consumer warps
-constexpr uint32_t kCStage = EP_COMBINE_STAGE;                   // bytes per stage
-constexpr int kCStages = EP_COMBINE_SMEM_BUDGET / kCStage;       // ring length
+constexpr int64_t kCTmaMaxT = 1024;
+constexpr int64_t kCTmaMinT = 768;
+constexpr int kCWarps = 8;                                       // consumer warps
+constexpr uint32_t kCStage = 16384;                              // bytes per stage
+constexpr int kCStages = (208 * 1024) / kCStage;                 // ring length
 constexpr int kCPieces = kCStage / (16 * 32 * kCWarps);          // pieces per thread per stage
 constexpr int kCHead = 1024;                                     // barriers + descriptors
 constexpr uint32_t kDescLast = 1u, kDescNone = 2u, kDescDone = 4u;
@@ -328,15 +307,15 @@ cudaError_t launch_combine_regs(K1 kern_rows, KS kern_seg, const void* y, const 
   const int per_sm = occupancy_cached(kern_seg, kCThreads, cache);
   const int64_t most = (int64_t)device_sm_count() * per_sm;
   // Segments, when the batch has fewer tokens than the device has warp slots:
-  // enough (token, segment) units for EP_COMBINE_SEG_F units per slot, each
+  // enough (token, segment) units for kCSegUnits units per slot, each
   // segment at least one full round (32 * U chunks).  Measured on GB300 with
   // H = 7168, top-8: T = 256 runs in 12 us instead of 17 us, T = 512 in 16 us
   // instead of 22 us; from T = 4096 on whole rows are best.
   const int n16 = H / 8;
   const int64_t resident = most * (kCThreads / 32);
-  const int64_t target = (int64_t)(EP_COMBINE_SEG_F * (double)resident);
+  const int64_t target = (int64_t)(kCSegUnits * (double)resident);
   int64_t S = (T > 0 && T < resident) ? (target + T - 1) / T : 1;
-  const int64_t max_s = n16 / (32 * EP_COMBINE_U);
+  const int64_t max_s = n16 / (32 * kCU);
   if (S > max_s) S = max_s;
   if (S < 1) S = 1;
   int seg16 = (int)((n16 + S - 1) / S);
@@ -354,8 +333,7 @@ cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H,
   if (T == 0) return cudaSuccess;
   const uint32_t row_bytes = (uint32_t)H * 2u;
   // (a token's rows must fit the ring at once: W <= kCStages)
-  if (EP_COMBINE_TMA && !EP_FORCE_LSU && row_bytes >= 1024 && W <= kCStages &&
-      T <= EP_COMBINE_TMA_MAX_T && T >= EP_COMBINE_TMA_MIN_T) {
+  if (row_bytes >= 1024 && W <= kCStages && T <= kCTmaMaxT && T >= kCTmaMinT) {
     // chunks of at most one stage, equal up to 16 bytes
     const uint32_t nch = (row_bytes + kCStage - 1) / kCStage;
     const uint32_t chunk = ((row_bytes / nch + 15u) & ~15u);
@@ -375,8 +353,8 @@ cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H,
                       smem, stream, static_cast<const uint8_t*>(y), slot, T, row_bytes, chunk, W,
                       capacity_rows, static_cast<uint8_t*>(out), status);
   }
-  return launch_combine_regs(combine_kernel<EP_COMBINE_U, false, false>,
-                             combine_kernel<EP_COMBINE_U, false, true>, y, slot, nullptr, T, H, W,
+  return launch_combine_regs(combine_kernel<kCU, false, false>,
+                             combine_kernel<kCU, false, true>, y, slot, nullptr, T, H, W,
                              capacity_rows, out, status, stream);
 }
 
@@ -384,8 +362,8 @@ cudaError_t launch_combine_weighted(const void* y, const int32_t* slot, const fl
                                     int H, int C, int64_t capacity_rows, void* out,
                                     int32_t* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  return launch_combine_regs(combine_kernel<EP_COMBINE_U, true, false>,
-                             combine_kernel<EP_COMBINE_U, true, true>, y, slot, w, T, H, C,
+  return launch_combine_regs(combine_kernel<kCU, true, false>,
+                             combine_kernel<kCU, true, true>, y, slot, w, T, H, C,
                              capacity_rows, out, status, stream);
 }
 

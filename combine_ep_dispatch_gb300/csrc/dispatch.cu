@@ -68,29 +68,17 @@ __global__ void __launch_bounds__(kDThreads)
 // instruction instead of H/256 warp-wide 16-byte stores, which keeps the
 // load/store pipe free; the other lanes fetch the next token's slots early and
 // carry the metadata.
-#ifndef EP_TMA_STAGES
-#define EP_TMA_STAGES 3
-#endif
-#ifndef EP_TMA_SMEM_BUDGET
-#define EP_TMA_SMEM_BUDGET 100000
-#endif
-#ifndef EP_TMA_MAX_WARPS
-#define EP_TMA_MAX_WARPS 8
-#endif
-#ifndef EP_TMA_CTAS_PER_SM
-#define EP_TMA_CTAS_PER_SM 2
-#endif
-constexpr int kTmaStages = EP_TMA_STAGES;            // row buffers per warp
-constexpr int kTmaBarBytes = 1024;                   // barrier area ahead of the row buffers
-constexpr int kTmaSmemBudget = EP_TMA_SMEM_BUDGET;   // row buffers per CTA
-constexpr int kTmaMaxWarps = EP_TMA_MAX_WARPS;
+constexpr int kTmaStages = 3;            // row buffers per warp
+constexpr int kTmaBarBytes = 1024;       // barrier area ahead of the row buffers
+constexpr int kTmaSmemBudget = 100000;   // row buffers per CTA
+constexpr int kTmaMaxWarps = 8;
 // The received rows are stored with an L2 evict_last policy: it keeps the
 // rows just written in L2 for their consumer (the expert GEMM reads them next)
 // and moves part of their write-back out of this kernel.  Measured on GB300 it
 // shortens the layout + dispatch + combine step by 1.3 to 2.5 us at T=4096
 // (H=7168) and T=8192 (H=4096); evict_first changed nothing.
 constexpr int kL2EvictLast = 2;
-constexpr int kTmaCtasPerSm = EP_TMA_CTAS_PER_SM;
+constexpr int kTmaCtasPerSm = 2;
 constexpr uint32_t kTmaMinRowBytes = 1024;  // smaller rows: 16-byte stores from registers
 
 // A plain load: with a Finalize the kernel also writes the slot table (each
@@ -260,7 +248,7 @@ bool tma_shape(int H, TmaShape* sh) {
   sh->stage_bytes = (sh->row_bytes + 127u) & ~127u;
   const int fit = (int)(kTmaSmemBudget / ((size_t)kTmaStages * sh->stage_bytes));
   sh->cta_warps = fit < kTmaMaxWarps ? fit : kTmaMaxWarps;
-  return !EP_FORCE_LSU && sh->row_bytes >= kTmaMinRowBytes && fit >= 1;
+  return sh->row_bytes >= kTmaMinRowBytes && fit >= 1;
 }
 
 cudaError_t launch_tma(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T,

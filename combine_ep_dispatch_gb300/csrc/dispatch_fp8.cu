@@ -7,12 +7,8 @@ namespace ep {
 namespace {
 
 constexpr int kDThreads = 256;
-#ifndef EP_FP8_U
-#define EP_FP8_U 1  // block quadruples per step
-#endif
-#ifndef EP_FP8_MINB
-#define EP_FP8_MINB 4  // CTAs per SM the register allocation must allow
-#endif
+constexpr int kFp8U = 1;     // block quadruples per step
+constexpr int kFp8MinB = 4;  // CTAs per SM the register allocation must allow
 
 // Two fp32 values to two e4m3 codes, round to nearest even, saturating to
 // +-448: `lo` goes to the low byte.
@@ -116,7 +112,7 @@ __device__ __forceinline__ void block_scale(float m, const float* s_q7, const fl
 // segment), so that small batches still fill the GPU; each segment is
 // quantised once and its codes and scales are stored to every destination.
 template <int U>
-__global__ void __launch_bounds__(kDThreads, EP_FP8_MINB)
+__global__ void __launch_bounds__(kDThreads, kFp8MinB)
     dispatch_fp8_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ topk_idx,
                         const float* __restrict__ topk_w, int64_t T, int H, int k, int W,
                         int32_t* slot, int64_t cap, uint8_t* __restrict__ recv_x,
@@ -302,7 +298,7 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
   const uint4* x4 = static_cast<const uint4*>(x);
   // segments per token: enough (token, segment) units to give every resident warp
   // a few, but no more segments than block quadruples
-  auto kern = dispatch_fp8_kernel<EP_FP8_U>;
+  auto kern = dispatch_fp8_kernel<kFp8U>;
   static int cache[128];
   const int per_sm = occupancy_cached(kern, kDThreads, cache);
   const int64_t warps = (int64_t)device_sm_count() * per_sm * (kDThreads / 32);
@@ -311,7 +307,7 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
   nseg = nseg < 1 ? 1 : (nseg > nquad ? nquad : nseg);
   // segments of whole rounds of 2 quads (the kernel's unroll: no half-empty
   // rounds), and no empty segments
-  const int per_seg = ((nquad + nseg - 1) / nseg + EP_FP8_U - 1) / EP_FP8_U * EP_FP8_U;
+  const int per_seg = ((nquad + nseg - 1) / nseg + kFp8U - 1) / kFp8U * kFp8U;
   nseg = (nquad + per_seg - 1) / per_seg;
   const int64_t units = T * nseg;
   const int64_t grid = (units * 32 + kDThreads - 1) / kDThreads < device_sm_count() * per_sm

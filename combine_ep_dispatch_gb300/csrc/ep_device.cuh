@@ -10,13 +10,6 @@ namespace ep {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-// Build-time switch used when comparing kernel variants: 1 routes the bf16
-// copies through the register (16-byte load/store) kernels even where the
-// bulk-copy kernels apply.
-#ifndef EP_FORCE_LSU
-#define EP_FORCE_LSU 0
-#endif
-
 // ------------------------------------------------------------ dependent launch
 // Every kernel of the library is launched with programmatic stream
 // serialization and begins with pdl_wait(): the grid may become resident while
@@ -100,15 +93,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Waits for the barrier phase of the given parity to complete, for at most
 // about one second; returns false when the limit ran out.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-#ifndef EP_WAIT_CHECK_EVERY
-#define EP_WAIT_CHECK_EVERY 512
-#endif
+constexpr uint32_t kWaitCheckEvery = 512;  // polls between two reads of the timer
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (it % EP_WAIT_CHECK_EVERY == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (it % kWaitCheckEvery == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 

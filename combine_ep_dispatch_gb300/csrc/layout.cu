@@ -10,16 +10,15 @@
 //          rank, then numbers its tokens in ascending order with warp ballots.
 // Integer counts only, no atomics whose order could leak into a result: the
 // layout is a pure function of topk_idx.
-#include <atomic>
+#include <cuda.h>
+
+#include <mutex>
 
 #include "ep_device.cuh"
 
 namespace ep {
 namespace {
 
-#ifndef EP_LAYOUT_SINGLE
-#define EP_LAYOUT_SINGLE 1
-#endif
 constexpr int kLTShift = 7;
 constexpr int kLT = 1 << kLTShift;  // tokens per CTA, one per thread
 constexpr int kLWarps = kLT / 32;
@@ -413,7 +412,7 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
                           int32_t* rank_offset, int32_t* slot, void* workspace, int32_t* status,
                           cudaStream_t stream) {
   const bool vec = (reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0;
-  if (T <= kSingleMaxT && EP_LAYOUT_SINGLE) {
+  if (T <= kSingleMaxT) {
     const size_t smem1 = sizeof(int32_t) * ((size_t)E + (size_t)T);
     static bool attr_set[128];
     int dev = 0;
@@ -483,12 +482,16 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
 // GPU that loads the library until the process exits.
 //
 // Host code cannot use the array's name as a device address (on the host it
-// names a stand-in), so the first call on each device asks the runtime for
-// the address with cudaGetSymbolAddress, with that device current, and caches
-// it; later calls reuse the cached address.  Every call uses the same array:
-// calls whose kernels overlap on the GPU (different streams, or different
-// host threads) race on it.  Nothing in it needs clearing between calls: each
-// call writes every word it reads before reading it.
+// names a stand-in), so the runtime is asked for the address with
+// cudaGetSymbolAddress, with the caller's device current.  The address belongs
+// to a CUDA context, not to a device number: the lookup is cached per device
+// together with the unique id of the context that was current (cuCtxGetId), and
+// repeated whenever that id changes (the primary context re-created after
+// cudaDeviceReset, or another context made current on the device).  Every call
+// uses the same array: calls whose kernels overlap on the GPU (different
+// streams, or different host threads) race on it.  Nothing in it needs
+// clearing between calls: each call writes every word it reads before reading
+// it.
 static __device__ __align__(256) unsigned char
     g_layout_noalloc_scratch[EP_LAYOUT_NOALLOC_SCRATCH_BYTES];
 
@@ -496,18 +499,75 @@ namespace ep {
 namespace {
 
 constexpr int kMaxDevices = 128;
-std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+// The driver's cuCtxGetCurrent and cuCtxGetId, resolved at run time through
+// the runtime (the library does not link the driver library itself).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+struct DriverFns {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+const DriverFns& driver_fns() {
+  static const DriverFns fns = [] {
+    DriverFns f;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<CtxGetIdFn>(p);
+    return f;
+  }();
+  return fns;
+}
+
+// Unique id of the current context; false when it cannot be had (no context
+// current yet, or an old driver).
+bool current_context_id(unsigned long long* id) {
+  const DriverFns& f = driver_fns();
+  if (f.get_current == nullptr || f.get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (f.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return f.get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+struct ScratchEntry {
+  unsigned long long ctx_id = 0;
+  void* addr = nullptr;
+};
+ScratchEntry g_noalloc_cache[kMaxDevices];
+std::mutex g_noalloc_mutex;
 
 cudaError_t noalloc_scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    e = cudaGetSymbolAddress(&p, g_layout_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_noalloc_addr[dev].store(p, std::memory_order_release);
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  ScratchEntry& c = g_noalloc_cache[dev];
+  if (have_id && c.addr != nullptr && c.ctx_id == id) {
+    *out = c.addr;
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_layout_noalloc_scratch);  // makes a context current if none was
+  if (e != cudaSuccess) return e;
+  unsigned long long id_now = 0;
+  if (current_context_id(&id_now)) {
+    c.ctx_id = id_now;
+    c.addr = p;
+  } else {
+    c.addr = nullptr;  // no id to key on: look the address up on every call
   }
   *out = p;
   return cudaSuccess;

@@ -33,16 +33,10 @@ constexpr int kXGroups = 4;                    // groups of 32 pairs per warp
 constexpr int kXPairs = kXWarps * kXGroups * 32;  // 1024 pairs per chunk
 constexpr int kXSingleWarps = 32;
 constexpr int kXSingleGroups = 8;
-#ifndef EP_XSINGLE_MAX
-#define EP_XSINGLE_MAX 2048
-#endif
-constexpr int64_t kXSingleMax = EP_XSINGLE_MAX;  // <= kXSingleWarps * kXSingleGroups * 32
+constexpr int64_t kXSingleMax = 2048;  // <= kXSingleWarps * kXSingleGroups * 32
 static_assert(kXSingleMax <= kXSingleWarps * kXSingleGroups * 32, "one CTA holds 8192 pairs");
 constexpr int kXSingleMaxE = 1024;
-#ifndef EP_XSELF_SCAN_MAX_CHUNKS
-#define EP_XSELF_SCAN_MAX_CHUNKS 32
-#endif
-constexpr int64_t kXSelfScanMaxChunks = EP_XSELF_SCAN_MAX_CHUNKS;
+constexpr int64_t kXSelfScanMaxChunks = 32;
 constexpr int kXMaxE = 4096;
 
 inline size_t a256(size_t b) { return (b + 255) & ~size_t(255); }

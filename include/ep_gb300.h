@@ -75,7 +75,9 @@ enum {
 
 /*
  * Bytes of device workspace that ep_dispatch_layout needs for T tokens, W
- * ranks and E experts.  The contents need no initialisation.
+ * ranks and E experts.  The contents need no initialisation.  Returns 0 for
+ * invalid arguments.  Host only.  A convention of this library (the caller
+ * owns all device memory); the pages define no such call.
  */
 EP_API size_t ep_layout_workspace_bytes(int64_t T, int W, int E);
 
@@ -182,7 +184,8 @@ EP_API int ep_dispatch_with_layout(const void* x, const int32_t* topk_idx, const
  * (T > 1024, FP8 rows or bf16 rows of at least 1 KB, and a chunk table
  * (ceil(T / 128) * W ints) of at most 16 KB); else the layout's kernels (1 for
  * T <= 1024, else 2) plus 1 for the dispatch when T > 0.  Returns -1 for
- * invalid arguments.  Host only.
+ * invalid arguments.  Host only.  A convention of this library; the pages
+ * define no such call.
  */
 EP_API int ep_dispatch_with_layout_launches(int64_t T, int H, int k, int W, int quant);
 
@@ -255,9 +258,11 @@ EP_API int ep_combine(const void* y, const int32_t* slot, int64_t T, int H, int 
  * the call allocates nothing.
  *  - Returns EP_ERR_WORKSPACE when ep_layout_workspace_bytes(T, W, E) exceeds
  *    EP_LAYOUT_NOALLOC_SCRATCH_BYTES (up to 85504 tokens at W = 8, E = 256).
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) and caches it; make that first call before any
- *    stream capture on that device.
+ *  - The first call in a CUDA context looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it per device, keyed by the context's
+ *    unique id: a context re-created after cudaDeviceReset, or another context
+ *    made current on the device, triggers a new lookup, never a stale address.
+ *    Make that first call in each context before any stream capture in it.
  *  - All calls share the one array: calls whose kernels overlap on the GPU
  *    (other streams, other host threads) race and must be serialised by the
  *    caller.  The array needs no clearing: each call writes what it reads.
@@ -294,6 +299,9 @@ EP_API int ep_dispatch_layout_noalloc(const int32_t* topk_idx, int64_t T, int k,
  *                         16-byte aligned, no initialisation
  * Limits: 1 <= k; 1 <= E <= 4096; T * k < 2^31.  Up to 8192 pairs and 1024
  * experts it is one kernel on one CTA, above that three kernels.
+ * ep_layout_experts_workspace_bytes (host only, 0 for invalid arguments) is a
+ * convention of this library, like ep_layout_workspace_bytes; the pages define
+ * no such call.
  */
 EP_API size_t ep_layout_experts_workspace_bytes(int64_t T, int k, int E);
 EP_API int ep_dispatch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,
@@ -366,6 +374,8 @@ EP_API int ep_combine_weighted(const void* y, const int32_t* slot, const float* 
  *  amax           fp32 [E], read and written
  * Experts whose rows leave [0, capacity_rows) are skipped and set
  * EP_STATUS_CAPACITY.  Limits: H % 256 == 0; 1 <= E <= 8192.
+ * ep_cast_transpose_t_bytes (host only, 0 for invalid arguments) gives the
+ * size of out_t; a convention of this library, the pages define no such call.
  */
 EP_API size_t ep_cast_transpose_t_bytes(int64_t capacity_rows, int E, int H);
 EP_API int ep_cast_transpose_experts(const void* y, const int32_t* expert_offset, int E, int H,
@@ -379,11 +389,14 @@ EP_API int ep_cast_transpose_experts(const void* y, const int32_t* expert_offset
  * about one second the wait gives up: the kernel ORs EP_STATUS_TIMEOUT into
  * *status (device int32, required) and returns, and the context stays usable.
  * Returns EP_OK once the kernel is enqueued; the caller synchronises and reads
- * *status.
+ * *status.  A diagnostic of this library; the pages define no such call (their
+ * waits on peer memory are unbounded).
  */
 EP_API int ep_selftest_wait_timeout(int32_t* status, ep_stream_t stream);
 
-/* Human-readable name of an EP_* return code (static string). */
+/* Human-readable name of an EP_* return code (static string, never NULL;
+ * "unknown ep status code" for other values).  Host only.  A convention of
+ * this library; the pages define no such call. */
 EP_API const char* ep_status_string(int code);
 
 #ifdef __cplusplus

@@ -133,6 +133,12 @@ def _stream(stream):
     return int(stream)
 
 
+try:  # the current device without building a torch.device
+    _current_device = torch._C._cuda_getDevice
+except AttributeError:  # pragma: no cover - older or newer torch
+    _current_device = torch.cuda.current_device
+
+
 def _check_cuda(name: str, t: torch.Tensor | None, dtype=None, optional=False):
     if t is None:
         if optional:
@@ -140,10 +146,77 @@ def _check_cuda(name: str, t: torch.Tensor | None, dtype=None, optional=False):
         raise ValueError(f"{name} is required")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != _current_device():
+        raise ValueError(f"{name} is on {t.device}, not on the current device "
+                         f"cuda:{_current_device()} where the kernels run")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _shape(name: str, t: torch.Tensor | None, *shape: int):
+    """The kernels trust the sizes they are given: every tensor must have
+    exactly the shape the sizes imply (checked before anything is launched)."""
+    if t is not None and tuple(t.shape) != shape:
+        raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+
+
+def _rows(name: str, t: torch.Tensor | None, *inner: int) -> int | None:
+    """Receive tensors: [capacity_rows, *inner]; returns capacity_rows."""
+    if t is None:
+        return None
+    if t.dim() != 1 + len(inner) or tuple(t.shape[1:]) != inner:
+        want = ", ".join(["capacity_rows", *map(str, inner)])
+        raise ValueError(f"{name} must have shape ({want}), got {tuple(t.shape)}")
+    return int(t.shape[0])
+
+
+def _status(status: torch.Tensor | None):
+    if status is not None and status.numel() < 1:
+        raise ValueError("status must hold at least one int32")
+
+
+def _matrix(name: str, t: torch.Tensor) -> tuple[int, int]:
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(t.shape)}")
+    return int(t.shape[0]), int(t.shape[1])
+
+
+def _check_layout_shapes(topk_idx, E, W, ne, nr, off, slot, status):
+    T, k = _matrix("topk_idx", topk_idx)
+    _shape("num_tokens_per_expert", ne, E)
+    _shape("num_tokens_per_rank", nr, W)
+    _shape("rank_offset", off, W + 1)
+    _shape("slot", slot, T, W)
+    _status(status)
+    return T, k
+
+
+def _check_dispatch_shapes(x, topk_idx, topk_w, C, slot, recv_x, recv_topk_idx, recv_topk_w,
+                           recv_src, recv_scale, quant, status):
+    """Shapes of a dispatch's tensors (C = columns of the slot table); returns
+    (T, H, k, capacity_rows)."""
+    T, H = _matrix("x", x)
+    _, k = _matrix("topk_idx", topk_idx)
+    _shape("topk_idx", topk_idx, T, k)
+    _shape("topk_w", topk_w, T, k)
+    _shape("slot", slot, T, C)
+    cap = _rows("recv_x", recv_x, H)
+    _rows("recv_topk_idx", recv_topk_idx, k)
+    _rows("recv_topk_w", recv_topk_w, k)
+    _rows("recv_src", recv_src)
+    for n, t in (("recv_topk_idx", recv_topk_idx), ("recv_topk_w", recv_topk_w),
+                 ("recv_src", recv_src)):
+        if t is not None and t.shape[0] != cap:
+            raise ValueError(f"{n} must have capacity_rows = recv_x.shape[0] = {cap} rows, "
+                             f"got {t.shape[0]}")
+    if quant == EP_QUANT_FP8_E4M3_B128 and recv_scale is not None:
+        if H % 128 != 0:
+            raise ValueError("FP8 dispatch needs H % 128 == 0")
+        _shape("recv_scale", recv_scale, cap, H // 128)
+    _status(status)
+    return T, H, k, cap
 
 
 def _raise(fn: str, code: int):
@@ -173,13 +246,14 @@ def ep_dispatch_layout(topk_idx: torch.Tensor, E: int, W: int,
     """ep_dispatch_layout: per-expert and per-rank counts, rank_offset and the
     slot of every (token, rank) pair for topk_idx [T, k] (int32 CUDA tensors;
     workspace of ep_layout_workspace_bytes(T, W, E) bytes)."""
+    T, k = _check_layout_shapes(topk_idx, E, W, num_tokens_per_expert, num_tokens_per_rank,
+                                rank_offset, slot, status)
     for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
                  ("num_tokens_per_rank", num_tokens_per_rank), ("rank_offset", rank_offset),
                  ("slot", slot)):
         _check_cuda(n, t, torch.int32)
     _check_cuda("workspace", workspace)
     _check_cuda("status", status, torch.int32, optional=True)
-    T, k = topk_idx.shape
     rc = load_library().ep_dispatch_layout(
         _ptr(topk_idx), T, k, E, W, _ptr(num_tokens_per_expert), _ptr(num_tokens_per_rank),
         _ptr(rank_offset), _ptr(slot), _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -187,14 +261,8 @@ def ep_dispatch_layout(topk_idx: torch.Tensor, E: int, W: int,
     _raise("ep_dispatch_layout", rc)
 
 
-def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor, W: int,
-                slot: torch.Tensor, recv_x: torch.Tensor, recv_topk_idx: torch.Tensor | None = None,
-                recv_topk_w: torch.Tensor | None = None, recv_src: torch.Tensor | None = None,
-                recv_scale: torch.Tensor | None = None, quant: int = EP_QUANT_BF16,
-                status: torch.Tensor | None = None, stream=None) -> None:
-    """ep_dispatch: rows of x [T, H] bf16 to their receive rows (bf16, or FP8
-    codes with recv_scale for EP_QUANT_FP8_E4M3_B128) with the metadata; the
-    capacity is recv_x.shape[0]."""
+def _check_dispatch_cuda(x, topk_idx, topk_w, slot, recv_x, recv_topk_idx, recv_topk_w, recv_src,
+                         recv_scale, quant, status):
     _check_cuda("x", x, torch.bfloat16)
     _check_cuda("topk_idx", topk_idx, torch.int32)
     _check_cuda("topk_w", topk_w, torch.float32)
@@ -205,10 +273,22 @@ def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor, W
     _check_cuda("recv_src", recv_src, torch.int32, optional=True)
     _check_cuda("recv_scale", recv_scale, torch.float32, optional=quant == EP_QUANT_BF16)
     _check_cuda("status", status, torch.int32, optional=True)
-    T, H = x.shape
-    k = topk_idx.shape[1]
+
+
+def ep_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor, W: int,
+                slot: torch.Tensor, recv_x: torch.Tensor, recv_topk_idx: torch.Tensor | None = None,
+                recv_topk_w: torch.Tensor | None = None, recv_src: torch.Tensor | None = None,
+                recv_scale: torch.Tensor | None = None, quant: int = EP_QUANT_BF16,
+                status: torch.Tensor | None = None, stream=None) -> None:
+    """ep_dispatch: rows of x [T, H] bf16 to their receive rows (bf16, or FP8
+    codes with recv_scale for EP_QUANT_FP8_E4M3_B128) with the metadata; the
+    capacity is recv_x.shape[0]."""
+    T, H, k, cap = _check_dispatch_shapes(x, topk_idx, topk_w, W, slot, recv_x, recv_topk_idx,
+                                          recv_topk_w, recv_src, recv_scale, quant, status)
+    _check_dispatch_cuda(x, topk_idx, topk_w, slot, recv_x, recv_topk_idx, recv_topk_w, recv_src,
+                         recv_scale, quant, status)
     rc = load_library().ep_dispatch(
-        _ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, W, _ptr(slot), recv_x.shape[0], quant,
+        _ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, W, _ptr(slot), cap, quant,
         _ptr(recv_x), _ptr(recv_scale), _ptr(recv_topk_idx), _ptr(recv_topk_w), _ptr(recv_src),
         _ptr(status), _stream(stream))
     _raise("ep_dispatch", rc)
@@ -225,25 +305,20 @@ def ep_dispatch_with_layout(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: tor
                             status: torch.Tensor | None = None, stream=None) -> None:
     """ep_dispatch_layout + ep_dispatch in one call (the dispatch starts
     loading x while the layout runs)."""
-    for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
-                 ("num_tokens_per_rank", num_tokens_per_rank), ("rank_offset", rank_offset),
-                 ("slot", slot)):
+    _check_layout_shapes(topk_idx, E, W, num_tokens_per_expert, num_tokens_per_rank, rank_offset,
+                         slot, status)
+    T, H, k, cap = _check_dispatch_shapes(x, topk_idx, topk_w, W, slot, recv_x, recv_topk_idx,
+                                          recv_topk_w, recv_src, recv_scale, quant, status)
+    for n, t in (("num_tokens_per_expert", num_tokens_per_expert),
+                 ("num_tokens_per_rank", num_tokens_per_rank), ("rank_offset", rank_offset)):
         _check_cuda(n, t, torch.int32)
     _check_cuda("workspace", workspace)
-    _check_cuda("x", x, torch.bfloat16)
-    _check_cuda("topk_w", topk_w, torch.float32)
-    _check_cuda("recv_x", recv_x, torch.bfloat16 if quant == EP_QUANT_BF16 else torch.uint8)
-    _check_cuda("recv_topk_idx", recv_topk_idx, torch.int32, optional=True)
-    _check_cuda("recv_topk_w", recv_topk_w, torch.float32, optional=True)
-    _check_cuda("recv_src", recv_src, torch.int32, optional=True)
-    _check_cuda("recv_scale", recv_scale, torch.float32, optional=quant == EP_QUANT_BF16)
-    _check_cuda("status", status, torch.int32, optional=True)
-    T, H = x.shape
-    k = topk_idx.shape[1]
+    _check_dispatch_cuda(x, topk_idx, topk_w, slot, recv_x, recv_topk_idx, recv_topk_w, recv_src,
+                         recv_scale, quant, status)
     rc = load_library().ep_dispatch_with_layout(
         _ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, E, W, _ptr(num_tokens_per_expert),
         _ptr(num_tokens_per_rank), _ptr(rank_offset), _ptr(slot), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), recv_x.shape[0], quant, _ptr(recv_x),
+        workspace.numel() * workspace.element_size(), cap, quant, _ptr(recv_x),
         _ptr(recv_scale), _ptr(recv_topk_idx), _ptr(recv_topk_w), _ptr(recv_src), _ptr(status),
         _stream(stream))
     _raise("ep_dispatch_with_layout", rc)
@@ -261,24 +336,21 @@ def ep_dispatch_experts_with_layout(x: torch.Tensor, topk_idx: torch.Tensor, top
                                     stream=None) -> None:
     """ep_dispatch_layout_experts + ep_dispatch (W = k) in one call (the
     dispatch starts loading x while the layout runs)."""
-    for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
-                 ("expert_offset", expert_offset), ("slot", slot)):
+    _, k = _matrix("topk_idx", topk_idx)
+    T, H, k, cap = _check_dispatch_shapes(x, topk_idx, topk_w, k, slot, recv_x, recv_topk_idx,
+                                          recv_topk_w, recv_src, recv_scale, quant, status)
+    _shape("num_tokens_per_expert", num_tokens_per_expert, E)
+    _shape("expert_offset", expert_offset, E + 1)
+    for n, t in (("num_tokens_per_expert", num_tokens_per_expert),
+                 ("expert_offset", expert_offset)):
         _check_cuda(n, t, torch.int32)
     _check_cuda("workspace", workspace)
-    _check_cuda("x", x, torch.bfloat16)
-    _check_cuda("topk_w", topk_w, torch.float32)
-    _check_cuda("recv_x", recv_x, torch.bfloat16 if quant == EP_QUANT_BF16 else torch.uint8)
-    _check_cuda("recv_topk_idx", recv_topk_idx, torch.int32, optional=True)
-    _check_cuda("recv_topk_w", recv_topk_w, torch.float32, optional=True)
-    _check_cuda("recv_src", recv_src, torch.int32, optional=True)
-    _check_cuda("recv_scale", recv_scale, torch.float32, optional=quant == EP_QUANT_BF16)
-    _check_cuda("status", status, torch.int32, optional=True)
-    T, H = x.shape
-    k = topk_idx.shape[1]
+    _check_dispatch_cuda(x, topk_idx, topk_w, slot, recv_x, recv_topk_idx, recv_topk_w, recv_src,
+                         recv_scale, quant, status)
     rc = load_library().ep_dispatch_experts_with_layout(
         _ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, E, _ptr(num_tokens_per_expert),
         _ptr(expert_offset), _ptr(slot), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), recv_x.shape[0], quant, _ptr(recv_x),
+        workspace.numel() * workspace.element_size(), cap, quant, _ptr(recv_x),
         _ptr(recv_scale), _ptr(recv_topk_idx), _ptr(recv_topk_w), _ptr(recv_src), _ptr(status),
         _stream(stream))
     _raise("ep_dispatch_experts_with_layout", rc)
@@ -290,20 +362,26 @@ def ep_dispatch_with_layout_launches(T: int, H: int, k: int, W: int,
     return int(load_library().ep_dispatch_with_layout_launches(T, H, k, W, quant))
 
 
+def _check_combine_shapes(y, slot, out, status):
+    T, C = _matrix("slot", slot)
+    _, H = _matrix("out", out)
+    _shape("out", out, T, H)
+    cap = _rows("y", y, H)
+    _status(status)
+    return T, C, H, cap
+
+
 def ep_combine(y: torch.Tensor, slot: torch.Tensor, out: torch.Tensor,
                status: torch.Tensor | None = None, stream=None) -> None:
     """ep_combine: out[t] = bf16 of the fp32 sum, in ascending rank order from
     +0, of the rows y[slot[t][r]] (y [capacity_rows, H] bf16)."""
+    T, W, H, cap = _check_combine_shapes(y, slot, out, status)
     _check_cuda("y", y, torch.bfloat16)
     _check_cuda("slot", slot, torch.int32)
     _check_cuda("out", out, torch.bfloat16)
     _check_cuda("status", status, torch.int32, optional=True)
-    T, W = slot.shape
-    H = out.shape[1]
-    if y.dim() != 2 or y.shape[1] != H:
-        raise ValueError("y must be [capacity_rows, H] with the same H as out")
-    rc = load_library().ep_combine(_ptr(y), _ptr(slot), T, H, W, y.shape[0], _ptr(out),
-                                   _ptr(status), _stream(stream))
+    rc = load_library().ep_combine(_ptr(y), _ptr(slot), T, H, W, cap, _ptr(out), _ptr(status),
+                                   _stream(stream))
     _raise("ep_combine", rc)
 
 
@@ -315,12 +393,13 @@ def ep_dispatch_layout_noalloc(topk_idx: torch.Tensor, E: int, W: int,
     """ep_dispatch_layout for callers that cannot allocate device memory: the
     workspace is the library's built-in EP_LAYOUT_NOALLOC_SCRATCH_BYTES array,
     shared by every call (calls that overlap on the GPU race on it)."""
+    T, k = _check_layout_shapes(topk_idx, E, W, num_tokens_per_expert, num_tokens_per_rank,
+                                rank_offset, slot, status)
     for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
                  ("num_tokens_per_rank", num_tokens_per_rank), ("rank_offset", rank_offset),
                  ("slot", slot)):
         _check_cuda(n, t, torch.int32)
     _check_cuda("status", status, torch.int32, optional=True)
-    T, k = topk_idx.shape
     rc = load_library().ep_dispatch_layout_noalloc(
         _ptr(topk_idx), T, k, E, W, _ptr(num_tokens_per_expert), _ptr(num_tokens_per_rank),
         _ptr(rank_offset), _ptr(slot), _ptr(status), _stream(stream))
@@ -335,22 +414,18 @@ def ep_dispatch_fused(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Ten
                       recv_src: torch.Tensor | None = None, status: torch.Tensor | None = None,
                       stream=None) -> None:
     """ep_dispatch_layout + bf16 ep_dispatch in one launch (T <= EP_FUSED_MAX_TOKENS)."""
-    _check_cuda("x", x, torch.bfloat16)
-    for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
-                 ("num_tokens_per_rank", num_tokens_per_rank), ("rank_offset", rank_offset),
-                 ("slot", slot)):
+    _check_layout_shapes(topk_idx, E, W, num_tokens_per_expert, num_tokens_per_rank, rank_offset,
+                         slot, status)
+    T, H, k, cap = _check_dispatch_shapes(x, topk_idx, topk_w, W, slot, recv_x, recv_topk_idx,
+                                          recv_topk_w, recv_src, None, EP_QUANT_BF16, status)
+    for n, t in (("num_tokens_per_expert", num_tokens_per_expert),
+                 ("num_tokens_per_rank", num_tokens_per_rank), ("rank_offset", rank_offset)):
         _check_cuda(n, t, torch.int32)
-    _check_cuda("topk_w", topk_w, torch.float32)
-    _check_cuda("recv_x", recv_x, torch.bfloat16)
-    _check_cuda("recv_topk_idx", recv_topk_idx, torch.int32, optional=True)
-    _check_cuda("recv_topk_w", recv_topk_w, torch.float32, optional=True)
-    _check_cuda("recv_src", recv_src, torch.int32, optional=True)
-    _check_cuda("status", status, torch.int32, optional=True)
-    T, H = x.shape
-    k = topk_idx.shape[1]
+    _check_dispatch_cuda(x, topk_idx, topk_w, slot, recv_x, recv_topk_idx, recv_topk_w, recv_src,
+                         None, EP_QUANT_BF16, status)
     rc = load_library().ep_dispatch_fused(
         _ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, E, W, _ptr(num_tokens_per_expert),
-        _ptr(num_tokens_per_rank), _ptr(rank_offset), _ptr(slot), recv_x.shape[0], _ptr(recv_x),
+        _ptr(num_tokens_per_rank), _ptr(rank_offset), _ptr(slot), cap, _ptr(recv_x),
         _ptr(recv_topk_idx), _ptr(recv_topk_w), _ptr(recv_src), _ptr(status), _stream(stream))
     _raise("ep_dispatch_fused", rc)
 
@@ -358,9 +433,10 @@ def ep_dispatch_fused(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Ten
 def ep_localize_expert_ids(recv_topk_idx: torch.Tensor, rank_offset: torch.Tensor, E: int, W: int,
                            stream=None) -> None:
     """In place: ids of rank r's receive rows become local indices e - r*(E/W), or -1."""
+    cap, k = _matrix("recv_topk_idx", recv_topk_idx)
+    _shape("rank_offset", rank_offset, W + 1)
     _check_cuda("recv_topk_idx", recv_topk_idx, torch.int32)
     _check_cuda("rank_offset", rank_offset, torch.int32)
-    cap, k = recv_topk_idx.shape
     rc = load_library().ep_localize_expert_ids(_ptr(recv_topk_idx), _ptr(rank_offset), cap, k, E, W,
                                                _stream(stream))
     _raise("ep_localize_expert_ids", rc)
@@ -377,14 +453,16 @@ def ep_dispatch_layout_experts(topk_idx: torch.Tensor, E: int, num_tokens_per_ex
                                stream=None) -> None:
     """Expert-major layout: slot [T, k] gives each valid (token, column) pair its
     own row, rows grouped by expert (expert_offset [E + 1])."""
+    T, k = _matrix("topk_idx", topk_idx)
+    _shape("num_tokens_per_expert", num_tokens_per_expert, E)
+    _shape("expert_offset", expert_offset, E + 1)
+    _shape("slot", slot, T, k)
+    _status(status)
     for n, t in (("topk_idx", topk_idx), ("num_tokens_per_expert", num_tokens_per_expert),
                  ("expert_offset", expert_offset), ("slot", slot)):
         _check_cuda(n, t, torch.int32)
     _check_cuda("workspace", workspace)
     _check_cuda("status", status, torch.int32, optional=True)
-    T, k = topk_idx.shape
-    if tuple(slot.shape) != (T, k):
-        raise ValueError("slot must be [T, k]")
     rc = load_library().ep_dispatch_layout_experts(
         _ptr(topk_idx), T, k, E, _ptr(num_tokens_per_expert), _ptr(expert_offset), _ptr(slot),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
@@ -396,18 +474,14 @@ def ep_combine_weighted(y: torch.Tensor, slot: torch.Tensor, w: torch.Tensor, ou
                         status: torch.Tensor | None = None, stream=None) -> None:
     """out[t] = bf16 of the fp32 FMA chain over the columns c of slot[t] >= 0,
     in ascending order, of w[t][c] * y[slot[t][c]]."""
+    T, C, H, cap = _check_combine_shapes(y, slot, out, status)
+    _shape("w", w, T, C)
     _check_cuda("y", y, torch.bfloat16)
     _check_cuda("slot", slot, torch.int32)
     _check_cuda("w", w, torch.float32)
     _check_cuda("out", out, torch.bfloat16)
     _check_cuda("status", status, torch.int32, optional=True)
-    T, C = slot.shape
-    H = out.shape[1]
-    if y.dim() != 2 or y.shape[1] != H:
-        raise ValueError("y must be [capacity_rows, H] with the same H as out")
-    if tuple(w.shape) != (T, C):
-        raise ValueError("w must have the shape of slot")
-    rc = load_library().ep_combine_weighted(_ptr(y), _ptr(slot), _ptr(w), T, H, C, y.shape[0],
+    rc = load_library().ep_combine_weighted(_ptr(y), _ptr(slot), _ptr(w), T, H, C, cap,
                                             _ptr(out), _ptr(status), _stream(stream))
     _raise("ep_combine_weighted", rc)
 
@@ -415,6 +489,7 @@ def ep_combine_weighted(y: torch.Tensor, slot: torch.Tensor, w: torch.Tensor, ou
 def ep_selftest_wait_timeout(status: torch.Tensor, stream=None) -> None:
     """Diagnostic: a kernel whose bounded wait must run out (about one second)
     and set EP_STATUS_TIMEOUT in ``status``."""
+    _status(status)
     _check_cuda("status", status, torch.int32)
     rc = load_library().ep_selftest_wait_timeout(_ptr(status), _stream(stream))
     _raise("ep_selftest_wait_timeout", rc)
@@ -430,6 +505,14 @@ def ep_cast_transpose_experts(y: torch.Tensor, expert_offset: torch.Tensor, scal
                               status: torch.Tensor | None = None, stream=None) -> None:
     """FP8 cast (out_c) and per-expert transposed cast (out_t) of the
     expert-major rows y, amax[e] = max(amax[e], max |x|)."""
+    cap, H = _matrix("y", y)
+    if expert_offset.dim() != 1 or expert_offset.numel() < 2:
+        raise ValueError("expert_offset must be [E + 1] with E >= 1")
+    E = expert_offset.numel() - 1
+    _shape("scale", scale, E)
+    _shape("amax", amax, E)
+    _shape("out_c", out_c, cap, H)
+    _status(status)
     _check_cuda("y", y, torch.bfloat16)
     _check_cuda("expert_offset", expert_offset, torch.int32)
     _check_cuda("scale", scale, torch.float32)
@@ -437,10 +520,6 @@ def ep_cast_transpose_experts(y: torch.Tensor, expert_offset: torch.Tensor, scal
     _check_cuda("out_t", out_t, torch.uint8)
     _check_cuda("amax", amax, torch.float32)
     _check_cuda("status", status, torch.int32, optional=True)
-    cap, H = y.shape
-    E = expert_offset.numel() - 1
-    if tuple(out_c.shape) != (cap, H):
-        raise ValueError("out_c must have the shape of y")
     if out_t.numel() < ep_cast_transpose_t_bytes(cap, E, H):
         raise ValueError("out_t is smaller than ep_cast_transpose_t_bytes(capacity_rows, E, H)")
     rc = load_library().ep_cast_transpose_experts(_ptr(y), _ptr(expert_offset), E, H, _ptr(scale),

@@ -3,15 +3,16 @@ allocate device memory (C or embedded hosts without a device allocator, and
 latency-critical paths that must not call cudaMalloc, which blocks the host and
 synchronises the device).  It keeps its workspace in a device array built into
 the library, so these tests check that its outputs equal those of
-ep_dispatch_layout (caller-provided workspace) bit for bit, over two calls in a
-row: the array keeps the previous call's contents, which must not leak into the
-next result.  Collected last so that a run stopping at its first failure has
-already run every other test."""
+ep_dispatch_layout (caller-provided workspace) and those of the CPU oracle's
+layout bit for bit, over two calls in a row: the array keeps the previous
+call's contents, which must not leak into the next result.  Collected last so
+that a run stopping at its first failure has already run every other test."""
 import numpy as np
 import pytest
 import torch
 
 import combine_ep_dispatch_gb300 as ep
+import oracle
 from combine_ep_dispatch_gb300.inputs import make_routing
 
 pytestmark = pytest.mark.gpu
@@ -74,6 +75,10 @@ def test_noalloc_matches_workspace_layout_two_calls_in_a_row(first, second):
         torch.cuda.synchronize()
         for key in want:
             assert torch.equal(got[key], want[key]), (n, key)
+        ref = oracle.layout(idx.cpu().numpy(), E, W)
+        for key in ("num_tokens_per_expert", "num_tokens_per_rank", "rank_offset", "slot"):
+            np.testing.assert_array_equal(got[key].cpu().numpy(), ref[key], err_msg=f"{n} {key}")
+        assert int(got["status"].item()) == ref["status"], n
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():

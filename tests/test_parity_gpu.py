@@ -421,9 +421,11 @@ def test_host_errors_through_binding():
     cfg = inp["cfg"]
     dc = ep.DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W)
     idx = torch.from_numpy(inp["topk_idx"]).cuda()
-    with pytest.raises(ep.EPError) as e:
-        ep.ep_dispatch_layout(idx, cfg.E, 3, dc.num_tokens_per_expert, dc.num_tokens_per_rank,
-                              dc.rank_offset, dc.slot, dc.workspace, dc.status)   # E % W != 0
+    i32 = dict(dtype=torch.int32, device="cuda")
+    with pytest.raises(ep.EPError) as e:   # shapes fit W = 3, but E % W != 0
+        ep.ep_dispatch_layout(idx, cfg.E, 3, dc.num_tokens_per_expert, torch.zeros(3, **i32),
+                              torch.zeros(4, **i32), torch.zeros(cfg.T, 3, **i32), dc.workspace,
+                              dc.status)
     assert e.value.code == ep.EP_ERR_INVALID_ARG
     small = torch.empty(8, dtype=torch.uint8, device="cuda")
     with pytest.raises(ep.EPError) as e:

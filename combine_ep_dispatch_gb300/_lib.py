@@ -33,13 +33,21 @@ EXPORTED = ("ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_dispatch_layout
             "ep_localize_expert_ids", "ep_layout_experts_workspace_bytes",
             "ep_dispatch_layout_experts", "ep_combine_weighted", "ep_selftest_wait_timeout",
             "ep_cast_transpose_t_bytes", "ep_cast_transpose_experts", "ep_dispatch_with_layout",
-            "ep_dispatch_with_layout_launches", "ep_dispatch_experts_with_layout")
+            "ep_dispatch_with_layout_launches", "ep_dispatch_experts_with_layout",
+            "ep_dispatch_regions", "ep_combine_regions")
 
 # Largest batch ep_dispatch_fused takes.
 EP_FUSED_MAX_TOKENS = 1024
 
 # Size of the library's built-in layout workspace (ep_dispatch_layout_noalloc).
 EP_LAYOUT_NOALLOC_SCRATCH_BYTES = 1 << 20
+
+
+class RankRegion(ctypes.Structure):
+    """ep_rank_region_t: the receive storage of one rank (device pointers)."""
+    _fields_ = [("recv_x", ctypes.c_void_p), ("recv_scale", ctypes.c_void_p),
+                ("recv_topk_idx", ctypes.c_void_p), ("recv_topk_w", ctypes.c_void_p),
+                ("recv_src", ctypes.c_void_p), ("rows", ctypes.c_int64)]
 
 
 class EPError(RuntimeError):
@@ -104,6 +112,13 @@ def load_library() -> ctypes.CDLL:
     lib.ep_cast_transpose_t_bytes.restype = ctypes.c_size_t
     lib.ep_cast_transpose_experts.argtypes = [_P, _P, _I, _I, _P, _I64, _P, _P, _P, _P, _P]
     lib.ep_cast_transpose_experts.restype = _I
+    lib.ep_dispatch_regions.argtypes = [_P, _P, _P, _I64, _I, _I, _I, _P, _P,
+                                        ctypes.POINTER(RankRegion), _I, _P, _P]
+    lib.ep_dispatch_regions.restype = _I
+    lib.ep_combine_regions.argtypes = [ctypes.POINTER(ctypes.c_void_p),
+                                       ctypes.POINTER(ctypes.c_int64), _P, _P, _I64, _I, _I, _P,
+                                       _P, _P]
+    lib.ep_combine_regions.restype = _I
     lib.ep_selftest_wait_timeout.argtypes = [_P, _P]
     lib.ep_selftest_wait_timeout.restype = _I
     lib.ep_status_string.argtypes = [_I]
@@ -526,3 +541,84 @@ def ep_cast_transpose_experts(y: torch.Tensor, expert_offset: torch.Tensor, scal
                                                   cap, _ptr(out_c), _ptr(out_t), _ptr(amax),
                                                   _ptr(status), _stream(stream))
     _raise("ep_cast_transpose_experts", rc)
+
+
+def ep_dispatch_regions(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                        slot: torch.Tensor, rank_offset: torch.Tensor, regions: list[dict],
+                        quant: int = EP_QUANT_BF16, status: torch.Tensor | None = None,
+                        stream=None) -> None:
+    """ep_dispatch into per-rank regions: ``regions[r]`` is a dict with rank r's
+    receive tensors ``recv_x`` [rows_r, H] (bf16, or uint8 codes for FP8),
+    ``recv_scale`` [rows_r, H / 128] (FP8), and optionally ``recv_topk_idx``
+    [rows_r, k], ``recv_topk_w`` [rows_r, k], ``recv_src`` [rows_r]; token t's
+    row for rank r lands in row slot[t][r] - rank_offset[r] of region r."""
+    W = len(regions)
+    if W < 1 or W > 32:
+        raise ValueError("regions must name 1 to 32 ranks")
+    T, H = _matrix("x", x)
+    _, k = _matrix("topk_idx", topk_idx)
+    _shape("topk_idx", topk_idx, T, k)
+    _shape("topk_w", topk_w, T, k)
+    _shape("slot", slot, T, W)
+    _shape("rank_offset", rank_offset, W + 1)
+    _status(status)
+    fp8 = quant == EP_QUANT_FP8_E4M3_B128
+    table = (RankRegion * W)()
+    for r, g in enumerate(regions):
+        rx = g["recv_x"]
+        rows = _rows(f"regions[{r}].recv_x", rx, H)
+        _rows(f"regions[{r}].recv_topk_idx", g.get("recv_topk_idx"), k)
+        _rows(f"regions[{r}].recv_topk_w", g.get("recv_topk_w"), k)
+        _rows(f"regions[{r}].recv_src", g.get("recv_src"))
+        for n in ("recv_topk_idx", "recv_topk_w", "recv_src"):
+            t = g.get(n)
+            if t is not None and t.shape[0] != rows:
+                raise ValueError(f"regions[{r}].{n} must have {rows} rows, got {t.shape[0]}")
+        if fp8:
+            _shape(f"regions[{r}].recv_scale", g.get("recv_scale"), rows, H // 128)
+        _check_cuda(f"regions[{r}].recv_x", rx, torch.uint8 if fp8 else torch.bfloat16)
+        _check_cuda(f"regions[{r}].recv_scale", g.get("recv_scale"), torch.float32,
+                    optional=not fp8)
+        _check_cuda(f"regions[{r}].recv_topk_idx", g.get("recv_topk_idx"), torch.int32,
+                    optional=True)
+        _check_cuda(f"regions[{r}].recv_topk_w", g.get("recv_topk_w"), torch.float32, optional=True)
+        _check_cuda(f"regions[{r}].recv_src", g.get("recv_src"), torch.int32, optional=True)
+        table[r] = RankRegion(_ptr(rx), _ptr(g.get("recv_scale") if fp8 else None),
+                              _ptr(g.get("recv_topk_idx")), _ptr(g.get("recv_topk_w")),
+                              _ptr(g.get("recv_src")), rows)
+    _check_cuda("x", x, torch.bfloat16)
+    _check_cuda("topk_idx", topk_idx, torch.int32)
+    _check_cuda("topk_w", topk_w, torch.float32)
+    _check_cuda("slot", slot, torch.int32)
+    _check_cuda("rank_offset", rank_offset, torch.int32)
+    _check_cuda("status", status, torch.int32, optional=True)
+    rc = load_library().ep_dispatch_regions(
+        _ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, W, _ptr(slot), _ptr(rank_offset), table,
+        quant, _ptr(status), _stream(stream))
+    _raise("ep_dispatch_regions", rc)
+
+
+def ep_combine_regions(y_regions: list[torch.Tensor], slot: torch.Tensor, rank_offset: torch.Tensor,
+                       out: torch.Tensor, status: torch.Tensor | None = None, stream=None) -> None:
+    """ep_combine with rank r's expert outputs in ``y_regions[r]`` [rows_r, H]
+    (bf16): row slot[t][r] - rank_offset[r] of it belongs to token t."""
+    W = len(y_regions)
+    if W < 1 or W > 32:
+        raise ValueError("y_regions must name 1 to 32 ranks")
+    T, H = _matrix("out", out)
+    _shape("slot", slot, T, W)
+    _shape("rank_offset", rank_offset, W + 1)
+    _status(status)
+    ptrs = (ctypes.c_void_p * W)()
+    rows = (ctypes.c_int64 * W)()
+    for r, y in enumerate(y_regions):
+        rows[r] = _rows(f"y_regions[{r}]", y, H)
+        _check_cuda(f"y_regions[{r}]", y, torch.bfloat16)
+        ptrs[r] = _ptr(y)
+    _check_cuda("slot", slot, torch.int32)
+    _check_cuda("rank_offset", rank_offset, torch.int32)
+    _check_cuda("out", out, torch.bfloat16)
+    _check_cuda("status", status, torch.int32, optional=True)
+    rc = load_library().ep_combine_regions(ptrs, rows, _ptr(slot), _ptr(rank_offset), T, H, W,
+                                           _ptr(out), _ptr(status), _stream(stream))
+    _raise("ep_combine_regions", rc)

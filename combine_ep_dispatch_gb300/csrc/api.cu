@@ -2,7 +2,7 @@
 // Nothing here allocates, synchronises or keeps per-call state.
 #include <stdint.h>
 
-#include "ep_device.cuh"
+#include "dispatch_common.cuh"
 
 namespace ep {
 
@@ -186,6 +186,60 @@ int ep_combine(const void* y, const int32_t* slot, int64_t T, int H, int W, int6
     return EP_ERR_MISALIGNED;
   return from_cuda(ep::launch_combine(y, slot, T, H, W, capacity_rows, out, status,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ep_dispatch_regions(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T,
+                        int H, int k, int W, const int32_t* slot, const int32_t* rank_offset,
+                        const ep_rank_region_t* regions, int quant, int32_t* status,
+                        ep_stream_t stream) {
+  if (W < 1 || W > 32 || !regions || !rank_offset) return EP_ERR_INVALID_ARG;
+  const bool fp8 = quant == EP_QUANT_FP8_E4M3_B128;
+  ep::RankRegions rt{};
+  for (int r = 0; r < W; ++r) {
+    const ep_rank_region_t& g = regions[r];
+    if (g.rows < 0 || g.rows > kMaxRows) return EP_ERR_INVALID_ARG;
+    if (g.rows > 0 && (!g.recv_x || (fp8 && !g.recv_scale))) return EP_ERR_INVALID_ARG;
+    if (!aligned(g.recv_x, 16) || !aligned(g.recv_scale, 4) || !aligned(g.recv_topk_idx, 4) ||
+        !aligned(g.recv_topk_w, 4) || !aligned(g.recv_src, 4))
+      return EP_ERR_MISALIGNED;
+    rt.x[r] = static_cast<uint8_t*>(g.recv_x);
+    rt.scale[r] = g.recv_scale;
+    rt.topk_idx[r] = g.recv_topk_idx;
+    rt.topk_w[r] = g.recv_topk_w;
+    rt.src[r] = g.recv_src;
+    rt.rows[r] = g.rows;
+  }
+  rt.rank_offset = rank_offset;
+  // the common checks of a dispatch (no single receive buffer: capacity 0)
+  const int rc = check_dispatch(x, topk_idx, topk_w, T, H, k, W, slot, 0, quant, nullptr, nullptr,
+                                nullptr, nullptr, nullptr, status);
+  if (rc != EP_OK) return rc;
+  if (!aligned(rank_offset, 4)) return EP_ERR_MISALIGNED;
+  return from_cuda(ep::launch_dispatch_regions(x, topk_idx, topk_w, T, H, k, W, slot, quant, rt,
+                                               status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ep_combine_regions(const void* const* y_regions, const int64_t* y_rows, const int32_t* slot,
+                       const int32_t* rank_offset, int64_t T, int H, int W, void* out,
+                       int32_t* status, ep_stream_t stream) {
+  if (T < 0 || H < 1 || W < 1 || W > 32 || !y_regions || !y_rows || !rank_offset)
+    return EP_ERR_INVALID_ARG;
+  if (H % 8 != 0) return EP_ERR_UNSUPPORTED;
+  if (T > kMaxRows / W) return EP_ERR_UNSUPPORTED;
+  if (T > 0 && (!slot || !out)) return EP_ERR_INVALID_ARG;
+  ep::RankRegions rt{};
+  for (int r = 0; r < W; ++r) {
+    if (y_rows[r] < 0 || y_rows[r] > kMaxRows) return EP_ERR_INVALID_ARG;
+    if (y_rows[r] > 0 && !y_regions[r]) return EP_ERR_INVALID_ARG;
+    if (!aligned(y_regions[r], 16)) return EP_ERR_MISALIGNED;
+    rt.x[r] = static_cast<uint8_t*>(const_cast<void*>(y_regions[r]));
+    rt.rows[r] = y_rows[r];
+  }
+  rt.rank_offset = rank_offset;
+  if (!aligned(out, 16) || !aligned(slot, 4) || !aligned(rank_offset, 4) || !aligned(status, 4))
+    return EP_ERR_MISALIGNED;
+  return from_cuda(ep::launch_combine_regions(rt, slot, T, H, W, out, status,
+                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t ep_layout_experts_workspace_bytes(int64_t T, int k, int E) {

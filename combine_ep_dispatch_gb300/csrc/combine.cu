@@ -1,6 +1,6 @@
 // Combine: one warp per token gathers the token's receive rows and sums them in
 // fp32 in ascending rank order from +0, then rounds once to bf16.
-#include "ep_device.cuh"
+#include "dispatch_common.cuh"
 
 namespace ep {
 namespace {
@@ -48,12 +48,14 @@ __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float wt, const uint
 // each row enters as a fused multiply-add with the weight of its column,
 // w[t][c] ("perf(ep): optimize IntraNode dispatch kernel for MI350X",
 // Remaining gap: combine accumulates the rows with FMA).
-template <int U, bool WEIGHTED, bool SEG>
+template <int U, bool WEIGHTED, bool SEG, class RT>
 __global__ void __launch_bounds__(kCThreads)
     combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ slot,
                    const float* __restrict__ w, int64_t T, int n16, int S, int seg16, int W,
-                   int64_t cap, uint4* __restrict__ out, int32_t* __restrict__ status) {
+                   int64_t cap, uint4* __restrict__ out, int32_t* __restrict__ status, RT rt) {
   pdl_wait();
+  __shared__ typename RT::View s_rv;  // per-rank regions of y: the table (with its first rows)
+  load_region_view(rt, W, s_rv);
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = ((int64_t)blockIdx.x * kCThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kCThreads) >> 5;
@@ -69,12 +71,17 @@ __global__ void __launch_bounds__(kCThreads)
     const int64_t un2 = un + nwarps;
     s_next = (un2 < units && lane < W) ? __ldg(slot + (SEG ? un2 / S : un2) * W + lane) : -1;
 
-    const bool keep = s >= 0 && (int64_t)s < cap;
-    cap_err |= __any_sync(kFull, s >= 0 && (int64_t)s >= cap);
+    int64_t srow = s, lim = cap;  // the row in its storage and that storage's capacity
+    if (RT::kRegions && s >= 0) {
+      srow = storage_row<RT>(s, lane, s_rv);
+      lim = storage_rows<RT>(lane, cap, s_rv);
+    }
+    const bool keep = s >= 0 && srow < lim;
+    cap_err |= __any_sync(kFull, s >= 0 && srow >= lim);
     const unsigned dmask = __ballot_sync(kFull, keep);
     const int nd = __popc(dmask);
     const int r = nth_set_bit_of_lane(dmask, lane);
-    const int my_row = __shfl_sync(kFull, s, r & 31);  // lane i: row of i-th destination
+    const int my_row = __shfl_sync(kFull, (int)srow, r & 31);  // lane i: row of i-th destination
     float my_w = 0.0f;
     if constexpr (WEIGHTED) {
       const float wl = lane < W ? __ldg(w + t * W + lane) : 0.0f;
@@ -90,10 +97,15 @@ __global__ void __launch_bounds__(kCThreads)
       for (int dg = 0; dg < nd; dg += 8) {
         int rows[8];
         float wts[8];
+        const uint4* ybase[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           rows[q] = __shfl_sync(kFull, my_row, (dg + q) & 31);
           wts[q] = WEIGHTED ? __shfl_sync(kFull, my_w, (dg + q) & 31) : 1.0f;
+          if constexpr (RT::kRegions)
+            ybase[q] = reinterpret_cast<const uint4*>(s_rv.x[__shfl_sync(kFull, r, (dg + q) & 31) & 31]);
+          else
+            ybase[q] = y;
         }
         uint4 v[8][U];
 #pragma unroll
@@ -102,7 +114,8 @@ __global__ void __launch_bounds__(kCThreads)
           for (int u = 0; u < U; ++u) {
             const int c = c0 + u * 32 + lane;
             v[q][u] = make_uint4(0u, 0u, 0u, 0u);
-            if (dg + q < nd && c < c_hi) v[q][u] = ld_stream_v4(y + (int64_t)rows[q] * n16 + c);
+            if (dg + q < nd && c < c_hi)
+              v[q][u] = ld_stream_v4(ybase[q] + (int64_t)rows[q] * n16 + c);
           }
         }
 #pragma unroll
@@ -299,10 +312,10 @@ __global__ void __launch_bounds__((kCWarps + 1) * 32, 1)
 
 // One warp per token, as many CTAs as fit on the device at once (grid-stride
 // over the tokens beyond that).
-template <typename K1, typename KS>
+template <typename K1, typename KS, class RT>
 cudaError_t launch_combine_regs(K1 kern_rows, KS kern_seg, const void* y, const int32_t* slot,
                                 const float* w, int64_t T, int H, int W, int64_t capacity_rows,
-                                void* out, int32_t* status, cudaStream_t stream) {
+                                void* out, int32_t* status, cudaStream_t stream, const RT& rt) {
   static int cache[128];
   const int per_sm = occupancy_cached(kern_seg, kCThreads, cache);
   const int64_t most = (int64_t)device_sm_count() * per_sm;
@@ -325,7 +338,7 @@ cudaError_t launch_combine_regs(K1 kern_rows, KS kern_seg, const void* y, const 
   const int grid = (int)(want < most ? want : most);
   return launch_pdl(S > 1 ? kern_seg : kern_rows, dim3(grid < 1 ? 1 : grid), dim3(kCThreads), 0,
                     stream, static_cast<const uint4*>(y), slot, w, T, n16, (int)S, seg16, W,
-                    capacity_rows, static_cast<uint4*>(out), status);
+                    capacity_rows, static_cast<uint4*>(out), status, rt);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H, int W,
@@ -353,18 +366,26 @@ cudaError_t launch_combine(const void* y, const int32_t* slot, int64_t T, int H,
                       smem, stream, static_cast<const uint8_t*>(y), slot, T, row_bytes, chunk, W,
                       capacity_rows, static_cast<uint8_t*>(out), status);
   }
-  return launch_combine_regs(combine_kernel<kCU, false, false>,
-                             combine_kernel<kCU, false, true>, y, slot, nullptr, T, H, W,
-                             capacity_rows, out, status, stream);
+  return launch_combine_regs(combine_kernel<kCU, false, false, OneBuffer>,
+                             combine_kernel<kCU, false, true, OneBuffer>, y, slot, nullptr, T, H, W,
+                             capacity_rows, out, status, stream, OneBuffer{});
+}
+
+cudaError_t launch_combine_regions(const RankRegions& y_regions, const int32_t* slot, int64_t T,
+                                   int H, int W, void* out, int32_t* status, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  return launch_combine_regs(combine_kernel<kCU, false, false, RankRegions>,
+                             combine_kernel<kCU, false, true, RankRegions>, nullptr, slot, nullptr,
+                             T, H, W, /*capacity_rows=*/0, out, status, stream, y_regions);
 }
 
 cudaError_t launch_combine_weighted(const void* y, const int32_t* slot, const float* w, int64_t T,
                                     int H, int C, int64_t capacity_rows, void* out,
                                     int32_t* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  return launch_combine_regs(combine_kernel<kCU, true, false>,
-                             combine_kernel<kCU, true, true>, y, slot, w, T, H, C,
-                             capacity_rows, out, status, stream);
+  return launch_combine_regs(combine_kernel<kCU, true, false, OneBuffer>,
+                             combine_kernel<kCU, true, true, OneBuffer>, y, slot, w, T, H, C,
+                             capacity_rows, out, status, stream, OneBuffer{});
 }
 
 }  // namespace ep

@@ -13,22 +13,25 @@ constexpr int kDThreads = 256;
 // bf16 payload: lane l moves 16-byte chunks l, l+32, ... of the row; U chunks
 // are loaded before the stores of a round so that each lane keeps U loads in
 // flight.  The row is read once whatever the number of destinations.
-template <int U>
+template <int U, class RT>
 __global__ void __launch_bounds__(kDThreads)
     dispatch_bf16_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ topk_idx,
                          const float* __restrict__ topk_w, int64_t T, int n16, int k, int W,
                          const int32_t* __restrict__ slot, int64_t cap, uint4* __restrict__ recv_x,
                          int32_t* __restrict__ recv_topk_idx, float* __restrict__ recv_topk_w,
-                         int32_t* __restrict__ recv_src, int32_t* __restrict__ status) {
+                         int32_t* __restrict__ recv_src, int32_t* __restrict__ status, RT rt) {
   pdl_wait();
+  __shared__ typename RT::View s_rv;
+  load_region_view(rt, W, s_rv);
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = ((int64_t)blockIdx.x * kDThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kDThreads) >> 5;
   bool cap_err = false;
   for (int64_t t = gwarp; t < T; t += nwarps) {
-    const Dests d = token_dests(slot, t, W, cap, lane);
+    const Dests d = token_dests<RT>(slot, t, W, cap, lane, &s_rv);
     cap_err |= d.cap_err;
-    carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
+    carry_metadata<RT>(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane,
+                       &s_rv);
     const uint4* src = x + t * n16;
     for (int c0 = 0; c0 < n16; c0 += 32 * U) {
       uint4 v[U];
@@ -38,13 +41,18 @@ __global__ void __launch_bounds__(kDThreads)
         if (c < n16) v[u] = ld_stream_v4(src + c);
       }
       for (int dg = 0; dg < d.nd; dg += 8) {
-        int rows[8];
+        int rows[8], ranks[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) rows[q] = __shfl_sync(kFull, d.my_row, (dg + q) & 31);
+        for (int q = 0; q < 8; ++q) {
+          rows[q] = __shfl_sync(kFull, d.my_row, (dg + q) & 31);
+          ranks[q] = RT::kRegions ? __shfl_sync(kFull, d.my_rank, (dg + q) & 31) : 0;
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           if (dg + q < d.nd) {
-            uint4* dst = recv_x + (int64_t)rows[q] * n16;
+            uint4* const base = reinterpret_cast<uint4*>(
+                rows_base<RT>(s_rv, ranks[q] & 31, reinterpret_cast<uint8_t*>(recv_x)));
+            uint4* dst = base + (int64_t)rows[q] * n16;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
               const int c = c0 + u * 32 + lane;
@@ -88,6 +96,7 @@ __device__ __forceinline__ int load_slot(const int32_t* slot, int64_t t, int W, 
   return (t < T && lane < W) ? slot[t * W + lane] : -1;
 }
 
+template <class RT>
 __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
     dispatch_bf16_tma_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
                              const float* __restrict__ topk_w, int64_t T, uint32_t row_bytes,
@@ -95,7 +104,7 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
                              int64_t cap, uint8_t* __restrict__ recv_x,
                              int32_t* __restrict__ recv_topk_idx, float* __restrict__ recv_topk_w,
                              int32_t* __restrict__ recv_src, int32_t* __restrict__ status,
-                             int x_early, Finalize fin) {
+                             int x_early, Finalize fin, RT rt) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta_warps = blockDim.x >> 5;
@@ -127,6 +136,8 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
   if (x_early) first_loads(kTmaStages);
   pdl_wait();
   first_loads(kTmaStages);
+  __shared__ typename RT::View s_rv;  // per-rank regions: the table (with its first rows)
+  load_region_view(rt, W, s_rv);
 
   const bool fin_mode = fin.chunk_rank != nullptr;  // uniform over the grid
   __shared__ int32_t s_tot[32], s_off[33];
@@ -161,12 +172,17 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
         mv = (int32_t)t;
     }
     const int s_next = load_slot(slot, t + NW, W, lane, T);
-    const bool keep = s_cur >= 0 && (int64_t)s_cur < cap;
-    cap_err |= __any_sync(kFull, s_cur >= 0 && (int64_t)s_cur >= cap);
+    int64_t srow = s_cur, lim = cap;  // the row in its storage and that storage's capacity
+    if (RT::kRegions && s_cur >= 0) {
+      srow = storage_row<RT>(s_cur, lane, s_rv);
+      lim = storage_rows<RT>(lane, cap, s_rv);
+    }
+    const bool keep = s_cur >= 0 && srow < lim;
+    cap_err |= __any_sync(kFull, s_cur >= 0 && srow >= lim);
     const unsigned dmask = __ballot_sync(kFull, keep);
     const int nd = __popc(dmask);
     const int r = nth_set_bit_of_lane(dmask, lane);
-    const int my_row = __shfl_sync(kFull, s_cur, r & 31);
+    const int my_row = __shfl_sync(kFull, (int)srow, r & 31);
 
     // every lane observes the row's arrival, lane q sends it to destination q
     const bool ok = mbar_wait_bounded(&full[st], parity);
@@ -174,27 +190,40 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
       timed_out = true;
       break;
     }
-    if (lane < nd)
-      bulk_store_hint(recv_x + (int64_t)my_row * row_bytes, buf + st * stage_bytes, row_bytes,
+    if (lane < nd) {
+      uint8_t* const base = rows_base<RT>(s_rv, r, recv_x);
+      bulk_store_hint(base + (int64_t)my_row * row_bytes, buf + st * stage_bytes, row_bytes,
                       make_l2_policy<kL2EvictLast>());
+    }
     bulk_commit();
     if (meta_lanes) {
       for (int q = 0; q < nd; ++q) {
         const int64_t row = __shfl_sync(kFull, my_row, q);
+        int32_t* ridx = recv_topk_idx;
+        float* rw = recv_topk_w;
+        int32_t* rsrc = recv_src;
+        if constexpr (RT::kRegions) {
+          const int rq = __shfl_sync(kFull, r, q);
+          ridx = s_rv.topk_idx[rq];
+          rw = s_rv.topk_w[rq];
+          rsrc = s_rv.src[rq];
+        }
         if (lane < k) {
-          if (recv_topk_idx) recv_topk_idx[row * k + lane] = mv;
+          if (ridx) ridx[row * k + lane] = mv;
         } else if (lane < 2 * k) {
-          if (recv_topk_w) recv_topk_w[row * k + (lane - k)] = __int_as_float(mv);
+          if (rw) rw[row * k + (lane - k)] = __int_as_float(mv);
         } else if (lane == 2 * k) {
-          if (recv_src) recv_src[row] = mv;
+          if (rsrc) rsrc[row] = mv;
         }
       }
     } else {
       Dests d;
       d.nd = nd;
       d.my_row = r >= 0 ? my_row : -1;
+      d.my_rank = r;
       d.cap_err = false;
-      carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
+      carry_metadata<RT>(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane,
+                         &s_rv);
     }
     // refill the previous token's buffer once the copies out of it (issued by
     // several lanes) have read it
@@ -228,12 +257,21 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
 
 }  // namespace
 
+template <class RT>
 cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const float* topk_w,
                                 int64_t T, int H, int k, int W, const int32_t* slot,
                                 int64_t capacity_rows, void* recv_x, float* recv_scale,
                                 int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
                                 int32_t* status, cudaStream_t stream, int x_early,
-                                const Finalize& fin);
+                                const Finalize& fin, const RT& rt);
+extern template cudaError_t launch_dispatch_fp8<OneBuffer>(
+    const void*, const int32_t*, const float*, int64_t, int, int, int, const int32_t*, int64_t,
+    void*, float*, int32_t*, float*, int32_t*, int32_t*, cudaStream_t, int, const Finalize&,
+    const OneBuffer&);
+extern template cudaError_t launch_dispatch_fp8<RankRegions>(
+    const void*, const int32_t*, const float*, int64_t, int, int, int, const int32_t*, int64_t,
+    void*, float*, int32_t*, float*, int32_t*, int32_t*, cudaStream_t, int, const Finalize&,
+    const RankRegions&);
 
 namespace {
 
@@ -251,18 +289,19 @@ bool tma_shape(int H, TmaShape* sh) {
   return sh->row_bytes >= kTmaMinRowBytes && fit >= 1;
 }
 
+template <class RT>
 cudaError_t launch_tma(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T,
                        int k, int W, int32_t* slot, int64_t capacity_rows, void* recv_x,
                        int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
                        int32_t* status, cudaStream_t stream, int x_early, const TmaShape& sh,
-                       const Finalize& fin) {
+                       const Finalize& fin, const RT& rt) {
   size_t smem = kTmaBarBytes + (size_t)sh.cta_warps * kTmaStages * sh.stage_bytes;
   if (fin.chunk_rank != nullptr) smem += ((size_t)(fin.C * W) * sizeof(int32_t) + 15) & ~size_t(15);
   static bool attr_set[128];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(dispatch_bf16_tma_kernel,
+    cudaError_t e = cudaFuncSetAttribute(dispatch_bf16_tma_kernel<RT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kTmaBarBytes + kTmaSmemBudget + kFinMaxBytes);
     if (e != cudaSuccess) return e;
@@ -271,11 +310,48 @@ cudaError_t launch_tma(const void* x, const int32_t* topk_idx, const float* topk
   const int64_t want = (T + sh.cta_warps - 1) / sh.cta_warps;
   const int64_t sms = (int64_t)device_sm_count() * kTmaCtasPerSm;
   const int grid = (int)(want < sms ? want : sms);
-  return launch_pdl(dispatch_bf16_tma_kernel, dim3(grid < 1 ? 1 : grid), dim3(sh.cta_warps * 32),
-                    smem, stream, static_cast<const uint8_t*>(x), topk_idx, topk_w, T,
-                    sh.row_bytes, sh.stage_bytes, k, W, slot, capacity_rows,
+  return launch_pdl(dispatch_bf16_tma_kernel<RT>, dim3(grid < 1 ? 1 : grid),
+                    dim3(sh.cta_warps * 32), smem, stream, static_cast<const uint8_t*>(x), topk_idx,
+                    topk_w, T, sh.row_bytes, sh.stage_bytes, k, W, slot, capacity_rows,
                     static_cast<uint8_t*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status,
-                    x_early, fin);
+                    x_early, fin, rt);
+}
+
+// The dispatch of a final slot table into receive storage RT (one buffer, or
+// per-rank regions).
+template <class RT>
+cudaError_t launch_dispatch_rt(const void* x, const int32_t* topk_idx, const float* topk_w,
+                               int64_t T, int H, int k, int W, const int32_t* slot,
+                               int64_t capacity_rows, int quant, void* recv_x, float* recv_scale,
+                               int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
+                               int32_t* status, cudaStream_t stream, int x_early, const RT& rt) {
+  if (T == 0) return cudaSuccess;
+  const uint4* x4 = static_cast<const uint4*>(x);
+  Finalize none{};
+  if (quant == EP_QUANT_BF16) {
+    TmaShape sh;
+    if (tma_shape(H, &sh)) {
+      // the kernel writes the slot table only with a Finalize
+      return launch_tma(x, topk_idx, topk_w, T, k, W, const_cast<int32_t*>(slot), capacity_rows,
+                        recv_x, recv_topk_idx, recv_topk_w, recv_src, status, stream, x_early,
+                        sh, none, rt);
+    }
+    const int n16 = H / 8;
+    if (n16 % (32 * 7) == 0) {
+      auto kern = dispatch_bf16_kernel<7, RT>;
+      return launch_pdl(kern, dim3(grid_for(kern, T, kDThreads)), dim3(kDThreads), 0, stream, x4,
+                        topk_idx, topk_w, T, n16, k, W, slot, capacity_rows,
+                        static_cast<uint4*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status,
+                        rt);
+    }
+    auto kern = dispatch_bf16_kernel<8, RT>;
+    return launch_pdl(kern, dim3(grid_for(kern, T, kDThreads)), dim3(kDThreads), 0, stream, x4,
+                      topk_idx, topk_w, T, n16, k, W, slot, capacity_rows,
+                      static_cast<uint4*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status, rt);
+  }
+  return launch_dispatch_fp8<RT>(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, recv_x,
+                                 recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream,
+                                 x_early, none, rt);
 }
 
 }  // namespace
@@ -285,33 +361,18 @@ cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float*
                             int64_t capacity_rows, int quant, void* recv_x, float* recv_scale,
                             int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
                             int32_t* status, cudaStream_t stream, int x_early) {
-  if (T == 0) return cudaSuccess;
-  const uint4* x4 = static_cast<const uint4*>(x);
-  if (quant == EP_QUANT_BF16) {
-    TmaShape sh;
-    if (tma_shape(H, &sh)) {
-      Finalize none{};
-      // the kernel writes the slot table only with a Finalize
-      return launch_tma(x, topk_idx, topk_w, T, k, W, const_cast<int32_t*>(slot), capacity_rows,
-                        recv_x, recv_topk_idx, recv_topk_w, recv_src, status, stream, x_early,
-                        sh, none);
-    }
-    const int n16 = H / 8;
-    if (n16 % (32 * 7) == 0) {
-      auto kern = dispatch_bf16_kernel<7>;
-      return launch_pdl(kern, dim3(grid_for(kern, T, kDThreads)), dim3(kDThreads), 0, stream, x4,
-                        topk_idx, topk_w, T, n16, k, W, slot, capacity_rows,
-                        static_cast<uint4*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status);
-    }
-    auto kern = dispatch_bf16_kernel<8>;
-    return launch_pdl(kern, dim3(grid_for(kern, T, kDThreads)), dim3(kDThreads), 0, stream, x4,
-                      topk_idx, topk_w, T, n16, k, W, slot, capacity_rows,
-                      static_cast<uint4*>(recv_x), recv_topk_idx, recv_topk_w, recv_src, status);
-  }
-  Finalize none{};
-  return launch_dispatch_fp8(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, recv_x,
+  return launch_dispatch_rt(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, quant, recv_x,
                             recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream,
-                            x_early, none);
+                            x_early, OneBuffer{});
+}
+
+cudaError_t launch_dispatch_regions(const void* x, const int32_t* topk_idx, const float* topk_w,
+                                    int64_t T, int H, int k, int W, const int32_t* slot,
+                                    int quant, const RankRegions& regions, int32_t* status,
+                                    cudaStream_t stream) {
+  return launch_dispatch_rt(x, topk_idx, topk_w, T, H, k, W, slot, /*capacity_rows=*/0, quant,
+                            nullptr, nullptr, nullptr, nullptr, nullptr, status, stream,
+                            /*x_early=*/0, regions);
 }
 
 namespace {
@@ -365,9 +426,9 @@ cudaError_t launch_dispatch_with_layout(const void* x, const int32_t* topk_idx, 
     if (quant == EP_QUANT_FP8_E4M3_B128)
       return launch_dispatch_fp8(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, recv_x,
                                  recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream,
-                                 /*x_early=*/1, fin);
+                                 /*x_early=*/1, fin, OneBuffer{});
     return launch_tma(x, topk_idx, topk_w, T, k, W, slot, capacity_rows, recv_x, recv_topk_idx,
-                      recv_topk_w, recv_src, status, stream, /*x_early=*/1, sh, fin);
+                      recv_topk_w, recv_src, status, stream, /*x_early=*/1, sh, fin, OneBuffer{});
   }
   // the whole layout, then the dispatch, which loads its first rows of x while
   // the layout kernels run

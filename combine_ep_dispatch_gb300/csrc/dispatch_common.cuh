@@ -5,28 +5,122 @@
 
 namespace ep {
 
+// Where the receive rows live.  OneBuffer: one allocation for all ranks, rank
+// r's rows are the global rows [rank_offset[r], rank_offset[r+1]) of it (the
+// layout's slot is the row).  RankRegions: one allocation per rank
+// (ep_dispatch_regions, ep_combine_regions), passed as a table of base
+// pointers: the row of (t, r) is slot[t][r] - rank_offset[r] of rank r's
+// region, and each region has its own capacity.  Kernels copy the table and
+// the regions' first global rows into shared memory (RegionView) after their
+// dependency wait, since rank_offset comes from the layout.
+struct OneBuffer {
+  static constexpr bool kRegions = false;
+  struct View {
+    int32_t unused;
+  };
+};
+
+struct RankRegions {
+  static constexpr bool kRegions = true;
+  uint8_t* x[kMaxRanks];          // rank r's receive rows (bf16 rows or e4m3 codes)
+  float* scale[kMaxRanks];        // FP8 block scales of those rows, or null
+  int32_t* topk_idx[kMaxRanks];   // metadata of those rows, each may be null
+  float* topk_w[kMaxRanks];
+  int32_t* src[kMaxRanks];
+  int64_t rows[kMaxRanks];        // capacity of each region
+  const int32_t* rank_offset;     // [W + 1] from the layout (device memory)
+  struct View {
+    uint8_t* x[kMaxRanks];
+    float* scale[kMaxRanks];
+    int32_t* topk_idx[kMaxRanks];
+    float* topk_w[kMaxRanks];
+    int32_t* src[kMaxRanks];
+    int64_t rows[kMaxRanks];
+    int32_t off[kMaxRanks + 1];
+  };
+};
+
+// Fills the shared view of a region table; every thread of the CTA calls it,
+// after the kernel's dependency wait.
+template <class RT>
+__device__ __forceinline__ void load_region_view(const RT& rt, int W, typename RT::View& v) {
+  if constexpr (RT::kRegions) {
+    for (int r = threadIdx.x; r <= W; r += blockDim.x) {
+      v.off[r] = rt.rank_offset[r];
+      if (r < W) {
+        v.x[r] = rt.x[r];
+        v.scale[r] = rt.scale[r];
+        v.topk_idx[r] = rt.topk_idx[r];
+        v.topk_w[r] = rt.topk_w[r];
+        v.src[r] = rt.src[r];
+        v.rows[r] = rt.rows[r];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Row of the slot entry s (>= 0) of rank r inside r's storage, and that
+// storage's capacity: the global row and `cap` for one buffer, the row inside
+// the region and the region's capacity for per-rank regions.
+template <class RT>
+__device__ __forceinline__ int64_t storage_row(int s, int r, const typename RT::View& v) {
+  if constexpr (RT::kRegions)
+    return (int64_t)s - v.off[r];
+  else
+    return s;
+}
+template <class RT>
+__device__ __forceinline__ int64_t storage_rows(int r, int64_t cap, const typename RT::View& v) {
+  if constexpr (RT::kRegions)
+    return v.rows[r];
+  else
+    return cap;
+}
+
+// Base of rank r's receive rows: the one buffer, or rank r's region.
+template <class RT>
+__device__ __forceinline__ uint8_t* rows_base(const typename RT::View& v, int r, uint8_t* one) {
+  if constexpr (RT::kRegions)
+    return v.x[r];
+  else
+    return one;
+}
+
 // Destinations of token t in ascending rank order: lane i < nd holds the i-th
-// destination's receive row.  Rows at or beyond the capacity are dropped and
-// reported.  (The cached (token, rank) -> row map of "perf(ep): optimize
-// IntraNode dispatch kernel for MI350X", Technical Details 1, is `slot`.)
+// destination's row (in its storage, see storage_row) and rank.  Rows at or
+// beyond their storage's capacity are dropped and reported.  (The cached
+// (token, rank) -> row map of "perf(ep): optimize IntraNode dispatch kernel
+// for MI350X", Technical Details 1, is `slot`.)
 struct Dests {
   int nd;
   int my_row;
+  int my_rank;
   bool cap_err;
 };
 
+template <class RT = OneBuffer>
 __device__ __forceinline__ Dests token_dests(const int32_t* __restrict__ slot, int64_t t, int W,
-                                             int64_t cap, int lane) {
+                                             int64_t cap, int lane,
+                                             const typename RT::View* v = nullptr) {
   int s = -1;
   if (lane < W) s = __ldg(slot + t * W + lane);
-  const bool keep = s >= 0 && (int64_t)s < cap;
-  const bool over = s >= 0 && (int64_t)s >= cap;
+  int64_t row = s, lim = cap;
+  if constexpr (RT::kRegions) {
+    if (s >= 0) {
+      row = storage_row<RT>(s, lane, *v);
+      lim = storage_rows<RT>(lane, cap, *v);
+    }
+  }
+  const bool keep = s >= 0 && row < lim;
+  const bool over = s >= 0 && row >= lim;
   const unsigned dmask = __ballot_sync(kFull, keep);
   const int r = nth_set_bit_of_lane(dmask, lane);
-  const int row = __shfl_sync(kFull, s, r & 31);
+  const int rr = __shfl_sync(kFull, (int)row, r & 31);
   Dests d;
   d.nd = __popc(dmask);
-  d.my_row = r >= 0 ? row : -1;
+  d.my_row = r >= 0 ? rr : -1;
+  d.my_rank = r;
   d.cap_err = __any_sync(kFull, over);
   return d;
 }
@@ -42,36 +136,50 @@ __device__ __forceinline__ void st_b32(void* p, uint32_t v) {
 // Details 4).  Lane j takes word j of the token (id j, weight j - k, or the
 // source index at j = 2k), reads it once, and stores it to every destination
 // row with one multiply-add for the address: no division, no per-destination
-// reloads.
+// reloads.  With per-rank regions the destination's rank picks the array.
+template <class RT = OneBuffer>
 __device__ __forceinline__ void carry_metadata(const int32_t* __restrict__ topk_idx,
                                                const float* __restrict__ topk_w, int64_t t, int k,
                                                const Dests& d, int32_t* __restrict__ recv_topk_idx,
                                                float* __restrict__ recv_topk_w,
-                                               int32_t* __restrict__ recv_src, int lane) {
+                                               int32_t* __restrict__ recv_src, int lane,
+                                               const typename RT::View* v = nullptr) {
   const int per = 2 * k + 1;
   for (int w0 = 0; w0 < per; w0 += 32) {
     const int j = w0 + lane;
+    int kind = -1;  // 0: id, 1: weight, 2: source index
     uint32_t* col = nullptr;  // the word's address in receive row 0
     uint32_t stride = 1, val = 0;
     if (j < k) {
-      if (recv_topk_idx != nullptr) {
-        col = reinterpret_cast<uint32_t*>(recv_topk_idx) + j;
-        stride = (uint32_t)k;
-        val = (uint32_t)__ldg(topk_idx + t * k + j);
-      }
+      kind = 0;
+      stride = (uint32_t)k;
+      val = (uint32_t)__ldg(topk_idx + t * k + j);
+      if (recv_topk_idx != nullptr) col = reinterpret_cast<uint32_t*>(recv_topk_idx) + j;
     } else if (j < 2 * k) {
-      if (recv_topk_w != nullptr) {
-        col = reinterpret_cast<uint32_t*>(recv_topk_w) + (j - k);
-        stride = (uint32_t)k;
-        val = __float_as_uint(__ldg(topk_w + t * k + (j - k)));
-      }
-    } else if (j == 2 * k && recv_src != nullptr) {
-      col = reinterpret_cast<uint32_t*>(recv_src);
+      kind = 1;
+      stride = (uint32_t)k;
+      val = __float_as_uint(__ldg(topk_w + t * k + (j - k)));
+      if (recv_topk_w != nullptr) col = reinterpret_cast<uint32_t*>(recv_topk_w) + (j - k);
+    } else if (j == 2 * k) {
+      kind = 2;
       val = (uint32_t)t;
+      if (recv_src != nullptr) col = reinterpret_cast<uint32_t*>(recv_src);
     }
     for (int qq = 0; qq < d.nd; ++qq) {
       const uint32_t row = (uint32_t)__shfl_sync(kFull, d.my_row, qq);
-      if (col != nullptr) st_b32(col + (uint64_t)row * stride, val);
+      if constexpr (RT::kRegions) {
+        const int r = __shfl_sync(kFull, d.my_rank, qq);
+        uint32_t* base = nullptr;
+        if (kind == 0 && v->topk_idx[r] != nullptr)
+          base = reinterpret_cast<uint32_t*>(v->topk_idx[r]) + j;
+        else if (kind == 1 && v->topk_w[r] != nullptr)
+          base = reinterpret_cast<uint32_t*>(v->topk_w[r]) + (j - k);
+        else if (kind == 2 && v->src[r] != nullptr)
+          base = reinterpret_cast<uint32_t*>(v->src[r]);
+        if (base != nullptr) st_b32(base + (uint64_t)row * stride, val);
+      } else {
+        if (col != nullptr) st_b32(col + (uint64_t)row * stride, val);
+      }
     }
   }
 }
@@ -157,6 +265,15 @@ __device__ __forceinline__ void finish_expert_totals(const Finalize& fin) {
     if (lane == 0) fin.num_tokens_per_expert[e] = sum;
   }
 }
+
+// ep_dispatch_regions / ep_combine_regions: the dispatch of a final slot
+// table into per-rank regions, and the combine that reads them.
+cudaError_t launch_dispatch_regions(const void* x, const int32_t* topk_idx, const float* topk_w,
+                                    int64_t T, int H, int k, int W, const int32_t* slot,
+                                    int quant, const RankRegions& regions, int32_t* status,
+                                    cudaStream_t stream);
+cudaError_t launch_combine_regions(const RankRegions& y_regions, const int32_t* slot, int64_t T,
+                                   int H, int W, void* out, int32_t* status, cudaStream_t stream);
 
 template <typename K>
 inline int grid_for(K kernel, int64_t T, int threads) {

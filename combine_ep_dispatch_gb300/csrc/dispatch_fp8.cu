@@ -111,7 +111,7 @@ __device__ __forceinline__ void block_scale(float m, const float* s_q7, const fl
 // split into `nseg` segments of block quadruples, one warp per (token,
 // segment), so that small batches still fill the GPU; each segment is
 // quantised once and its codes and scales are stored to every destination.
-template <int U>
+template <int U, class RT>
 __global__ void __launch_bounds__(kDThreads, kFp8MinB)
     dispatch_fp8_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ topk_idx,
                         const float* __restrict__ topk_w, int64_t T, int H, int k, int W,
@@ -119,9 +119,12 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
                         float* __restrict__ recv_scale, int32_t* __restrict__ recv_topk_idx,
                         float* __restrict__ recv_topk_w, int32_t* __restrict__ recv_src,
                         int nseg, int per_seg, int32_t* __restrict__ status, int x_early,
-                        Finalize fin) {
+                        Finalize fin, RT rt) {
   __shared__ float s_q7[128], s_r7[128];
   __shared__ int32_t s_dst[kDThreads / 32][32];  // per warp: rows of the unit's destinations
+  // per warp: ranks of the unit's destinations (per-rank regions only)
+  __shared__ int32_t s_drank[RT::kRegions ? kDThreads / 32 : 1][32];
+  __shared__ typename RT::View s_rv;
   if (threadIdx.x < 128) {
     const float q = __fdiv_rn((float)(128 + threadIdx.x), 7.0f);
     s_q7[threadIdx.x] = q;
@@ -130,6 +133,7 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
   __syncthreads();
   const int lane = threadIdx.x & 31;
   int32_t* const my_dst = s_dst[threadIdx.x >> 5];
+  int32_t* const my_drank = s_drank[RT::kRegions ? threadIdx.x >> 5 : 0];
   const unsigned below = (1u << lane) - 1u;  // lanes under this one
   const int qb = lane >> 3, hl = lane & 7;  // block within the quad, lane within the block
   const int nb = H >> 7;
@@ -175,6 +179,7 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
     if (x_early) load_step(t, q0, q_end, A, C);
   }
   pdl_wait();
+  load_region_view(rt, W, s_rv);
   // With a Finalize the slot table holds in-chunk positions: every CTA scans
   // the chunk counts first; the warp taking a token's first segment writes
   // its receive rows back (other segments may read either form).
@@ -192,6 +197,7 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
   d.nd = 0;
   d.my_row = -1;
   int sc_row = -1;  // lane (qb, hl): row of destination hl, which receives block qb's scale
+  int sc_rank = 0;  // and (per-rank regions) its rank
   // Unit by unit; inside a unit, step by step.  Each step issues the loads
   // of the next one (the next unit's first step at a unit's last) before it
   // quantises and stores its own, so loads stay in flight during the
@@ -203,20 +209,31 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
         s_raw = final_slot(s_raw, t, lane, W, fin.shift, s_base, s_off);
         if (seg == 0) slot[t * W + lane] = s_raw;
       }
-      const bool keep = s_raw >= 0 && (int64_t)s_raw < cap;
-      const bool over = s_raw >= 0 && (int64_t)s_raw >= cap;
+      int64_t srow = s_raw, lim = cap;  // the row in its storage and that storage's capacity
+      if (RT::kRegions && s_raw >= 0) {
+        srow = storage_row<RT>(s_raw, lane, s_rv);
+        lim = storage_rows<RT>(lane, cap, s_rv);
+      }
+      const bool keep = s_raw >= 0 && srow < lim;
+      const bool over = s_raw >= 0 && srow >= lim;
       const unsigned dmask = __ballot_sync(kFull, keep);
       // compact the destinations: lane i gets the row of the i-th one
       __syncwarp();  // the previous unit's rows have been read
-      if (keep) my_dst[__popc(dmask & below)] = s_raw;
+      if (keep) {
+        my_dst[__popc(dmask & below)] = (int)srow;
+        if constexpr (RT::kRegions) my_drank[__popc(dmask & below)] = lane;
+      }
       __syncwarp();
       d.nd = __popc(dmask);
       d.my_row = lane < d.nd ? my_dst[lane] : -1;
+      d.my_rank = RT::kRegions && lane < d.nd ? my_drank[lane] : -1;
       d.cap_err = __any_sync(kFull, over);
       sc_row = hl < d.nd ? my_dst[hl] : -1;
+      if constexpr (RT::kRegions) sc_rank = hl < d.nd ? my_drank[hl] : 0;
       if (seg == 0) {
         cap_err |= d.cap_err;
-        carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
+        carry_metadata<RT>(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane,
+                           &s_rv);
       }
     }
     const int64_t un = u + nwarps;  // the next unit
@@ -256,16 +273,32 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
         if (q + v >= q_end) continue;  // warp-uniform
         const int b = (q + v) * 4 + qb;
         const bool has = b < nb;          // the last quadruple may be partial
-        uint8_t* const xb = recv_x + b * 128 + hl * 16;
+        if constexpr (RT::kRegions) {
 #pragma unroll 1
-        for (int qq = 0; qq < d.nd; ++qq) {
-          const uint32_t row = (uint32_t)__shfl_sync(kFull, d.my_row, qq);
-          if (has) st_v4(reinterpret_cast<uint4*>(xb + (uint64_t)row * (uint32_t)H), codes[v]);
-        }
-        if (has) {
-          if (sc_row >= 0) recv_scale[(uint64_t)(uint32_t)sc_row * (uint32_t)nb + b] = sc[v];
-          for (int j = hl + 8; j < d.nd; j += 8)
-            recv_scale[(uint64_t)(uint32_t)my_dst[j] * (uint32_t)nb + b] = sc[v];
+          for (int qq = 0; qq < d.nd; ++qq) {
+            const uint32_t row = (uint32_t)__shfl_sync(kFull, d.my_row, qq);
+            const int rk = __shfl_sync(kFull, d.my_rank, qq);
+            uint8_t* const xb = s_rv.x[rk] + b * 128 + hl * 16;
+            if (has) st_v4(reinterpret_cast<uint4*>(xb + (uint64_t)row * (uint32_t)H), codes[v]);
+          }
+          if (has) {
+            if (sc_row >= 0)
+              s_rv.scale[sc_rank][(uint64_t)(uint32_t)sc_row * (uint32_t)nb + b] = sc[v];
+            for (int j = hl + 8; j < d.nd; j += 8)
+              s_rv.scale[my_drank[j]][(uint64_t)(uint32_t)my_dst[j] * (uint32_t)nb + b] = sc[v];
+          }
+        } else {
+          uint8_t* const xb = recv_x + b * 128 + hl * 16;
+#pragma unroll 1
+          for (int qq = 0; qq < d.nd; ++qq) {
+            const uint32_t row = (uint32_t)__shfl_sync(kFull, d.my_row, qq);
+            if (has) st_v4(reinterpret_cast<uint4*>(xb + (uint64_t)row * (uint32_t)H), codes[v]);
+          }
+          if (has) {
+            if (sc_row >= 0) recv_scale[(uint64_t)(uint32_t)sc_row * (uint32_t)nb + b] = sc[v];
+            for (int j = hl + 8; j < d.nd; j += 8)
+              recv_scale[(uint64_t)(uint32_t)my_dst[j] * (uint32_t)nb + b] = sc[v];
+          }
         }
       }
 #pragma unroll
@@ -288,17 +321,18 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
 
 }  // namespace
 
+template <class RT>
 cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const float* topk_w,
                                 int64_t T, int H, int k, int W, const int32_t* slot,
                                 int64_t capacity_rows, void* recv_x, float* recv_scale,
                                 int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
                                 int32_t* status, cudaStream_t stream, int x_early,
-                                const Finalize& fin) {
+                                const Finalize& fin, const RT& rt) {
   if (T == 0) return cudaSuccess;
   const uint4* x4 = static_cast<const uint4*>(x);
   // segments per token: enough (token, segment) units to give every resident warp
   // a few, but no more segments than block quadruples
-  auto kern = dispatch_fp8_kernel<kFp8U>;
+  auto kern = dispatch_fp8_kernel<kFp8U, RT>;
   static int cache[128];
   const int per_sm = occupancy_cached(kern, kDThreads, cache);
   const int64_t warps = (int64_t)device_sm_count() * per_sm * (kDThreads / 32);
@@ -319,7 +353,16 @@ cudaError_t launch_dispatch_fp8(const void* x, const int32_t* topk_idx, const fl
   return launch_pdl(kern, dim3((unsigned)(grid < 1 ? 1 : grid)), dim3(kDThreads), smem, stream, x4,
                     topk_idx, topk_w, T, H, k, W, const_cast<int32_t*>(slot), capacity_rows,
                     static_cast<uint8_t*>(recv_x), recv_scale, recv_topk_idx, recv_topk_w, recv_src,
-                    nseg, per_seg, status, x_early, fin);
+                    nseg, per_seg, status, x_early, fin, rt);
 }
+
+template cudaError_t launch_dispatch_fp8<OneBuffer>(
+    const void*, const int32_t*, const float*, int64_t, int, int, int, const int32_t*, int64_t,
+    void*, float*, int32_t*, float*, int32_t*, int32_t*, cudaStream_t, int, const Finalize&,
+    const OneBuffer&);
+template cudaError_t launch_dispatch_fp8<RankRegions>(
+    const void*, const int32_t*, const float*, int64_t, int, int, int, const int32_t*, int64_t,
+    void*, float*, int32_t*, float*, int32_t*, int32_t*, cudaStream_t, int, const Finalize&,
+    const RankRegions&);
 
 }  // namespace ep

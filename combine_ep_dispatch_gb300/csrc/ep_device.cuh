@@ -9,6 +9,7 @@
 namespace ep {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMaxRanks = 32;  // a token's destination ranks are one 32-bit mask
 
 // ------------------------------------------------------------ dependent launch
 // Every kernel of the library is launched with programmatic stream

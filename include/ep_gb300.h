@@ -246,6 +246,67 @@ EP_API int ep_combine(const void* y, const int32_t* slot, int64_t T, int H, int 
                void* out, int32_t* status, ep_stream_t stream);
 
 /*
+ * Receive storage of one rank when the W rank regions live in separate
+ * allocations (ep_dispatch_regions, ep_combine_regions).  All pointers are
+ * device pointers owned by the caller; rows are dense and row-major.
+ */
+typedef struct ep_rank_region {
+  void* recv_x;           /* bf16 [rows, H] (EP_QUANT_BF16) or uint8 codes [rows, H] (FP8);
+                             16-byte aligned */
+  float* recv_scale;      /* fp32 [rows, H / 128] for FP8, else ignored (may be NULL) */
+  int32_t* recv_topk_idx; /* int32 [rows, k], or NULL: not written */
+  float* recv_topk_w;     /* fp32 [rows, k], or NULL: not written */
+  int32_t* recv_src;      /* int32 [rows], or NULL: not written */
+  int64_t rows;           /* capacity of this region, 0 <= rows < 2^31 */
+} ep_rank_region_t;
+
+/*
+ * Dispatch into per-rank regions: ep_dispatch with rank r's receive rows in an
+ * allocation of their own, named by a table of base pointers.  Token t's row
+ * for rank r in D(t) goes to row slot[t][r] - rank_offset[r] of region r (its
+ * position among rank r's tokens, ascending token order), with the same bits
+ * (bf16 copy, or FP8 codes and scales) and metadata that ep_dispatch writes
+ * at global row slot[t][r].  Rows at or beyond regions[r].rows are skipped and
+ * set EP_STATUS_CAPACITY.  This is the push model of "perf(ep): optimize
+ * IntraNode dispatch kernel for MI350X", Technical Details 1 (each rank's rows
+ * are stored straight into that rank's receive buffer), on one GPU: a region
+ * is any allocation of this device.  (A region on a peer GPU would need the
+ * kernels' row stores to be plain peer stores; this library keeps every copy
+ * on this GPU's memory.)
+ *
+ *  x, topk_idx, topk_w  as for ep_dispatch
+ *  slot, rank_offset    int32 [T, W] and [W + 1] from ep_dispatch_layout (or any
+ *                       of the layout calls), complete in stream order
+ *  regions              HOST array of W ep_rank_region_t, read during the call
+ *                       (the table travels with the launch; the caller may
+ *                       reuse the array as soon as the call returns)
+ * Limits: those of ep_dispatch.
+ */
+EP_API int ep_dispatch_regions(const void* x, const int32_t* topk_idx, const float* topk_w,
+                               int64_t T, int H, int k, int W, const int32_t* slot,
+                               const int32_t* rank_offset, const ep_rank_region_t* regions,
+                               int quant, int32_t* status, ep_stream_t stream);
+
+/*
+ * Combine from per-rank regions: ep_combine with rank r's expert outputs in an
+ * allocation of their own.  The row of (t, r) is y_regions[r] row
+ * slot[t][r] - rank_offset[r]; out[t] is the bf16 rounding of the fp32 sum of
+ * those rows over the ranks of D(t) in ascending order from +0, as in
+ * ep_combine.  Rows at or beyond y_rows[r] are skipped and set
+ * EP_STATUS_CAPACITY.  Follows "perf(ep): optimize IntraNode dispatch kernel
+ * for MI350X", "Remaining gap" (combine reads each token's rows where the
+ * ranks hold them and accumulates them).
+ *
+ *  y_regions  HOST array of W device pointers, bf16 [y_rows[r], H], 16-byte aligned
+ *  y_rows     HOST array of W capacities
+ *  slot, rank_offset, out  as for ep_combine / ep_dispatch_regions
+ * Limits: H % 8 == 0; 1 <= W <= 32.
+ */
+EP_API int ep_combine_regions(const void* const* y_regions, const int64_t* y_rows,
+                              const int32_t* slot, const int32_t* rank_offset, int64_t T, int H,
+                              int W, void* out, int32_t* status, ep_stream_t stream);
+
+/*
  * ep_dispatch_layout without a workspace argument, for callers that cannot
  * allocate device memory: C or embedded hosts without a device allocator, and
  * latency-critical paths that must not call cudaMalloc (it blocks the host and

@@ -254,3 +254,47 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         _lib.load_library()
+
+
+@cpu_only
+@pytest.mark.parametrize("kw,code", [
+    (dict(W=0), _lib.EP_ERR_INVALID_ARG),
+    (dict(W=33), _lib.EP_ERR_INVALID_ARG),
+    (dict(table_null=True), _lib.EP_ERR_INVALID_ARG),
+    (dict(off_null=True), _lib.EP_ERR_INVALID_ARG),
+    (dict(rows=-1), _lib.EP_ERR_INVALID_ARG),
+    (dict(region_off=8), _lib.EP_ERR_MISALIGNED),               # a region's rows 8-byte aligned
+    (dict(quant=1, scale_null=True), _lib.EP_ERR_INVALID_ARG),  # FP8 region without scales
+    (dict(H=12), _lib.EP_ERR_UNSUPPORTED),
+])
+def test_dispatch_regions_rejects(lib, kw, code):
+    W = kw.get("W", 8)
+    n = max(W, 1)
+    table = (_lib.RankRegion * n)()
+    for r in range(n):
+        table[r] = _lib.RankRegion(A + 0x100000 * r + (kw.get("region_off", 0) if r == 3 else 0),
+                                   None if kw.get("scale_null") else A, A, A, A,
+                                   kw.get("rows", 100))
+    rc = lib.ep_dispatch_regions(A, A, A, 100, kw.get("H", 256), 8, W, A,
+                                 None if kw.get("off_null") else A,
+                                 None if kw.get("table_null") else table, kw.get("quant", 0),
+                                 None, None)
+    assert rc == code
+
+
+@cpu_only
+@pytest.mark.parametrize("kw,code", [
+    (dict(W=33), _lib.EP_ERR_INVALID_ARG),
+    (dict(H=12), _lib.EP_ERR_UNSUPPORTED),
+    (dict(rows=-5), _lib.EP_ERR_INVALID_ARG),
+    (dict(y_off=4), _lib.EP_ERR_MISALIGNED),
+    (dict(out_off=8), _lib.EP_ERR_MISALIGNED),
+    (dict(off_null=True), _lib.EP_ERR_INVALID_ARG),
+])
+def test_combine_regions_rejects(lib, kw, code):
+    W = kw.get("W", 8)
+    ptrs = (ctypes.c_void_p * W)(*[A + 0x100000 * r + kw.get("y_off", 0) for r in range(W)])
+    rows = (ctypes.c_int64 * W)(*[kw.get("rows", 100)] * W)
+    rc = lib.ep_combine_regions(ptrs, rows, A, None if kw.get("off_null") else A, 100,
+                                kw.get("H", 256), W, A + kw.get("out_off", 0), None, None)
+    assert rc == code

@@ -13,7 +13,14 @@ of inside the first kernel (measured: it would add about 11 us to combine).
 
 Prints ONE JSON line.  ``value`` is the step's algorithmic HBM GB/s (bytes the
 method must move, summed over ranks, over the max-over-ranks step time); the
-per-kernel microseconds and GB/s are in ``us`` and ``gbs``.
+per-kernel microseconds and GB/s are in ``us`` and ``gbs``.  Also in the line:
+``roofline`` (the step's dominant kernel against the measured copy peak, with
+the DRAM bytes of its committed ncu summary and the fraction they give),
+``steady_state`` (the step back to back over buffer sets larger than twice the
+L2, no flush, so every write-back lands inside the loop), ``workloads`` (every
+workload's kernels on their own, the FP8 Zipf dispatch, Qwen and the decode
+batch with CUDA-graph figures), ``e2e`` (host buffers in and out) and ``env``
+(GPU, driver, CUDA, library source hash).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -48,10 +55,13 @@ DRAIN_BYTES = 512 << 20
 
 # ----------------------------------------------------------------- byte model
 
-def alg_bytes(T: int, H: int, E: int, k: int, W: int, R: int) -> dict:
-    """Minimum HBM bytes each kernel must move (x read once per token)."""
+def alg_bytes(T: int, H: int, E: int, k: int, W: int, R: int, fp8: bool = False) -> dict:
+    """Minimum HBM bytes each kernel must move (x read once per token).  With
+    ``fp8`` the dispatch writes e4m3 codes and one fp32 scale per 128 values
+    instead of bf16 rows; combine always reads bf16 expert outputs."""
     layout = T * k * 4 + T * W * 4 + (E + 2 * W + 1) * 4
-    dispatch = T * H * 2 + T * k * 8 + T * W * 4 + R * H * 2 + R * (8 * k + 4)
+    payload = R * H + R * (H // 128) * 4 if fp8 else R * H * 2
+    dispatch = T * H * 2 + T * k * 8 + T * W * 4 + payload + R * (8 * k + 4)
     combine = R * H * 2 + T * W * 4 + T * H * 2
     return {"layout": layout, "dispatch": dispatch, "combine": combine,
             "step": layout + dispatch + combine}
@@ -88,6 +98,9 @@ KERNEL_SOURCES = {
     "combine": ("combine.cu", "ep_device.cuh"),
     "layout": ("layout.cu", "ep_device.cuh"),
     "dispatch_fp8": ("dispatch_fp8.cu", "dispatch_common.cuh", "ep_device.cuh"),
+    "dispatch_with_layout": ("layout.cu", "dispatch.cu", "dispatch_common.cuh", "ep_device.cuh"),
+    "dispatch_fp8_with_layout": ("layout.cu", "dispatch_fp8.cu", "dispatch_common.cuh",
+                                 "ep_device.cuh"),
 }
 
 
@@ -100,11 +113,11 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic_from_profile(kernel: str):
+def _traffic_from_profile(kernel: str, workload: str = WORKLOAD):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
     workload, if it was taken on the current kernel sources (its
     'source_sha256_16' line), else None."""
-    p = os.path.join(ROOT, "profiles", f"{kernel}_{WORKLOAD}.txt")
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     try:
         txt = open(p).read()
     except OSError:
@@ -201,6 +214,258 @@ def _dist():
     return world, rank, local
 
 
+def environment() -> dict:
+    """What the numbers were taken on: GPU, driver, CUDA and library sources."""
+    import torch
+
+    env = {"gpu": None, "driver": None, "cuda_runtime": torch.version.cuda,
+           "torch": torch.__version__, "git": None}
+    try:
+        env["gpu"] = torch.cuda.get_device_name(torch.cuda.current_device())
+    except Exception:
+        pass
+    try:
+        env["driver"] = subprocess.run(
+            ["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader"],
+            capture_output=True, text=True, timeout=20).stdout.strip().splitlines()[0]
+    except Exception:
+        pass
+    try:
+        r = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True,
+                           text=True, timeout=20)
+        if r.returncode == 0:
+            env["git"] = r.stdout.strip()
+    except Exception:
+        pass
+    # the sources the library is built from (a copy without git history still names them)
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_ep_dispatch_gb300", "csrc")
+    for d, names in ((csrc, sorted(os.listdir(csrc))), (os.path.join(ROOT, "include"),
+                                                       sorted(os.listdir(os.path.join(ROOT, "include"))))):
+        for n in names:
+            with open(os.path.join(d, n), "rb") as f:
+                h.update(n.encode() + b"\0" + f.read())
+    env["library_sources_sha256_16"] = h.hexdigest()[:16]
+    return env
+
+
+class L2Flush:
+    """A 256 MiB write, then a 512 MiB read that evicts the write's dirty lines,
+    so that their write-back lands before the next timed region, not inside it."""
+
+    def __init__(self, dev):
+        import torch
+
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.drain = torch.ones(DRAIN_BYTES // 8, dtype=torch.int64, device=dev)
+        self.drained = torch.empty((), dtype=torch.int64, device=dev)
+
+    def __call__(self, i: int = 0):
+        import torch
+
+        self.flush.fill_(i & 0xFF)
+        torch.sum(self.drain, dim=0, out=self.drained)
+
+
+def flushed_us(fns, n: int, l2: L2Flush, stream, warm: int = 3) -> list[float]:
+    """Median microseconds of each of ``fns`` (run in order, events between
+    them) over n repetitions, the L2 flushed before every repetition."""
+    import torch
+
+    evs = []
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(20_000_000)
+        for i in range(n + warm):
+            l2(i)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
+            e[0].record(stream)
+            for j, fn in enumerate(fns):
+                fn()
+                e[j + 1].record(stream)
+            if i >= warm:
+                evs.append(e)
+    stream.synchronize()
+    return [statistics.median(e[j].elapsed_time(e[j + 1]) * 1e3 for e in evs)
+            for j in range(len(fns))]
+
+
+def graph_us(fn, dev, per_graph: int = 20, replays: int = 10) -> float:
+    """Microseconds per call of ``fn`` captured in a CUDA graph (per_graph calls)
+    and replayed back to back (warm caches, no launch overhead)."""
+    import torch
+
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(per_graph):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / (replays * per_graph)
+
+
+def _kernel_entry(us: float, nbytes: int, peak: float, traffic: float | None) -> dict:
+    gbs = nbytes / (us * 1e-6) / 1e9
+    e = {"us": round(us, 2), "alg_bytes": int(nbytes), "gbs": round(gbs, 1),
+         "frac_of_peak": round(gbs / peak, 4), "dram_bytes": traffic}
+    e["dram_frac"] = None if traffic is None else round(traffic / (us * 1e-6) / 1e9 / peak, 4)
+    return e
+
+
+def time_workload(name: str, dev, stream, l2: L2Flush, n: int, peak: float, seed: int = 0) -> dict:
+    """Every kernel of one workload on its own and the step (layout + dispatch in
+    one call, then combine: there the combine also pays the write-back of the
+    rows the dispatch left dirty in L2), medians of n calls each after an L2
+    flush; GB/s of
+    algorithmic bytes, the fraction of the measured copy peak, and the DRAM bytes
+    of the kernel's committed ncu summary (with the fraction they give) where
+    that summary was taken on the current sources."""
+    import numpy as np
+    import torch
+
+    import combine_ep_dispatch_gb300 as ep
+    from combine_ep_dispatch_gb300.inputs import CONFIGS, make_inputs
+
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg, seed=seed)
+    T, H, E, k, W = cfg.T, cfg.H, cfg.E, cfg.k, cfg.W
+    fp8 = cfg.quant == "fp8"
+    x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+    idx = torch.from_numpy(inp["topk_idx"]).to(dev)
+    w = torch.from_numpy(inp["topk_w"]).to(dev)
+    # expert outputs: identity experts over a bf16 dispatch of the same routing
+    ident = ep.DispatchCombine(T, H, E, k, W, device=dev)
+    with torch.cuda.stream(stream):
+        ident.layout_dispatch(x, idx, w, stream)
+    stream.synchronize()
+    R = int(ident.rank_offset[W].item())
+    y = ident.recv_x[:R].clone()
+    del ident
+    dc = ep.DispatchCombine(T, H, E, k, W, capacity_rows=R, device=dev,
+                            quant=ep.EP_QUANT_FP8_E4M3_B128 if fp8 else ep.EP_QUANT_BF16)
+    nb = alg_bytes(T, H, E, k, W, R, fp8=fp8)
+    # each kernel on its own (the L2 flushed clean before it), then the step
+    (lay,) = flushed_us([lambda: dc.layout(idx, stream)], n, l2, stream)
+    (dis,) = flushed_us([lambda: dc.dispatch(x, idx, w, stream)], n, l2, stream)
+    (com,) = flushed_us([lambda: dc.combine(y, stream=stream)], n, l2, stream)
+    call, com_in_step = flushed_us([lambda: dc.layout_dispatch(x, idx, w, stream),
+                                    lambda: dc.combine(y, stream=stream)], n, l2, stream)
+    # the same dispatch and combine with each rank's rows in an allocation of
+    # its own (ep_dispatch_regions / ep_combine_regions), each on its own
+    off = [int(v) for v in dc.rank_offset.cpu()]
+    regs, y_regs = [], []
+    for r in range(W):
+        rows = off[r + 1] - off[r]
+        regs.append({"recv_x": torch.empty(rows, H, dtype=torch.uint8 if fp8 else torch.bfloat16,
+                                           device=dev),
+                     "recv_scale": torch.empty(rows, H // 128, dtype=torch.float32, device=dev)
+                     if fp8 else None,
+                     "recv_topk_idx": torch.empty(rows, k, dtype=torch.int32, device=dev),
+                     "recv_topk_w": torch.empty(rows, k, dtype=torch.float32, device=dev),
+                     "recv_src": torch.empty(rows, dtype=torch.int32, device=dev)})
+        y_regs.append(y[off[r]:off[r + 1]].clone())
+    q = ep.EP_QUANT_FP8_E4M3_B128 if fp8 else ep.EP_QUANT_BF16
+    (rdis,) = flushed_us([lambda: ep.ep_dispatch_regions(x, idx, w, dc.slot, dc.rank_offset, regs,
+                                                         q, dc.status, stream)], n, l2, stream)
+    (rcom,) = flushed_us([lambda: ep.ep_combine_regions(y_regs, dc.slot, dc.rank_offset, dc.out,
+                                                        dc.status, stream)], n, l2, stream)
+    del regs, y_regs
+    ok = int(dc.status.item()) == 0
+    dk = "dispatch_fp8" if fp8 else "dispatch"
+    entry = {
+        "config": {"T": T, "H": H, "E": E, "k": k, "W": W, "R": R, "routing": cfg.routing,
+                   "dispatch_payload": "fp8 e4m3, 1x128 fp32 scales" if fp8 else "bf16",
+                   "combine": "bf16 expert outputs"},
+        "layout": _kernel_entry(lay, nb["layout"], peak, None),
+        "dispatch": _kernel_entry(dis, nb["dispatch"], peak, _traffic_from_profile(dk, name)),
+        "combine": _kernel_entry(com, nb["combine"], peak, _traffic_from_profile("combine", name)),
+        "layout_dispatch_call": _kernel_entry(
+            call, nb["layout"] + nb["dispatch"], peak,
+            _traffic_from_profile(dk + "_with_layout", name)),
+        "regions": {"dispatch": _kernel_entry(rdis, nb["dispatch"], peak, None),
+                    "combine": _kernel_entry(rcom, nb["combine"], peak, None),
+                    "mode": "rank r's receive rows / expert outputs in an allocation of its own"},
+        "step_us": round(call + com_in_step, 2),
+        "step_gbs": round(nb["step"] / ((call + com_in_step) * 1e-6) / 1e9, 1),
+        "launches_per_step": ep.ep_dispatch_with_layout_launches(
+            T, H, k, W, ep.EP_QUANT_FP8_E4M3_B128 if fp8 else ep.EP_QUANT_BF16) + 1,
+        "status_ok": ok,
+    }
+    if T <= 1024:  # latency-bound: per call, eager and in a CUDA graph
+        def step():
+            dc.layout_dispatch(x, idx, w)
+            dc.combine(y)
+        entry["graph_us_per_step"] = round(graph_us(step, dev), 2)
+        entry["graph_us_per_dispatch_call"] = round(
+            graph_us(lambda: dc.layout_dispatch(x, idx, w), dev), 2)
+        entry["graph_us_per_combine"] = round(graph_us(lambda: dc.combine(y), dev), 2)
+    del dc, y, x, idx, w
+    torch.cuda.empty_cache()
+    return entry
+
+
+def steady_state_us(dev, stream, seed: int, n: int = 300, sets: int = 3) -> dict:
+    """The headline step run back to back over ``sets`` buffer sets used in turn
+    (inputs, receive rows, expert outputs, output: about 1 GB each, together
+    well over twice the L2), with no flush: every step's write-back of the rows
+    it leaves dirty lands inside the loop, in the following steps."""
+    import numpy as np
+    import torch
+
+    import combine_ep_dispatch_gb300 as ep
+    from combine_ep_dispatch_gb300.inputs import CONFIGS, make_inputs
+
+    cfg = CONFIGS[WORKLOAD]
+    bufs = []
+    for b in range(sets):
+        inp = make_inputs(cfg, seed=seed + 100 + b)
+        x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+        idx = torch.from_numpy(inp["topk_idx"]).to(dev)
+        w = torch.from_numpy(inp["topk_w"]).to(dev)
+        dc = ep.DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, device=dev)
+        with torch.cuda.stream(stream):
+            dc.layout_dispatch(x, idx, w, stream)
+        stream.synchronize()
+        R = int(dc.rank_offset[cfg.W].item())
+        bufs.append({"dc": dc, "x": x, "idx": idx, "w": w, "y": dc.recv_x.clone(), "R": R})
+    total = sum(alg_bytes(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, b["R"])["step"] for b in bufs)
+    set_bytes = sum(t.numel() * t.element_size() for b in bufs
+                    for t in (b["x"], b["y"], b["dc"].recv_x, b["dc"].out)) / sets
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(2 * sets):   # warm
+            b = bufs[i % sets]
+            b["dc"].layout_dispatch(b["x"], b["idx"], b["w"], stream)
+            b["dc"].combine(b["y"], stream=stream)
+        torch.cuda._sleep(20_000_000)
+        a.record(stream)
+        for i in range(n):
+            b = bufs[i % sets]
+            b["dc"].layout_dispatch(b["x"], b["idx"], b["w"], stream)
+            b["dc"].combine(b["y"], stream=stream)
+        e.record(stream)
+    stream.synchronize()
+    us = a.elapsed_time(e) * 1e3 / n
+    ok = all(int(b["dc"].status.item()) == 0 for b in bufs)
+    del bufs
+    torch.cuda.empty_cache()
+    return {"us_per_step": round(us, 2), "gbs": round(total / sets / (us * 1e-6) / 1e9, 1),
+            "sets": sets, "bytes_per_set": int(set_bytes), "steps": n, "status_ok": ok,
+            "mode": "back to back, buffer sets used in turn, no flush: each step pays the "
+                    "write-back of what the previous steps left dirty in L2"}
+
+
 # ----------------------------------------------------------------- our arm
 
 def run_ours(args) -> dict | None:
@@ -233,14 +498,7 @@ def run_ours(args) -> dict | None:
     idx = idx_h.to(dev)
     w = w_h.to(dev)
     dc = ep.DispatchCombine(T, H, E, k, W, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    drain = torch.ones(DRAIN_BYTES // 8, dtype=torch.int64, device=dev)
-    drained = torch.empty((), dtype=torch.int64, device=dev)
-
-    def l2_flush(i):
-        flush.fill_(i & 0xFF)
-        torch.sum(drain, dim=0, out=drained)
-
+    l2_flush = L2Flush(dev)
     torch.cuda.synchronize()
 
     # expert outputs of identity experts, in a buffer of their own
@@ -275,6 +533,8 @@ def run_ours(args) -> dict | None:
             # the step as a user runs it: layout + dispatch in one call (the
             # dispatch loads x while the layout runs), then combine
             dc.layout_dispatch(x, idx, w, stream)
+            if events is not None and len(events) == 3:
+                events[1].record(stream)
         dc.combine(y, stream=stream)
         if events is not None:
             events[-1].record(stream)
@@ -306,7 +566,16 @@ def run_ours(args) -> dict | None:
         barrier()
         step_ms = [e[0].elapsed_time(e[1]) for e in ev]
 
-        # (2) per-kernel breakdown: events between the kernels
+        # (2) the same step with an event between its two calls: the one
+        # layout + dispatch call and the combine, each as the step runs it
+        evc = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(40_000_000)
+        for i in range(args.steps):
+            l2_flush(i)
+            step(evc[i])
+        torch.cuda.synchronize()
+        # (2b) per-kernel breakdown: layout, dispatch and combine as three calls
         evk = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
         torch.cuda.synchronize()
         torch.cuda._sleep(40_000_000)
@@ -316,6 +585,8 @@ def run_ours(args) -> dict | None:
         torch.cuda.synchronize()
         sampler.mark_stop()
     clocks = sampler.stop()
+    call_ms = [e[0].elapsed_time(e[1]) for e in evc]
+    cstep_ms = [e[1].elapsed_time(e[2]) for e in evc]
     lay_ms = [e[0].elapsed_time(e[1]) for e in evk]
     dis_ms = [e[1].elapsed_time(e[2]) for e in evk]
     com_ms = [e[2].elapsed_time(e[3]) for e in evk]
@@ -349,18 +620,37 @@ def run_ours(args) -> dict | None:
     # resident in L2
     warm_ms = graph_step_ms(dc, x, idx, w, y, dev)
 
+    # (6) steady state over buffer sets larger than L2, no flush; (7) every
+    # workload on its own (rank 0 only: they are context, not the headline)
+    steady = steady_state_us(dev, stream, args.seed + rank) if not args.quick else None
+    peak, peak_kind = _peaks()
+    workloads = None
+    if rank == 0 and not args.quick:
+        workloads = {"tiny": {"timed": False,
+                              "role": "parity case only (T=128 H=256 E=16 top-4 W=4): the GPU "
+                                      "tests compare every output with the oracle"}}
+        n_wl = max(20, min(args.steps, 200))
+        for name in ("dsv3", "dsv3_zipf_fp8", "qwen", "decode"):
+            workloads[name] = time_workload(name, dev, stream, l2_flush, n_wl, peak, args.seed)
+
     mean = statistics.fmean
-    (s_ms, l_ms, d_ms, c_ms, e_ms, p_ms, g_ms), total_bytes = aggregate(
-        [mean(step_ms), mean(lay_ms), mean(dis_ms), mean(com_ms), mean(e2e_ms), pipe_ms, warm_ms],
-        nbytes["step"], world, dev)
+    (s_ms, l_ms, d_ms, c_ms, e_ms, p_ms, g_ms, call_m, cst_m), total_bytes = aggregate(
+        [mean(step_ms), mean(lay_ms), mean(dis_ms), mean(com_ms), mean(e2e_ms), pipe_ms, warm_ms,
+         mean(call_ms), mean(cstep_ms)], nbytes["step"], world, dev)
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
         return None
 
-    peak, peak_kind = _peaks()
-    dom, dom_ms = ("dispatch", d_ms) if d_ms >= c_ms else ("combine", c_ms)
-    achieved = nbytes[dom] / (dom_ms * 1e-3) / 1e9
+    # the dominant kernel of the step as it runs: the one layout + dispatch call
+    # (its bytes include the layout's) or the combine that follows it
+    call_bytes = nbytes["layout"] + nbytes["dispatch"]
+    if call_m >= cst_m:
+        dom, dom_ms, dom_bytes = "dispatch_with_layout", call_m, call_bytes
+    else:
+        dom, dom_ms, dom_bytes = "combine", cst_m, nbytes["combine"]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = _traffic_from_profile(dom)
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
     h2d = x_h.numel() * 2 + idx_h.numel() * 4 + w_h.numel() * 4
     d2h = out_h.numel() * 2
@@ -389,17 +679,25 @@ def run_ours(args) -> dict | None:
                           "best": round(min(step_ms) * 1e3, 2),
                           "median": round(statistics.median(step_ms) * 1e3, 2),
                           "n": len(step_ms)},
-        # per-kernel figures come from separate calls with events in between
-        "us": {"step": round(s_ms * 1e3, 2), "layout": round(l_ms * 1e3, 2),
+        # per-kernel figures: the step's two calls with an event between them
+        # (layout_dispatch_call, combine_in_step), and three separate calls
+        # with events in between (layout, dispatch, combine)
+        "us": {"step": round(s_ms * 1e3, 2), "layout_dispatch_call": round(call_m * 1e3, 2),
+               "combine_in_step": round(cst_m * 1e3, 2), "layout": round(l_ms * 1e3, 2),
                "dispatch": round(d_ms * 1e3, 2), "combine": round(c_ms * 1e3, 2)},
         "gbs": {"step": round(gbs(nbytes["step"], s_ms), 1),
+                "layout_dispatch_call": round(gbs(call_bytes, call_m), 1),
+                "combine_in_step": round(gbs(nbytes["combine"], cst_m), 1),
                 "layout": round(gbs(nbytes["layout"], l_ms), 1),
                 "dispatch": round(gbs(nbytes["dispatch"], d_ms), 1),
                 "combine": round(gbs(nbytes["combine"], c_ms), 1),
                 "frac_of_nominal_8tbs": {"step": round(gbs(nbytes["step"], s_ms) / 8000.0, 4),
                                          "dispatch": round(gbs(nbytes["dispatch"], d_ms) / 8000.0, 4),
                                          "combine": round(gbs(nbytes["combine"], c_ms) / 8000.0, 4)},
-                "frac_of_peak": {"dispatch": round(gbs(nbytes["dispatch"], d_ms) / peak, 4),
+                "frac_of_peak": {"step": round(gbs(nbytes["step"], s_ms) / peak, 4),
+                                 "layout_dispatch_call": round(gbs(call_bytes, call_m) / peak, 4),
+                                 "combine_in_step": round(gbs(nbytes["combine"], cst_m) / peak, 4),
+                                 "dispatch": round(gbs(nbytes["dispatch"], d_ms) / peak, 4),
                                  "combine": round(gbs(nbytes["combine"], c_ms) / peak, 4)},
                 "pages_convention": {"dispatch": round(pages_convention_gbs(R, H, 2, d_ms * 1e-3), 1),
                                      "combine": round(pages_convention_gbs(R, H, 2, c_ms * 1e-3), 1)}},
@@ -407,7 +705,16 @@ def run_ours(args) -> dict | None:
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": _traffic_from_profile(dom)},
+                     "alg_bytes_per_launch": int(dom_bytes), "us_per_launch": round(dom_ms * 1e3, 2),
+                     "traffic": traffic,
+                     # DRAM bytes of the kernel's ncu summary over the same time: the
+                     # fraction of the peak that reached HBM within the launch
+                     "dram_frac": None if traffic is None else round(
+                         traffic / (dom_ms * 1e-3) / 1e9 / peak, 4),
+                     "steady_state_us_per_step": None if steady is None else steady["us_per_step"]},
+        "steady_state": steady,
+        "workloads": workloads,
+        "env": environment(),
         "cpu_baseline": cpu_baseline(args) if not args.no_cpu else None,
         "e2e": {"value": round(total_bytes / (p_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(p_ms, 4), "h2d_bytes_per_step": h2d,
@@ -635,6 +942,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--quick", action="store_true",
+                    help="only the headline step (no per-workload table, no steady state)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

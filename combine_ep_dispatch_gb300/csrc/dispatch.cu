@@ -155,10 +155,23 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
 
   const bool meta_lanes = 2 * k + 1 <= 32;
   bool cap_err = false, timed_out = false;
-  int s_cur = finalize(load_slot(slot, gw, W, lane, T), gw);
+  // Token order.  Stage q % kTmaStages holds the warp's q-th token, s_ring
+  // records which (-1: none).  The first kTmaStages tokens of warp gw are gw,
+  // gw + NW, gw + 2 NW (loaded early).  After that, with a claim counter (the
+  // dispatch that finishes the layout: the count kernel zeroed it) a warp
+  // takes the next unclaimed token of [kTmaStages NW, T) whenever it refills a
+  // stage, so warps that drew tokens with few destinations take more of them
+  // and all finish together; without one it keeps the fixed stride.
+  __shared__ int64_t s_ring[kTmaMaxWarps][kTmaStages];
+  unsigned long long* const claim = fin.claim;
+  if (lane == 0)
+    for (int q = 0; q < kTmaStages; ++q) s_ring[warp][q] = q < n ? gw + q * NW : -1;
+  __syncwarp();
+  bool more = true;  // later tokens may still exist
+  int64_t t = s_ring[warp][0];
+  int s_cur = t >= 0 ? finalize(load_slot(slot, t, W, lane, T), t) : -1;
   int64_t j = 0;
-  for (; j < n; ++j) {
-    const int64_t t = gw + j * NW;
+  for (; t >= 0; ++j) {
     const int st = (int)(j % kTmaStages);
     const uint32_t parity = (uint32_t)((j / kTmaStages) & 1);
     // one metadata word per lane: k ids, k weights, the source index
@@ -171,7 +184,8 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
       else
         mv = (int32_t)t;
     }
-    const int s_next = load_slot(slot, t + NW, W, lane, T);
+    const int64_t t_next = s_ring[warp][(j + 1) % kTmaStages];
+    const int s_next = t_next >= 0 ? load_slot(slot, t_next, W, lane, T) : -1;
     int64_t srow = s_cur, lim = cap;  // the row in its storage and that storage's capacity
     if (RT::kRegions && s_cur >= 0) {
       srow = storage_row<RT>(s_cur, lane, s_rv);
@@ -225,20 +239,39 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
       carry_metadata<RT>(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane,
                          &s_rv);
     }
-    // refill the previous token's buffer once the copies out of it (issued by
-    // several lanes) have read it
-    if (j >= 1 && issued < n) {
-      bulk_wait_read<1>();
+    // refill the previous token's stage with the warp's (j + kTmaStages - 1)-th
+    // token, once the copies out of it (issued by several lanes) have read it
+    if (j >= 1) {
+      const int sp = (int)((j - 1) % kTmaStages);
+      int64_t tn = -1;
+      if (more) {
+        if (claim != nullptr) {
+          unsigned long long c = 0;
+          if (lane == 0) c = atomicAdd(claim, 1ull);
+          tn = (int64_t)kTmaStages * NW + (int64_t)__shfl_sync(kFull, c, 0);
+        } else {
+          tn = gw + (j + kTmaStages - 1) * NW;
+        }
+        if (tn >= T) {
+          tn = -1;
+          more = false;
+        }
+      }
+      if (tn >= 0) {
+        bulk_wait_read<1>();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[sp], row_bytes);
+          bulk_load(buf + sp * stage_bytes, x + tn * row_bytes, row_bytes, &full[sp]);
+          ++issued;
+        }
+      }
+      if (lane == 0) s_ring[warp][sp] = tn;
       __syncwarp();
     }
-    if (lane == 0 && j >= 1 && issued < n) {
-      const int sp = (int)((j - 1) % kTmaStages);
-      mbar_arrive_expect_tx(&full[sp], row_bytes);
-      bulk_load(buf + sp * stage_bytes, x + (gw + issued * NW) * row_bytes, row_bytes, &full[sp]);
-      ++issued;
-    }
     issued = __shfl_sync(kFull, issued, 0);
-    s_cur = finalize(s_next, t + NW);
+    t = t_next;
+    s_cur = t_next >= 0 ? finalize(s_next, t_next) : -1;
   }
   if (fin_mode) finish_expert_totals(fin);
   if (lane == 0) {
@@ -422,7 +455,7 @@ cudaError_t launch_dispatch_with_layout(const void* x, const int32_t* topk_idx, 
     cudaError_t e = launch_layout_count(topk_idx, T, k, E, W, workspace, slot, status, stream, &ch);
     if (e != cudaSuccess) return e;
     Finalize fin{ch.chunk_rank, ch.chunk_exp, ch.C, ch.shift, E, num_tokens_per_expert,
-                 num_tokens_per_rank, rank_offset};
+                 num_tokens_per_rank, rank_offset, ch.claim};
     if (quant == EP_QUANT_FP8_E4M3_B128)
       return launch_dispatch_fp8(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, recv_x,
                                  recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream,

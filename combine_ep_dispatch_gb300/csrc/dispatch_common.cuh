@@ -201,6 +201,7 @@ struct Finalize {
   int32_t* num_tokens_per_expert;
   int32_t* num_tokens_per_rank;
   int32_t* rank_offset;
+  unsigned long long* claim;  // zero at the dispatch's start (the count kernel zeroes it), or null
 };
 constexpr int kFinMaxBytes = 16384;  // shared memory for the chunk table (C * W ints)
 

@@ -204,6 +204,7 @@ struct LayoutChunks {
   const int32_t* chunk_exp;   // [C][E]  (t, j) entries of chunk c with expert e
   int64_t C;
   int shift;
+  unsigned long long* claim;  // a counter the count kernel zeroes for the dispatch after it
 };
 // The count kernel alone; with local_slot non-null it also writes each
 // (t, r)'s position p inside its chunk there as -2 - p (-1 when r is not in

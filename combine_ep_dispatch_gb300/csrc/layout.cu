@@ -29,11 +29,12 @@ struct LayoutWs {
   uint32_t* mask;       // [T]     bit r set iff r in D(t)
   int32_t* chunk_rank;  // [C][W]  tokens of chunk c with r in D(t)
   int32_t* chunk_exp;   // [C][E]  (t, j) entries of chunk c with expert e
+  unsigned long long* claim;  // token counter of the dispatch that finishes the layout
 };
 
 inline int64_t num_chunks(int64_t T) { return T <= 0 ? 1 : (T + kLT - 1) / kLT; }
 
-LayoutWs carve(void* ws, int64_t T, int W) {
+LayoutWs carve(void* ws, int64_t T, int W, int E) {
   char* p = static_cast<char*>(ws);
   const int64_t C = num_chunks(T);
   LayoutWs w;
@@ -42,6 +43,8 @@ LayoutWs carve(void* ws, int64_t T, int W) {
   w.chunk_rank = reinterpret_cast<int32_t*>(p);
   p += a256(sizeof(int32_t) * (size_t)(C * W));
   w.chunk_exp = reinterpret_cast<int32_t*>(p);
+  p += a256(sizeof(int32_t) * (size_t)(C * (size_t)E));
+  w.claim = reinterpret_cast<unsigned long long*>(p);
   return w;
 }
 
@@ -108,6 +111,9 @@ __global__ void __launch_bounds__(kLT)
     }
   }
   if (live) ws.mask[t] = m;
+  // the dispatch that finishes this layout claims tokens from this counter
+  // (it reads it only after this kernel has completed)
+  if (blockIdx.x == 0 && tid == 0) *ws.claim = 0ull;
 
   int cnt = 0;
   for (int r = 0; r < W; ++r) {
@@ -380,7 +386,7 @@ int64_t layout_num_chunks(int64_t T) { return num_chunks(T); }
 size_t layout_workspace_bytes(int64_t T, int W, int E) {
   const int64_t C = num_chunks(T);
   return a256(sizeof(uint32_t) * (size_t)T) + a256(sizeof(int32_t) * (size_t)(C * W)) +
-         a256(sizeof(int32_t) * (size_t)(C * E));
+         a256(sizeof(int32_t) * (size_t)(C * E)) + a256(sizeof(unsigned long long));
 }
 
 cudaError_t launch_layout_count(const int32_t* topk_idx, int64_t T, int k, int E, int W,
@@ -388,11 +394,12 @@ cudaError_t launch_layout_count(const int32_t* topk_idx, int64_t T, int k, int E
                                 cudaStream_t stream, LayoutChunks* chunks) {
   const bool vec = (reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0;
   const int64_t C = num_chunks(T);
-  const LayoutWs ws = carve(workspace, T, W);
+  const LayoutWs ws = carve(workspace, T, W, E);
   chunks->chunk_rank = ws.chunk_rank;
   chunks->chunk_exp = ws.chunk_exp;
   chunks->C = C;
   chunks->shift = kLTShift;
+  chunks->claim = ws.claim;
   const size_t smem = sizeof(int32_t) * (size_t)E;
   if (k == 8 && vec)
     return launch_pdl(layout_count_kernel<8, true>, dim3((unsigned)C), dim3(kLT), smem, stream,
@@ -449,7 +456,7 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
                       rank_offset, slot, status);
   }
   const int64_t C = num_chunks(T);
-  const LayoutWs ws = carve(workspace, T, W);
+  const LayoutWs ws = carve(workspace, T, W, E);
   const size_t smem = sizeof(int32_t) * (size_t)E;
   cudaError_t err;
   if (k == 8 && vec)

@@ -268,8 +268,8 @@ class L2Flush:
 
 
 def flushed_us(fns, n: int, l2: L2Flush, stream, warm: int = 3) -> list[float]:
-    """Median microseconds of each of ``fns`` (run in order, events between
-    them) over n repetitions, the L2 flushed before every repetition."""
+    """Microseconds of each of ``fns`` (run in order, events between them),
+    trimmed mean over n repetitions, the L2 flushed before every repetition."""
     import torch
 
     evs = []
@@ -285,8 +285,17 @@ def flushed_us(fns, n: int, l2: L2Flush, stream, warm: int = 3) -> list[float]:
             if i >= warm:
                 evs.append(e)
     stream.synchronize()
-    return [statistics.median(e[j].elapsed_time(e[j + 1]) * 1e3 for e in evs)
-            for j in range(len(fns))]
+    return [trimmed_mean([e[j].elapsed_time(e[j + 1]) * 1e3 for e in evs]) for j in range(len(fns))]
+
+
+def trimmed_mean(v: list[float], cut: float = 0.05) -> float:
+    """Mean without the lowest and highest 5%: CUDA events tick in steps of about
+    1 us here, so a median of single calls sits on a tick; the mean of the
+    middle 90% resolves finer and ignores rare outliers."""
+    v = sorted(v)
+    c = int(len(v) * cut)
+    v = v[c:len(v) - c] if len(v) > 2 * c else v
+    return sum(v) / len(v)
 
 
 def graph_us(fn, dev, per_graph: int = 20, replays: int = 10) -> float:
@@ -326,8 +335,8 @@ def _kernel_entry(us: float, nbytes: int, peak: float, traffic: float | None) ->
 def time_workload(name: str, dev, stream, l2: L2Flush, n: int, peak: float, seed: int = 0) -> dict:
     """Every kernel of one workload on its own and the step (layout + dispatch in
     one call, then combine: there the combine also pays the write-back of the
-    rows the dispatch left dirty in L2), medians of n calls each after an L2
-    flush; GB/s of
+    rows the dispatch left dirty in L2), trimmed means of n calls each after an
+    L2 flush; GB/s of
     algorithmic bytes, the fraction of the measured copy peak, and the DRAM bytes
     of the kernel's committed ncu summary (with the fraction they give) where
     that summary was taken on the current sources."""

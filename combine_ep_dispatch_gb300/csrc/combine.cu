@@ -53,10 +53,11 @@ __global__ void __launch_bounds__(kCThreads)
     combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ slot,
                    const float* __restrict__ w, int64_t T, int n16, int S, int seg16, int W,
                    int64_t cap, uint4* __restrict__ out, int32_t* __restrict__ status, RT rt) {
-  pdl_wait();
-  __shared__ typename RT::View s_rv;  // per-rank regions of y: the table (with its first rows)
+  __shared__ typename RT::View s_rv;  // per-rank regions of y: the table
   load_region_view(rt, W, s_rv);
+  pdl_wait();
   const int lane = threadIdx.x & 31;
+  const int32_t first_row = region_first_row(rt, W, lane);
   const int64_t gwarp = ((int64_t)blockIdx.x * kCThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kCThreads) >> 5;
   if constexpr (!SEG) S = 1;  // whole rows: the unit is the token
@@ -73,7 +74,7 @@ __global__ void __launch_bounds__(kCThreads)
 
     int64_t srow = s, lim = cap;  // the row in its storage and that storage's capacity
     if (RT::kRegions && s >= 0) {
-      srow = storage_row<RT>(s, lane, s_rv);
+      srow = storage_row<RT>(s, first_row);
       lim = storage_rows<RT>(lane, cap, s_rv);
     }
     const bool keep = s >= 0 && srow < lim;

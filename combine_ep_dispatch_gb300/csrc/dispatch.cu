@@ -20,15 +20,16 @@ __global__ void __launch_bounds__(kDThreads)
                          const int32_t* __restrict__ slot, int64_t cap, uint4* __restrict__ recv_x,
                          int32_t* __restrict__ recv_topk_idx, float* __restrict__ recv_topk_w,
                          int32_t* __restrict__ recv_src, int32_t* __restrict__ status, RT rt) {
-  pdl_wait();
   __shared__ typename RT::View s_rv;
   load_region_view(rt, W, s_rv);
+  pdl_wait();
   const int lane = threadIdx.x & 31;
+  const int32_t first_row = region_first_row(rt, W, lane);
   const int64_t gwarp = ((int64_t)blockIdx.x * kDThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kDThreads) >> 5;
   bool cap_err = false;
   for (int64_t t = gwarp; t < T; t += nwarps) {
-    const Dests d = token_dests<RT>(slot, t, W, cap, lane, &s_rv);
+    const Dests d = token_dests<RT>(slot, t, W, cap, lane, &s_rv, first_row);
     cap_err |= d.cap_err;
     carry_metadata<RT>(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane,
                        &s_rv);
@@ -77,6 +78,9 @@ __global__ void __launch_bounds__(kDThreads)
 // load/store pipe free; the other lanes fetch the next token's slots early and
 // carry the metadata.
 constexpr int kTmaStages = 3;            // row buffers per warp
+// The token loop reads the next token's stage before it refills the previous
+// one: three stages at least, so that the two are different.
+static_assert(kTmaStages >= 3, "the bulk-copy dispatch needs three row buffers per warp");
 constexpr int kTmaBarBytes = 1024;       // barrier area ahead of the row buffers
 constexpr int kTmaSmemBudget = 100000;   // row buffers per CTA
 constexpr int kTmaMaxWarps = 8;
@@ -133,11 +137,12 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
       }
     }
   };
+  __shared__ typename RT::View s_rv;  // per-rank regions: the table
+  load_region_view(rt, W, s_rv);
   if (x_early) first_loads(kTmaStages);
   pdl_wait();
   first_loads(kTmaStages);
-  __shared__ typename RT::View s_rv;  // per-rank regions: the table (with its first rows)
-  load_region_view(rt, W, s_rv);
+  const int32_t first_row = region_first_row(rt, W, lane);
 
   const bool fin_mode = fin.chunk_rank != nullptr;  // uniform over the grid
   __shared__ int32_t s_tot[32], s_off[33];
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
     const int s_next = t_next >= 0 ? load_slot(slot, t_next, W, lane, T) : -1;
     int64_t srow = s_cur, lim = cap;  // the row in its storage and that storage's capacity
     if (RT::kRegions && s_cur >= 0) {
-      srow = storage_row<RT>(s_cur, lane, s_rv);
+      srow = storage_row<RT>(s_cur, first_row);
       lim = storage_rows<RT>(lane, cap, s_rv);
     }
     const bool keep = s_cur >= 0 && srow < lim;

@@ -10,9 +10,11 @@ namespace ep {
 // layout's slot is the row).  RankRegions: one allocation per rank
 // (ep_dispatch_regions, ep_combine_regions), passed as a table of base
 // pointers: the row of (t, r) is slot[t][r] - rank_offset[r] of rank r's
-// region, and each region has its own capacity.  Kernels copy the table and
-// the regions' first global rows into shared memory (RegionView) after their
-// dependency wait, since rank_offset comes from the layout.
+// region, and each region has its own capacity.  Kernels copy the table into
+// shared memory before their dependency wait (it comes with the launch), and
+// lane r of every warp loads rank_offset[r], the first global row of rank r's
+// region, after it (rank_offset comes from the layout): the lanes of a warp
+// stand for the ranks whenever a slot row is read.
 struct OneBuffer {
   static constexpr bool kRegions = false;
   struct View {
@@ -36,37 +38,45 @@ struct RankRegions {
     float* topk_w[kMaxRanks];
     int32_t* src[kMaxRanks];
     int64_t rows[kMaxRanks];
-    int32_t off[kMaxRanks + 1];
   };
 };
 
-// Fills the shared view of a region table; every thread of the CTA calls it,
-// after the kernel's dependency wait.
+// Fills the shared view of a region table (the pointers and capacities that
+// come with the launch); every thread of the CTA calls it, before the
+// kernel's dependency wait.
 template <class RT>
 __device__ __forceinline__ void load_region_view(const RT& rt, int W, typename RT::View& v) {
   if constexpr (RT::kRegions) {
-    for (int r = threadIdx.x; r <= W; r += blockDim.x) {
-      v.off[r] = rt.rank_offset[r];
-      if (r < W) {
-        v.x[r] = rt.x[r];
-        v.scale[r] = rt.scale[r];
-        v.topk_idx[r] = rt.topk_idx[r];
-        v.topk_w[r] = rt.topk_w[r];
-        v.src[r] = rt.src[r];
-        v.rows[r] = rt.rows[r];
-      }
+    for (int r = threadIdx.x; r < W; r += blockDim.x) {
+      v.x[r] = rt.x[r];
+      v.scale[r] = rt.scale[r];
+      v.topk_idx[r] = rt.topk_idx[r];
+      v.topk_w[r] = rt.topk_w[r];
+      v.src[r] = rt.src[r];
+      v.rows[r] = rt.rows[r];
     }
     __syncthreads();
   }
 }
 
-// Row of the slot entry s (>= 0) of rank r inside r's storage, and that
-// storage's capacity: the global row and `cap` for one buffer, the row inside
-// the region and the region's capacity for per-rank regions.
+// First global row of rank `lane`'s region (per-rank regions, lane < W); read
+// after the dependency wait.  0 otherwise.
 template <class RT>
-__device__ __forceinline__ int64_t storage_row(int s, int r, const typename RT::View& v) {
+__device__ __forceinline__ int32_t region_first_row(const RT& rt, int W, int lane) {
   if constexpr (RT::kRegions)
-    return (int64_t)s - v.off[r];
+    return lane < W ? rt.rank_offset[lane] : 0;
+  else
+    return 0;
+}
+
+// Row of the slot entry s (>= 0) of rank r inside r's storage (first_row: the
+// region's first global row, region_first_row of lane r), and that storage's
+// capacity: the global row and `cap` for one buffer, the row inside the region
+// and the region's capacity for per-rank regions.
+template <class RT>
+__device__ __forceinline__ int64_t storage_row(int s, int32_t first_row) {
+  if constexpr (RT::kRegions)
+    return (int64_t)s - first_row;
   else
     return s;
 }
@@ -102,13 +112,14 @@ struct Dests {
 template <class RT = OneBuffer>
 __device__ __forceinline__ Dests token_dests(const int32_t* __restrict__ slot, int64_t t, int W,
                                              int64_t cap, int lane,
-                                             const typename RT::View* v = nullptr) {
+                                             const typename RT::View* v = nullptr,
+                                             int32_t first_row = 0) {
   int s = -1;
   if (lane < W) s = __ldg(slot + t * W + lane);
   int64_t row = s, lim = cap;
   if constexpr (RT::kRegions) {
     if (s >= 0) {
-      row = storage_row<RT>(s, lane, *v);
+      row = storage_row<RT>(s, first_row);
       lim = storage_rows<RT>(lane, cap, *v);
     }
   }

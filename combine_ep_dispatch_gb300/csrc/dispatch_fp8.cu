@@ -178,8 +178,9 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
     split(u, t, seg, q0, q_end);
     if (x_early) load_step(t, q0, q_end, A, C);
   }
-  pdl_wait();
   load_region_view(rt, W, s_rv);
+  pdl_wait();
+  const int32_t first_row = region_first_row(rt, W, lane);
   // With a Finalize the slot table holds in-chunk positions: every CTA scans
   // the chunk counts first; the warp taking a token's first segment writes
   // its receive rows back (other segments may read either form).
@@ -197,7 +198,10 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
   d.nd = 0;
   d.my_row = -1;
   int sc_row = -1;  // lane (qb, hl): row of destination hl, which receives block qb's scale
-  int sc_rank = 0;  // and (per-rank regions) its rank
+  // per-rank regions: lane i's destination row (codes) and lane (qb, hl)'s
+  // scale row, as addresses, formed once per unit
+  uint8_t* reg_code_row = nullptr;
+  float* reg_scale_row = nullptr;
   // Unit by unit; inside a unit, step by step.  Each step issues the loads
   // of the next one (the next unit's first step at a unit's last) before it
   // quantises and stores its own, so loads stay in flight during the
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
       }
       int64_t srow = s_raw, lim = cap;  // the row in its storage and that storage's capacity
       if (RT::kRegions && s_raw >= 0) {
-        srow = storage_row<RT>(s_raw, lane, s_rv);
+        srow = storage_row<RT>(s_raw, first_row);
         lim = storage_rows<RT>(lane, cap, s_rv);
       }
       const bool keep = s_raw >= 0 && srow < lim;
@@ -229,7 +233,12 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
       d.my_rank = RT::kRegions && lane < d.nd ? my_drank[lane] : -1;
       d.cap_err = __any_sync(kFull, over);
       sc_row = hl < d.nd ? my_dst[hl] : -1;
-      if constexpr (RT::kRegions) sc_rank = hl < d.nd ? my_drank[hl] : 0;
+      if constexpr (RT::kRegions) {
+        reg_code_row = lane < d.nd ? s_rv.x[my_drank[lane]] + (uint64_t)(uint32_t)my_dst[lane] * (uint32_t)H
+                                   : nullptr;
+        reg_scale_row = hl < d.nd ? s_rv.scale[my_drank[hl]] + (uint64_t)(uint32_t)sc_row * (uint32_t)nb
+                                  : nullptr;
+      }
       if (seg == 0) {
         cap_err |= d.cap_err;
         carry_metadata<RT>(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane,
@@ -284,14 +293,12 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
         if constexpr (RT::kRegions) {
 #pragma unroll 1
           for (int qq = 0; qq < d.nd; ++qq) {
-            const uint32_t row = (uint32_t)__shfl_sync(kFull, d.my_row, qq);
-            const int rk = __shfl_sync(kFull, d.my_rank, qq);
-            uint8_t* const xb = s_rv.x[rk] + b * 128 + hl * 16;
-            if (has) st_v4(reinterpret_cast<uint4*>(xb + (uint64_t)row * (uint32_t)H), codes[v]);
+            uint8_t* const xr = reinterpret_cast<uint8_t*>(
+                __shfl_sync(kFull, reinterpret_cast<unsigned long long>(reg_code_row), qq));
+            if (has) st_v4(reinterpret_cast<uint4*>(xr + b * 128 + hl * 16), codes[v]);
           }
           if (has) {
-            if (sc_row >= 0)
-              s_rv.scale[sc_rank][(uint64_t)(uint32_t)sc_row * (uint32_t)nb + b] = sc[v];
+            if (reg_scale_row != nullptr) reg_scale_row[b] = sc[v];
             for (int j = hl + 8; j < d.nd; j += 8)
               s_rv.scale[my_drank[j]][(uint64_t)(uint32_t)my_dst[j] * (uint32_t)nb + b] = sc[v];
           }

@@ -95,7 +95,7 @@ def _peaks():
 
 KERNEL_SOURCES = {
     "dispatch": ("dispatch.cu", "dispatch_common.cuh", "ep_device.cuh"),
-    "combine": ("combine.cu", "ep_device.cuh"),
+    "combine": ("combine.cu", "dispatch_common.cuh", "ep_device.cuh"),
     "layout": ("layout.cu", "ep_device.cuh"),
     "dispatch_fp8": ("dispatch_fp8.cu", "dispatch_common.cuh", "ep_device.cuh"),
     "dispatch_with_layout": ("layout.cu", "dispatch.cu", "dispatch_common.cuh", "ep_device.cuh"),

@@ -73,3 +73,43 @@ def test_aggregate_over_two_gloo_ranks():
 def test_aggregate_single_rank_is_identity():
     s, t = bench.aggregate([1.5, 2.5], 7.0, 1, torch.device("cpu"))
     assert s == [1.5, 2.5] and t == 7.0
+
+
+def test_alg_bytes_fp8_payload():
+    """FP8 rows: one byte per value plus one fp32 scale per 128 values, the
+    rest of the dispatch's bytes as for bf16; combine unchanged."""
+    T, H, E, k, W, R = 4096, 7168, 256, 8, 8, 11815
+    b16, b8 = bench.alg_bytes(T, H, E, k, W, R), bench.alg_bytes(T, H, E, k, W, R, fp8=True)
+    assert b16["dispatch"] - b8["dispatch"] == R * H * 2 - (R * H + R * (H // 128) * 4)
+    assert b8["combine"] == b16["combine"] and b8["layout"] == b16["layout"]
+    assert b8["step"] == b8["layout"] + b8["dispatch"] + b8["combine"]
+
+
+def test_trimmed_mean_drops_the_tails():
+    v = [10.0] * 90 + [1000.0] * 5 + [0.0] * 5
+    assert bench.trimmed_mean(v) == 10.0
+    assert bench.trimmed_mean([3.0, 5.0]) == 4.0
+    # on a 1 us tick grid, the mean of the middle resolves finer than the median
+    ticks = [1.024 * (50 + (i % 4 == 0)) for i in range(100)]
+    assert abs(bench.trimmed_mean(ticks) - 1.024 * 50.25) < 0.03
+
+
+def test_profile_traffic_needs_matching_sources(tmp_path, monkeypatch):
+    """DRAM bytes come from a profile summary only while its source hash is the
+    current one (a summary of other sources would describe another kernel)."""
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    good = bench.kernel_source_hash("combine")
+    (prof / "combine_dsv3.txt").write_text(f"source_sha256_16: {good}\ndram_bytes_per_launch: 123\n")
+    (prof / "dispatch_dsv3.txt").write_text("source_sha256_16: 0000\ndram_bytes_per_launch: 456\n")
+    real_join = os.path.join
+
+    def join(*a):
+        if len(a) >= 2 and a[1] == "profiles":
+            return real_join(str(tmp_path), *a[1:])
+        return real_join(*a)
+
+    monkeypatch.setattr(bench.os.path, "join", join)
+    assert bench._traffic_from_profile("combine", "dsv3") == 123.0
+    assert bench._traffic_from_profile("dispatch", "dsv3") is None
+    assert bench._traffic_from_profile("combine", "qwen") is None

@@ -267,3 +267,40 @@ def test_two_streams_do_not_interfere():
         assert torch.equal(dc.slot, slot)
         assert torch.equal(dc.out.view(torch.int16), out.view(torch.int16))
         assert int(dc.status.item()) == 0
+
+
+@pytest.mark.parametrize("T", [1825, 4096, 12000])
+def test_token_claims_give_the_same_bits_every_call(T):
+    """Past the first three tokens per warp the single call's dispatch hands
+    out tokens from a counter, so which warp sends which token changes from
+    call to call; every output must not.  Twelve calls in a row on one
+    workspace (the count kernel zeroes the counter each time) against the
+    oracle, T just past the static tokens (3 x 608 warps), at dsv3 and larger."""
+    rng = np.random.default_rng(T)
+    H, E, k, W = 7168, 256, 8, 8
+    x = make_bf16(rng, (T, H))
+    idx = make_routing(rng, T, E, k, "uniform")
+    w = rng.random((T, k), dtype=np.float32)
+    lay = oracle.layout(idx, E, W)
+    R = int(lay["rank_offset"][-1])
+    want = oracle.dispatch(x, idx, w, lay["slot"], R)
+    dc = ep.DispatchCombine(T, H, E, k, W, capacity_rows=R)
+    xd = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda()
+    idd, wd = torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()
+    first = None
+    for i in range(12):
+        dc.recv_x.view(torch.int16).fill_(0x7FAB)
+        dc.layout_dispatch(xd, idd, wd)
+        torch.cuda.synchronize()
+        got = (dc.recv_x.view(torch.int16).clone(), dc.slot.clone(), dc.recv_src.clone(),
+               dc.recv_topk_w.clone(), dc.num_tokens_per_expert.clone())
+        if first is None:
+            first = got
+            assert_rows_equal(got[0].cpu().numpy().view(np.uint16), want["recv_x"], "recv_x")
+            assert_rows_equal(got[1].cpu().numpy(), lay["slot"], "slot")
+            assert_rows_equal(got[2].cpu().numpy(), want["recv_src"], "recv_src")
+            assert_rows_equal(got[4].cpu().numpy(), lay["num_tokens_per_expert"], "counts")
+        else:
+            for a, b in zip(got, first):
+                assert torch.equal(a, b), i
+    assert int(dc.status.item()) == 0

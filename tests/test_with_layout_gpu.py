@@ -62,6 +62,8 @@ def test_workloads(name):
     (3001, 2048, 64, 6, 8),     # ragged chunks
     (700, 256, 32, 4, 4),       # rows under 1 KB: the register dispatch kernel
     (513, 1536, 96, 3, 6),
+    (10000, 7168, 256, 8, 8),   # FP8: one segment per token, longer than the units quantised early
+    (2500, 1152, 72, 5, 8),     # FP8: 9 blocks, a partial quadruple in every unit
 ])
 def test_shapes(T, H, E, k, W, quant):
     if quant == ep.EP_QUANT_FP8_E4M3_B128 and H % 128:

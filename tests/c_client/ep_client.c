@@ -6,10 +6,12 @@
  *     checks that reject a call before anything reaches a GPU;
  *   gpu mode (built with -DEP_CLIENT_GPU): a small batch through
  *     ep_dispatch_with_layout and ep_combine with identity experts (the
- *     combine reads the dispatched rows back).  Every output row must then be
- *     d_t * x_t exactly, with d_t the number of distinct destination ranks of
- *     token t: small integer inputs make the fp32 sum and the bf16 rounding
- *     exact, so this closed form needs no reference implementation.
+ *     combine reads the dispatched rows back), then the same rows through
+ *     ep_dispatch_regions and ep_combine_regions with every rank's rows in a
+ *     cudaMalloc of its own.  Every output row must then be d_t * x_t exactly,
+ *     with d_t the number of distinct destination ranks of token t: small
+ *     integer inputs make the fp32 sum and the bf16 rounding exact, so this
+ *     closed form needs no reference implementation.
  */
 #include <stdio.h>
 #include <stdlib.h>
@@ -41,6 +43,13 @@ static int query_mode(void) {
   if (ep_dispatch(NULL, NULL, NULL, 10, 12, 8, 8, NULL, 80, EP_QUANT_BF16, NULL, NULL, NULL, NULL,
                   NULL, NULL, NULL) != EP_ERR_UNSUPPORTED)
     return fail("reject H = 12");
+  /* per-rank regions: no table, or more than 32 ranks */
+  if (ep_dispatch_regions(NULL, NULL, NULL, 10, 256, 8, 8, NULL, NULL, NULL, EP_QUANT_BF16, NULL,
+                          NULL) != EP_ERR_INVALID_ARG)
+    return fail("reject regions without a table");
+  if (ep_combine_regions(NULL, NULL, NULL, NULL, 10, 256, 33, NULL, NULL, NULL) !=
+      EP_ERR_INVALID_ARG)
+    return fail("reject 33 ranks of regions");
   printf("query mode ok\n");
   return 0;
 }
@@ -128,7 +137,47 @@ static int gpu_mode(void) {
         fprintf(stderr, "token %d column %d\n", t, h);
         return fail("combine(dispatch(x)) != d_t * x");
       }
-  printf("gpu mode ok: T=%d H=%d E=%d k=%d W=%d R=%d\n", T, H, E, K, W, R);
+
+  /* the same rows into per-rank regions: one allocation per rank, sized to
+     its rows, the table passed from host memory */
+  ep_rank_region_t regions[W];
+  const void* yreg[W];
+  int64_t yrows[W];
+  for (int r = 0; r < W; ++r) {
+    const int64_t n = off[r + 1] - off[r];
+    memset(&regions[r], 0, sizeof regions[r]);
+    regions[r].rows = n;
+    CK(cudaMalloc(&regions[r].recv_x, (size_t)(n > 0 ? n : 1) * H * 2));
+    CK(cudaMalloc((void**)&regions[r].recv_src, (size_t)(n > 0 ? n : 1) * 4));
+    yreg[r] = regions[r].recv_x;
+    yrows[r] = n;
+  }
+  CK(cudaMemset(dout, 0, sizeof out));
+  rc = ep_dispatch_regions(dx, didx, dw, T, H, K, W, dslot, doff, regions, EP_QUANT_BF16, dst,
+                           NULL);
+  if (rc != EP_OK) return fail(ep_status_string(rc));
+  rc = ep_combine_regions(yreg, yrows, dslot, doff, T, H, W, dout, dst, NULL);
+  if (rc != EP_OK) return fail(ep_status_string(rc));
+  CK(cudaDeviceSynchronize());
+  CK(cudaMemcpy(out, dout, sizeof out, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(&status, dst, 4, cudaMemcpyDeviceToHost));
+  if (status != 0) return fail("status word (regions)");
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h)
+      if (out[t * H + h] != bf16_of_int(d[t] * ((t * 7 + h * 3) % 17 - 8))) {
+        fprintf(stderr, "token %d column %d\n", t, h);
+        return fail("combine_regions(dispatch_regions(x)) != d_t * x");
+      }
+  for (int r = 0; r < W; ++r) { /* region r's source tokens ascend */
+    const int64_t n = yrows[r];
+    static int32_t src[T];
+    if (n == 0) continue;
+    CK(cudaMemcpy(src, regions[r].recv_src, (size_t)n * 4, cudaMemcpyDeviceToHost));
+    for (int64_t i = 1; i < n; ++i)
+      if (src[i] <= src[i - 1]) return fail("region rows out of token order");
+  }
+  printf("gpu mode ok: T=%d H=%d E=%d k=%d W=%d R=%d (one buffer and per-rank regions)\n", T, H, E,
+         K, W, R);
   return 0;
 }
 #endif

@@ -99,6 +99,9 @@ KERNEL_SOURCES = {
     "layout": ("layout.cu", "ep_device.cuh"),
     "dispatch_fp8": ("dispatch_fp8.cu", "dispatch_common.cuh", "ep_device.cuh"),
     "combine_in_step": ("combine.cu", "dispatch_common.cuh", "ep_device.cuh"),
+    "combine_regions": ("combine.cu", "dispatch_common.cuh", "ep_device.cuh"),
+    "dispatch_regions": ("dispatch.cu", "dispatch_common.cuh", "ep_device.cuh"),
+    "dispatch_fp8_regions": ("dispatch_fp8.cu", "dispatch_common.cuh", "ep_device.cuh"),
     "dispatch_with_layout": ("layout.cu", "dispatch.cu", "dispatch_common.cuh", "ep_device.cuh"),
     "dispatch_fp8_with_layout": ("layout.cu", "dispatch_fp8.cu", "dispatch_common.cuh",
                                  "ep_device.cuh"),
@@ -403,8 +406,10 @@ def time_workload(name: str, dev, stream, l2: L2Flush, n: int, peak: float, seed
         "layout_dispatch_call": _kernel_entry(
             call, nb["layout"] + nb["dispatch"], peak,
             _traffic_from_profile(dk + "_with_layout", name)),
-        "regions": {"dispatch": _kernel_entry(rdis, nb["dispatch"], peak, None),
-                    "combine": _kernel_entry(rcom, nb["combine"], peak, None),
+        "regions": {"dispatch": _kernel_entry(rdis, nb["dispatch"], peak, _traffic_from_profile(
+                        "dispatch_fp8_regions" if fp8 else "dispatch_regions", name)),
+                    "combine": _kernel_entry(rcom, nb["combine"], peak,
+                                             _traffic_from_profile("combine_regions", name)),
                     "mode": "rank r's receive rows / expert outputs in an allocation of its own"},
         "step_us": round(call + com_in_step, 2),
         "step_gbs": round(nb["step"] / ((call + com_in_step) * 1e-6) / 1e9, 1),

@@ -11,7 +11,8 @@ expert-major path (one row per (token, expert) pair, combine weighted by the
 gate weights); --fused uses the one-launch layout + dispatch (rank order,
 bf16, small batches); --with-layout uses the single layout + dispatch call
 (rank order); --cast-transpose adds the FP8 cast and transposed cast of the
-received rows (expert order).
+received rows (expert order); --regions dispatches into and combines from
+per-rank regions, one allocation per rank (rank order, after the layout).
 """
 from __future__ import annotations
 
@@ -34,6 +35,7 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true")
     ap.add_argument("--with-layout", action="store_true")
     ap.add_argument("--cast-transpose", action="store_true")
+    ap.add_argument("--regions", action="store_true")
     args = ap.parse_args(argv)
 
     inp = make_inputs(args.workload, seed=args.seed)
@@ -55,6 +57,36 @@ def main(argv=None):
         cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, capacity_rows=R, device=dev, order=order)
     weights = w if order == "expert" else None
     scale = torch.full((cfg.E,), 112.0, dtype=torch.float32, device=dev)
+    if args.regions:
+        if order != "rank":
+            raise SystemExit("--regions takes the rank-major layout")
+        regions, y_regions = [], []
+        dc.layout(idx)
+        ident.layout(idx)
+        ident.dispatch(x, idx, w)
+        torch.cuda.synchronize()
+        off = [int(v) for v in dc.rank_offset.cpu()]
+        fp8 = quant != _lib.EP_QUANT_BF16
+        for r in range(cfg.W):
+            n = off[r + 1] - off[r]
+            regions.append({
+                "recv_x": torch.empty(n, cfg.H, dtype=torch.uint8 if fp8 else torch.bfloat16,
+                                      device=dev),
+                "recv_scale": (torch.empty(n, cfg.H // 128, dtype=torch.float32, device=dev)
+                               if fp8 else None),
+                "recv_topk_idx": torch.empty(n, cfg.k, dtype=torch.int32, device=dev),
+                "recv_topk_w": torch.empty(n, cfg.k, dtype=torch.float32, device=dev),
+                "recv_src": torch.empty(n, dtype=torch.int32, device=dev)})
+            y_regions.append(ident.recv_x[off[r]:off[r + 1]].clone())
+        for _ in range(args.iters):
+            dc.layout(idx)
+            _lib.ep_dispatch_regions(x, idx, w, dc.slot, dc.rank_offset, regions, quant,
+                                     dc.status)
+            _lib.ep_combine_regions(y_regions, dc.slot, dc.rank_offset, dc.out, dc.status)
+        torch.cuda.synchronize()
+        print(f"{args.workload} (rank, per-rank regions): T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} "
+              f"W={cfg.W} R={R} iters={args.iters} status={int(dc.status.item())}")
+        return
     for _ in range(args.iters):
         if args.fused:
             dc.dispatch_fused(x, idx, w)

@@ -107,7 +107,9 @@ EP_API int64_t ep_max_recv_rows(int64_t T, int k, int W);
  *  slot                  int32 [T, W]   out: receive row of (t, r):
  *                                       rank_offset[r] + #{t' < t : r in D(t')}
  *                                       if r in D(t), else -1
- *  workspace             ep_layout_workspace_bytes(T, W, E) bytes, 16-byte aligned
+ *  workspace             ep_layout_workspace_bytes(T, W, E) bytes, 16-byte aligned;
+ *                        it serves one call at a time (calls that overlap on
+ *                        the GPU need workspaces of their own)
  * Limits: 0 <= T, T * min(k, W) < 2^31; 1 <= k; 1 <= W <= 32; E % W == 0;
  * 1 <= E <= 8192.
  */
@@ -160,7 +162,11 @@ EP_API int ep_dispatch(const void* x, const int32_t* topk_idx, const float* topk
  * before ep_dispatch).  For T > 1024 (FP8 rows, or bf16 rows of at least
  * 1 KB) the dispatch also finishes the layout: the count kernel numbers each
  * token inside its chunk of 128 and the dispatch adds the chunk's base row, so
- * the scan kernel is not launched.  bf16 batches of up to 512 tokens (k <= 16)
+ * the scan kernel is not launched; its bf16 warps then take tokens from a
+ * counter that the count kernel zeroes in the workspace (the workspace must
+ * not be shared by calls that overlap on the GPU, as for ep_dispatch_layout).
+ * Which warp sends which token varies from call to call; the results do not.
+ * bf16 batches of up to 512 tokens (k <= 16)
  * take the one-launch kernel of ep_dispatch_fused, the fastest there
  * (ep_dispatch_with_layout_launches).  The layout
  * is the one of "perf(ep): optimize IntraNode dispatch kernel for MI350X",

@@ -88,6 +88,13 @@ __global__ void __launch_bounds__(kCThreads)
       const float wl = lane < W ? __ldg(w + t * W + lane) : 0.0f;
       my_w = __shfl_sync(kFull, wl, r & 31);               // and its weight
     }
+    // lane i's destination row as an address, formed once per unit (for
+    // per-rank regions: its region's base plus the row inside it)
+    const uint4* my_src = y;
+    if (r >= 0)
+      my_src = reinterpret_cast<const uint4*>(rows_base<RT>(
+                   s_rv, r, reinterpret_cast<uint8_t*>(const_cast<uint4*>(y)))) +
+               (int64_t)my_row * n16;
     uint4* dst = out + t * n16;
     for (int c0 = c_lo; c0 < c_hi; c0 += 32 * U) {
       float acc[U][8];
@@ -96,17 +103,13 @@ __global__ void __launch_bounds__(kCThreads)
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
       for (int dg = 0; dg < nd; dg += 8) {
-        int rows[8];
         float wts[8];
         const uint4* ybase[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          rows[q] = __shfl_sync(kFull, my_row, (dg + q) & 31);
           wts[q] = WEIGHTED ? __shfl_sync(kFull, my_w, (dg + q) & 31) : 1.0f;
-          if constexpr (RT::kRegions)
-            ybase[q] = reinterpret_cast<const uint4*>(s_rv.x[__shfl_sync(kFull, r, (dg + q) & 31) & 31]);
-          else
-            ybase[q] = y;
+          ybase[q] = reinterpret_cast<const uint4*>(__shfl_sync(
+              kFull, reinterpret_cast<unsigned long long>(my_src), (dg + q) & 31));
         }
         uint4 v[8][U];
 #pragma unroll
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(kCThreads)
             const int c = c0 + u * 32 + lane;
             v[q][u] = make_uint4(0u, 0u, 0u, 0u);
             if (dg + q < nd && c < c_hi)
-              v[q][u] = ld_stream_v4(ybase[q] + (int64_t)rows[q] * n16 + c);
+              v[q][u] = ld_stream_v4(ybase[q] + c);
           }
         }
 #pragma unroll

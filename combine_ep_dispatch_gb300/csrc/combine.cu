@@ -171,6 +171,12 @@ __global__ void __launch_bounds__(kCThreads)
       }
     }
   }
+  // The dependent launch is released once every warp of the CTA is done (as
+  // in the bulk-copy dispatch).  Released by each warp as it finished, the
+  // next step's kernels launched while other warps still summed rows: back
+  // to back over buffer sets larger than L2 (no flush), layout + dispatch +
+  // combine at T=4096, H=7168 took 124.0 us per step instead of 119.6 us.
+  __syncthreads();
   pdl_launch_dependents();
   if (cap_err && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_CAPACITY);
 }

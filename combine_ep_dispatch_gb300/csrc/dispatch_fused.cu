@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     if (timed_out && lane == 0) (void)mbar_wait_bounded(&s_bar[warp], (uses - 1u) & 1u);
     bulk_wait_all();
   }
-  __syncwarp();
+  __syncthreads();  // the CTA releases the dependent launch when all its warps are done
   pdl_launch_dependents();
   if (lane == 0 && status != nullptr) {
     if (cap_err) atomicOr(status, EP_STATUS_CAPACITY);

@@ -343,7 +343,8 @@ def time_workload(name: str, dev, stream, l2: L2Flush, n: int, peak: float, seed
     L2 flush.  The step is timed as a whole (``step_us``, the combine launched
     right behind the dispatch as in the headline) and split by an event
     between the two calls (``layout_dispatch_call``, ``combine_in_step``; the
-    event also ends the overlap of the two launches); GB/s of
+    event also ends the overlap of the two launches), and for T > 1024 back to
+    back over three buffer sets without a flush (``steady_state_us``); GB/s of
     algorithmic bytes, the fraction of the measured copy peak, and the DRAM bytes
     of the kernel's committed ncu summary (with the fraction they give) where
     that summary was taken on the current sources."""
@@ -422,6 +423,8 @@ def time_workload(name: str, dev, stream, l2: L2Flush, n: int, peak: float, seed
         "step_us": round(step, 2),
         "step_gbs": round(nb["step"] / (step * 1e-6) / 1e9, 1),
         "step_us_with_event_between": round(call + com_in_step, 2),
+        "steady_state_us": (steady_state_us(dev, stream, seed, name=name)["us_per_step"]
+                            if T > 1024 else None),
         "launches_per_step": ep.ep_dispatch_with_layout_launches(
             T, H, k, W, ep.EP_QUANT_FP8_E4M3_B128 if fp8 else ep.EP_QUANT_BF16) + 1,
         "status_ok": ok,
@@ -439,31 +442,40 @@ def time_workload(name: str, dev, stream, l2: L2Flush, n: int, peak: float, seed
     return entry
 
 
-def steady_state_us(dev, stream, seed: int, n: int = 300, sets: int = 3) -> dict:
-    """The headline step run back to back over ``sets`` buffer sets used in turn
-    (inputs, receive rows, expert outputs, output: about 1 GB each, together
-    well over twice the L2), with no flush: every step's write-back of the rows
-    it leaves dirty lands inside the loop, in the following steps."""
+def steady_state_us(dev, stream, seed: int, n: int = 300, sets: int = 3,
+                    name: str | None = None) -> dict:
+    """The step of workload ``name`` (the headline's by default) run back to
+    back over ``sets`` buffer sets used in turn (inputs, receive rows, expert
+    outputs, output: together well over twice the L2), with no flush: every
+    step's write-back of the rows it leaves dirty lands inside the loop, in
+    the following steps.  An FP8 workload dispatches FP8 rows and combines
+    bf16 expert outputs (identity experts over a bf16 dispatch)."""
     import numpy as np
     import torch
 
     import combine_ep_dispatch_gb300 as ep
     from combine_ep_dispatch_gb300.inputs import CONFIGS, make_inputs
 
-    cfg = CONFIGS[WORKLOAD]
+    cfg = CONFIGS[name or WORKLOAD]
+    fp8 = cfg.quant == "fp8"
     bufs = []
     for b in range(sets):
         inp = make_inputs(cfg, seed=seed + 100 + b)
         x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).to(dev)
         idx = torch.from_numpy(inp["topk_idx"]).to(dev)
         w = torch.from_numpy(inp["topk_w"]).to(dev)
-        dc = ep.DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, device=dev)
+        ident = ep.DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, device=dev)
         with torch.cuda.stream(stream):
-            dc.layout_dispatch(x, idx, w, stream)
+            ident.layout_dispatch(x, idx, w, stream)
         stream.synchronize()
-        R = int(dc.rank_offset[cfg.W].item())
-        bufs.append({"dc": dc, "x": x, "idx": idx, "w": w, "y": dc.recv_x.clone(), "R": R})
-    total = sum(alg_bytes(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, b["R"])["step"] for b in bufs)
+        R = int(ident.rank_offset[cfg.W].item())
+        y = ident.recv_x[:R].clone()
+        del ident
+        dc = ep.DispatchCombine(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, capacity_rows=R, device=dev,
+                                quant=ep.EP_QUANT_FP8_E4M3_B128 if fp8 else ep.EP_QUANT_BF16)
+        bufs.append({"dc": dc, "x": x, "idx": idx, "w": w, "y": y, "R": R})
+    total = sum(alg_bytes(cfg.T, cfg.H, cfg.E, cfg.k, cfg.W, b["R"], fp8=fp8)["step"]
+                for b in bufs)
     set_bytes = sum(t.numel() * t.element_size() for b in bufs
                     for t in (b["x"], b["y"], b["dc"].recv_x, b["dc"].out)) / sets
     a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

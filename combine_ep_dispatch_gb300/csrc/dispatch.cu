@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kDThreads)
       }
     }
   }
+  __syncthreads();  // the CTA releases the dependent launch when all its warps are done
   pdl_launch_dependents();
   if (cap_err && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_CAPACITY);
 }

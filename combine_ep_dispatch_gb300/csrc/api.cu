@@ -296,10 +296,12 @@ int ep_dispatch_experts_with_layout(const void* x, const int32_t* topk_idx, cons
                                            slot, workspace, status, s));
   if (rc != EP_OK) return rc;
   // the dispatch follows the layout kernels directly: its first rows of x are
-  // loaded while they run
+  // loaded while they run, and (bulk-copy rows) it takes its later tokens from
+  // a counter the layout zeroed in the workspace
   return from_cuda(ep::launch_dispatch(x, topk_idx, topk_w, T, H, k, k, slot, capacity_rows, quant,
                                        recv_x, recv_scale, recv_topk_idx, recv_topk_w, recv_src,
-                                       status, s, /*x_early=*/1));
+                                       status, s, /*x_early=*/1,
+                                       ep::layout_experts_claim(workspace, T, k, E)));
 }
 
 int ep_combine_weighted(const void* y, const int32_t* slot, const float* w, int64_t T, int H,

@@ -368,17 +368,21 @@ cudaError_t launch_dispatch_rt(const void* x, const int32_t* topk_idx, const flo
                                int64_t T, int H, int k, int W, const int32_t* slot,
                                int64_t capacity_rows, int quant, void* recv_x, float* recv_scale,
                                int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
-                               int32_t* status, cudaStream_t stream, int x_early, const RT& rt) {
+                               int32_t* status, cudaStream_t stream, int x_early, const RT& rt,
+                               unsigned long long* claim = nullptr) {
   if (T == 0) return cudaSuccess;
   const uint4* x4 = static_cast<const uint4*>(x);
   Finalize none{};
   if (quant == EP_QUANT_BF16) {
     TmaShape sh;
     if (tma_shape(H, &sh)) {
-      // the kernel writes the slot table only with a Finalize
+      // the kernel writes the slot table only with a Finalize; it takes tokens
+      // from `claim` (zeroed by the layout kernel before it) when given one
+      Finalize claims{};
+      claims.claim = claim;
       return launch_tma(x, topk_idx, topk_w, T, k, W, const_cast<int32_t*>(slot), capacity_rows,
                         recv_x, recv_topk_idx, recv_topk_w, recv_src, status, stream, x_early,
-                        sh, none, rt);
+                        sh, claims, rt);
     }
     const int n16 = H / 8;
     if (n16 % (32 * 7) == 0) {
@@ -404,10 +408,11 @@ cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float*
                             int64_t T, int H, int k, int W, const int32_t* slot,
                             int64_t capacity_rows, int quant, void* recv_x, float* recv_scale,
                             int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
-                            int32_t* status, cudaStream_t stream, int x_early) {
+                            int32_t* status, cudaStream_t stream, int x_early,
+                            unsigned long long* claim) {
   return launch_dispatch_rt(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, quant, recv_x,
                             recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream,
-                            x_early, OneBuffer{});
+                            x_early, OneBuffer{}, claim);
 }
 
 cudaError_t launch_dispatch_regions(const void* x, const int32_t* topk_idx, const float* topk_w,

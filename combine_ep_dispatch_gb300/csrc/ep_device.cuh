@@ -233,7 +233,8 @@ cudaError_t launch_dispatch(const void* x, const int32_t* topk_idx, const float*
                             int64_t T, int H, int k, int W, const int32_t* slot,
                             int64_t capacity_rows, int quant, void* recv_x, float* recv_scale,
                             int32_t* recv_topk_idx, float* recv_topk_w, int32_t* recv_src,
-                            int32_t* status, cudaStream_t stream, int x_early = 0);
+                            int32_t* status, cudaStream_t stream, int x_early = 0,
+                            unsigned long long* claim = nullptr);
 
 cudaError_t launch_localize_ids(int32_t* recv_topk_idx, const int32_t* rank_offset, int64_t cap,
                                 int k, int E, int W, cudaStream_t stream);
@@ -259,6 +260,9 @@ cudaError_t launch_cast_transpose(const void* y, const int32_t* expert_offset, i
 
 int layout_experts_max_experts();
 size_t layout_experts_workspace_bytes(int64_t T, int k, int E);
+// The token counter that launch_layout_experts zeroes in its workspace for the
+// dispatch that follows it (null when its one-CTA path runs, which has none).
+unsigned long long* layout_experts_claim(void* workspace, int64_t T, int k, int E);
 cudaError_t launch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,
                                   int32_t* num_tokens_per_expert, int32_t* expert_offset,
                                   int32_t* slot, void* workspace, int32_t* status,

@@ -45,6 +45,7 @@ inline int64_t x_chunks(int64_t P) { return P <= 0 ? 1 : (P + kXPairs - 1) / kXP
 struct XWs {
   int32_t* cnt;  // [C][E]: pairs of chunk c with expert e; after the scan, pairs in chunks < c
   int32_t* tot;  // [E]
+  unsigned long long* claim;  // token counter of the dispatch that follows in the same call
 };
 
 XWs x_carve(void* ws, int64_t P, int E) {
@@ -53,6 +54,8 @@ XWs x_carve(void* ws, int64_t P, int E) {
   w.cnt = reinterpret_cast<int32_t*>(p);
   p += a256(sizeof(int32_t) * (size_t)(x_chunks(P) * E));
   w.tot = reinterpret_cast<int32_t*>(p);
+  p += a256(sizeof(int32_t) * (size_t)E);
+  w.claim = reinterpret_cast<unsigned long long*>(p);
   return w;
 }
 
@@ -241,6 +244,10 @@ __global__ void __launch_bounds__(kXWarps * 32)
     }
   }
   if (__any_sync(kFull, bad) && lane == 0 && status != nullptr) atomicOr(status, EP_STATUS_BAD_EXPERT);
+  // the dispatch that follows these kernels in ep_dispatch_experts_with_layout
+  // claims tokens from this counter (it reads it only after its dependency
+  // wait, when this kernel has completed)
+  if (c == 0 && tid == 0) *ws.claim = 0ull;
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x) ws.cnt[c * E + e] = s_hist[e];
 }
@@ -369,7 +376,14 @@ int layout_experts_max_experts() { return kXMaxE; }
 
 size_t layout_experts_workspace_bytes(int64_t T, int k, int E) {
   const int64_t P = T * k;
-  return a256(sizeof(int32_t) * (size_t)(x_chunks(P) * E)) + a256(sizeof(int32_t) * (size_t)E);
+  return a256(sizeof(int32_t) * (size_t)(x_chunks(P) * E)) + a256(sizeof(int32_t) * (size_t)E) +
+         a256(sizeof(unsigned long long));
+}
+
+unsigned long long* layout_experts_claim(void* workspace, int64_t T, int k, int E) {
+  const int64_t P = T * k;
+  if (P <= kXSingleMax && E <= kXSingleMaxE) return nullptr;  // the one-CTA layout: no counter
+  return x_carve(workspace, P, E).claim;
 }
 
 cudaError_t launch_layout_experts(const int32_t* topk_idx, int64_t T, int k, int E,

@@ -363,9 +363,11 @@ EP_API int ep_dispatch_layout_noalloc(const int32_t* topk_idx, int64_t T, int k,
  *  expert_offset          int32 [E + 1]  expert_offset[E] = number of rows
  *  slot                   int32 [T, k]
  *  workspace              >= ep_layout_experts_workspace_bytes(T, k, E) bytes,
- *                         16-byte aligned, no initialisation
- * Limits: 1 <= k; 1 <= E <= 4096; T * k < 2^31.  Up to 8192 pairs and 1024
- * experts it is one kernel on one CTA, above that three kernels.
+ *                         16-byte aligned, no initialisation; it serves one
+ *                         call at a time
+ * Limits: 1 <= k; 1 <= E <= 4096; T * k < 2^31.  Up to 2048 pairs and 1024
+ * experts it is one kernel on one CTA; above that a count and an assign kernel
+ * (and a scan kernel between them beyond 32 chunks of 1024 pairs).
  * ep_layout_experts_workspace_bytes (host only, 0 for invalid arguments) is a
  * convention of this library, like ep_layout_workspace_bytes; the pages define
  * no such call.
@@ -382,7 +384,11 @@ EP_API int ep_dispatch_layout_experts(const int32_t* topk_idx, int64_t T, int k,
  * with the same arguments, limits (also k <= 32), results and errors.  The
  * dispatch becomes resident while the layout kernels run and loads its first
  * rows of x before the slots exist (x must be complete in stream order before
- * this call).
+ * this call).  Above 2048 pairs or 1024 experts, its bf16 bulk-copy warps
+ * then take tokens from a counter that the layout's count kernel zeroes in the
+ * workspace, so the workspace must not be shared by calls that overlap on the
+ * GPU; which warp sends which token varies from call to call, the results do
+ * not.
  */
 EP_API int ep_dispatch_experts_with_layout(const void* x, const int32_t* topk_idx,
                                            const float* topk_w, int64_t T, int H, int k, int E,

@@ -402,6 +402,9 @@ def time_workload(name: str, dev, stream, l2: L2Flush, n: int, peak: float, seed
                                                          q, dc.status, stream)], n, l2, stream)
     (rcom,) = flushed_us([lambda: ep.ep_combine_regions(y_regs, dc.slot, dc.rank_offset, dc.out,
                                                         dc.status, stream)], n, l2, stream)
+    (rcall,) = flushed_us([lambda: ep.ep_dispatch_regions_with_layout(
+        x, idx, w, E, dc.num_tokens_per_expert, dc.num_tokens_per_rank, dc.rank_offset, dc.slot,
+        dc.workspace, regs, q, dc.status, stream)], n, l2, stream)
     del regs, y_regs
     ok = int(dc.status.item()) == 0
     dk = "dispatch_fp8" if fp8 else "dispatch"
@@ -419,6 +422,8 @@ def time_workload(name: str, dev, stream, l2: L2Flush, n: int, peak: float, seed
                         "dispatch_fp8_regions" if fp8 else "dispatch_regions", name)),
                     "combine": _kernel_entry(rcom, nb["combine"], peak,
                                              _traffic_from_profile("combine_regions", name)),
+                    "layout_dispatch_call": _kernel_entry(rcall, nb["layout"] + nb["dispatch"],
+                                                          peak, None),
                     "mode": "rank r's receive rows / expert outputs in an allocation of its own"},
         "step_us": round(step, 2),
         "step_gbs": round(nb["step"] / (step * 1e-6) / 1e9, 1),

@@ -14,7 +14,8 @@ from ._lib import (EP_ERR_CUDA, EP_ERR_INVALID_ARG, EP_ERR_MISALIGNED, EP_ERR_UN
                    ep_dispatch_layout_experts, ep_combine_weighted, ep_selftest_wait_timeout,
                    EP_STATUS_TIMEOUT, ep_cast_transpose_t_bytes, ep_cast_transpose_experts,
                    ep_dispatch_with_layout, ep_dispatch_with_layout_launches,
-                   ep_dispatch_experts_with_layout, ep_dispatch_regions, ep_combine_regions)
+                   ep_dispatch_experts_with_layout, ep_dispatch_regions, ep_combine_regions,
+                   ep_dispatch_regions_with_layout)
 from .pipeline import DispatchCombine
 
 __all__ = [
@@ -27,5 +28,5 @@ __all__ = [
     "ep_selftest_wait_timeout", "EP_STATUS_TIMEOUT", "ep_cast_transpose_t_bytes",
     "ep_cast_transpose_experts", "ep_dispatch_with_layout",
     "ep_dispatch_with_layout_launches", "ep_dispatch_experts_with_layout",
-    "ep_dispatch_regions", "ep_combine_regions",
+    "ep_dispatch_regions", "ep_combine_regions", "ep_dispatch_regions_with_layout",
 ]

@@ -34,7 +34,7 @@ EXPORTED = ("ep_layout_workspace_bytes", "ep_max_recv_rows", "ep_dispatch_layout
             "ep_dispatch_layout_experts", "ep_combine_weighted", "ep_selftest_wait_timeout",
             "ep_cast_transpose_t_bytes", "ep_cast_transpose_experts", "ep_dispatch_with_layout",
             "ep_dispatch_with_layout_launches", "ep_dispatch_experts_with_layout",
-            "ep_dispatch_regions", "ep_combine_regions")
+            "ep_dispatch_regions", "ep_combine_regions", "ep_dispatch_regions_with_layout")
 
 # Largest batch ep_dispatch_fused takes.
 EP_FUSED_MAX_TOKENS = 1024
@@ -115,6 +115,10 @@ def load_library() -> ctypes.CDLL:
     lib.ep_dispatch_regions.argtypes = [_P, _P, _P, _I64, _I, _I, _I, _P, _P,
                                         ctypes.POINTER(RankRegion), _I, _P, _P]
     lib.ep_dispatch_regions.restype = _I
+    lib.ep_dispatch_regions_with_layout.argtypes = [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P,
+                                                    _P, _P, ctypes.c_size_t,
+                                                    ctypes.POINTER(RankRegion), _I, _P, _P]
+    lib.ep_dispatch_regions_with_layout.restype = _I
     lib.ep_combine_regions.argtypes = [ctypes.POINTER(ctypes.c_void_p),
                                        ctypes.POINTER(ctypes.c_int64), _P, _P, _I64, _I, _I, _P,
                                        _P, _P]
@@ -543,25 +547,11 @@ def ep_cast_transpose_experts(y: torch.Tensor, expert_offset: torch.Tensor, scal
     _raise("ep_cast_transpose_experts", rc)
 
 
-def ep_dispatch_regions(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
-                        slot: torch.Tensor, rank_offset: torch.Tensor, regions: list[dict],
-                        quant: int = EP_QUANT_BF16, status: torch.Tensor | None = None,
-                        stream=None) -> None:
-    """ep_dispatch into per-rank regions: ``regions[r]`` is a dict with rank r's
-    receive tensors ``recv_x`` [rows_r, H] (bf16, or uint8 codes for FP8),
-    ``recv_scale`` [rows_r, H / 128] (FP8), and optionally ``recv_topk_idx``
-    [rows_r, k], ``recv_topk_w`` [rows_r, k], ``recv_src`` [rows_r]; token t's
-    row for rank r lands in row slot[t][r] - rank_offset[r] of region r."""
+def _region_table(regions: list[dict], H: int, k: int, quant: int):
+    """The C table of per-rank receive regions, after checking every tensor."""
     W = len(regions)
     if W < 1 or W > 32:
         raise ValueError("regions must name 1 to 32 ranks")
-    T, H = _matrix("x", x)
-    _, k = _matrix("topk_idx", topk_idx)
-    _shape("topk_idx", topk_idx, T, k)
-    _shape("topk_w", topk_w, T, k)
-    _shape("slot", slot, T, W)
-    _shape("rank_offset", rank_offset, W + 1)
-    _status(status)
     fp8 = quant == EP_QUANT_FP8_E4M3_B128
     table = (RankRegion * W)()
     for r, g in enumerate(regions):
@@ -586,6 +576,29 @@ def ep_dispatch_regions(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.T
         table[r] = RankRegion(_ptr(rx), _ptr(g.get("recv_scale") if fp8 else None),
                               _ptr(g.get("recv_topk_idx")), _ptr(g.get("recv_topk_w")),
                               _ptr(g.get("recv_src")), rows)
+    return table
+
+
+def ep_dispatch_regions(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                        slot: torch.Tensor, rank_offset: torch.Tensor, regions: list[dict],
+                        quant: int = EP_QUANT_BF16, status: torch.Tensor | None = None,
+                        stream=None) -> None:
+    """ep_dispatch into per-rank regions: ``regions[r]`` is a dict with rank r's
+    receive tensors ``recv_x`` [rows_r, H] (bf16, or uint8 codes for FP8),
+    ``recv_scale`` [rows_r, H / 128] (FP8), and optionally ``recv_topk_idx``
+    [rows_r, k], ``recv_topk_w`` [rows_r, k], ``recv_src`` [rows_r]; token t's
+    row for rank r lands in row slot[t][r] - rank_offset[r] of region r."""
+    W = len(regions)
+    if W < 1 or W > 32:
+        raise ValueError("regions must name 1 to 32 ranks")
+    T, H = _matrix("x", x)
+    _, k = _matrix("topk_idx", topk_idx)
+    _shape("topk_idx", topk_idx, T, k)
+    _shape("topk_w", topk_w, T, k)
+    _shape("slot", slot, T, W)
+    _shape("rank_offset", rank_offset, W + 1)
+    _status(status)
+    table = _region_table(regions, H, k, quant)
     _check_cuda("x", x, torch.bfloat16)
     _check_cuda("topk_idx", topk_idx, torch.int32)
     _check_cuda("topk_w", topk_w, torch.float32)
@@ -596,6 +609,41 @@ def ep_dispatch_regions(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.T
         _ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, W, _ptr(slot), _ptr(rank_offset), table,
         quant, _ptr(status), _stream(stream))
     _raise("ep_dispatch_regions", rc)
+
+
+def ep_dispatch_regions_with_layout(x: torch.Tensor, topk_idx: torch.Tensor,
+                                    topk_w: torch.Tensor, E: int,
+                                    num_tokens_per_expert: torch.Tensor,
+                                    num_tokens_per_rank: torch.Tensor, rank_offset: torch.Tensor,
+                                    slot: torch.Tensor, workspace: torch.Tensor,
+                                    regions: list[dict], quant: int = EP_QUANT_BF16,
+                                    status: torch.Tensor | None = None, stream=None) -> None:
+    """ep_dispatch_layout + ep_dispatch_regions in one call (W = len(regions)):
+    every layout output is written, region r gets rank r's rows."""
+    W = len(regions)
+    if W < 1 or W > 32:
+        raise ValueError("regions must name 1 to 32 ranks")
+    _check_layout_shapes(topk_idx, E, W, num_tokens_per_expert, num_tokens_per_rank, rank_offset,
+                         slot, status)
+    T, H = _matrix("x", x)
+    _, k = _matrix("topk_idx", topk_idx)
+    _shape("topk_idx", topk_idx, T, k)
+    _shape("topk_w", topk_w, T, k)
+    table = _region_table(regions, H, k, quant)
+    for n, t in (("num_tokens_per_expert", num_tokens_per_expert),
+                 ("num_tokens_per_rank", num_tokens_per_rank), ("rank_offset", rank_offset),
+                 ("slot", slot)):
+        _check_cuda(n, t, torch.int32)
+    _check_cuda("workspace", workspace)
+    _check_cuda("x", x, torch.bfloat16)
+    _check_cuda("topk_idx", topk_idx, torch.int32)
+    _check_cuda("topk_w", topk_w, torch.float32)
+    _check_cuda("status", status, torch.int32, optional=True)
+    rc = load_library().ep_dispatch_regions_with_layout(
+        _ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, E, W, _ptr(num_tokens_per_expert),
+        _ptr(num_tokens_per_rank), _ptr(rank_offset), _ptr(slot), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), table, quant, _ptr(status), _stream(stream))
+    _raise("ep_dispatch_regions_with_layout", rc)
 
 
 def ep_combine_regions(y_regions: list[torch.Tensor], slot: torch.Tensor, rank_offset: torch.Tensor,

@@ -188,13 +188,13 @@ int ep_combine(const void* y, const int32_t* slot, int64_t T, int H, int W, int6
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int ep_dispatch_regions(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T,
-                        int H, int k, int W, const int32_t* slot, const int32_t* rank_offset,
-                        const ep_rank_region_t* regions, int quant, int32_t* status,
-                        ep_stream_t stream) {
+namespace {
+// The kernels' table of W receive regions, after checking each region.
+int region_table(const ep_rank_region_t* regions, int W, int quant, const int32_t* rank_offset,
+                 ep::RankRegions* rt) {
   if (W < 1 || W > 32 || !regions || !rank_offset) return EP_ERR_INVALID_ARG;
   const bool fp8 = quant == EP_QUANT_FP8_E4M3_B128;
-  ep::RankRegions rt{};
+  *rt = ep::RankRegions{};
   for (int r = 0; r < W; ++r) {
     const ep_rank_region_t& g = regions[r];
     if (g.rows < 0 || g.rows > kMaxRows) return EP_ERR_INVALID_ARG;
@@ -202,21 +202,52 @@ int ep_dispatch_regions(const void* x, const int32_t* topk_idx, const float* top
     if (!aligned(g.recv_x, 16) || !aligned(g.recv_scale, 4) || !aligned(g.recv_topk_idx, 4) ||
         !aligned(g.recv_topk_w, 4) || !aligned(g.recv_src, 4))
       return EP_ERR_MISALIGNED;
-    rt.x[r] = static_cast<uint8_t*>(g.recv_x);
-    rt.scale[r] = g.recv_scale;
-    rt.topk_idx[r] = g.recv_topk_idx;
-    rt.topk_w[r] = g.recv_topk_w;
-    rt.src[r] = g.recv_src;
-    rt.rows[r] = g.rows;
+    rt->x[r] = static_cast<uint8_t*>(g.recv_x);
+    rt->scale[r] = g.recv_scale;
+    rt->topk_idx[r] = g.recv_topk_idx;
+    rt->topk_w[r] = g.recv_topk_w;
+    rt->src[r] = g.recv_src;
+    rt->rows[r] = g.rows;
   }
-  rt.rank_offset = rank_offset;
-  // the common checks of a dispatch (no single receive buffer: capacity 0)
-  const int rc = check_dispatch(x, topk_idx, topk_w, T, H, k, W, slot, 0, quant, nullptr, nullptr,
-                                nullptr, nullptr, nullptr, status);
-  if (rc != EP_OK) return rc;
+  rt->rank_offset = rank_offset;
   if (!aligned(rank_offset, 4)) return EP_ERR_MISALIGNED;
+  return EP_OK;
+}
+}  // namespace
+
+int ep_dispatch_regions(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T,
+                        int H, int k, int W, const int32_t* slot, const int32_t* rank_offset,
+                        const ep_rank_region_t* regions, int quant, int32_t* status,
+                        ep_stream_t stream) {
+  ep::RankRegions rt;
+  int rc = region_table(regions, W, quant, rank_offset, &rt);
+  if (rc != EP_OK) return rc;
+  // the common checks of a dispatch (no single receive buffer: capacity 0)
+  rc = check_dispatch(x, topk_idx, topk_w, T, H, k, W, slot, 0, quant, nullptr, nullptr, nullptr,
+                      nullptr, nullptr, status);
+  if (rc != EP_OK) return rc;
   return from_cuda(ep::launch_dispatch_regions(x, topk_idx, topk_w, T, H, k, W, slot, quant, rt,
                                                status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ep_dispatch_regions_with_layout(const void* x, const int32_t* topk_idx, const float* topk_w,
+                                    int64_t T, int H, int k, int E, int W,
+                                    int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                                    int32_t* rank_offset, int32_t* slot, void* workspace,
+                                    size_t workspace_bytes, const ep_rank_region_t* regions,
+                                    int quant, int32_t* status, ep_stream_t stream) {
+  int rc = check_layout(topk_idx, T, k, E, W, num_tokens_per_expert, num_tokens_per_rank,
+                        rank_offset, slot, workspace, workspace_bytes, status);
+  if (rc != EP_OK) return rc;
+  ep::RankRegions rt;
+  rc = region_table(regions, W, quant, rank_offset, &rt);
+  if (rc != EP_OK) return rc;
+  rc = check_dispatch(x, topk_idx, topk_w, T, H, k, W, slot, 0, quant, nullptr, nullptr, nullptr,
+                      nullptr, nullptr, status);
+  if (rc != EP_OK) return rc;
+  return from_cuda(ep::launch_dispatch_regions_with_layout(
+      x, topk_idx, topk_w, T, H, k, E, W, num_tokens_per_expert, num_tokens_per_rank, rank_offset,
+      slot, workspace, quant, rt, status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int ep_combine_regions(const void* const* y_regions, const int64_t* y_rows, const int32_t* slot,

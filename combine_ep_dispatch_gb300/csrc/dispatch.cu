@@ -143,13 +143,16 @@ __global__ void __launch_bounds__(kTmaMaxWarps * 32, kTmaCtasPerSm)
   if (x_early) first_loads(kTmaStages);
   pdl_wait();
   first_loads(kTmaStages);
-  const int32_t first_row = region_first_row(rt, W, lane);
 
   const bool fin_mode = fin.chunk_rank != nullptr;  // uniform over the grid
   __shared__ int32_t s_tot[32], s_off[33];
   int32_t* const s_base =
       reinterpret_cast<int32_t*>(smem + kTmaBarBytes + (size_t)cta_warps * kTmaStages * stage_bytes);
   if (fin_mode) build_chunk_base(fin, W, s_base, s_tot, s_off);
+  // each region's first global row: rank_offset, or (finishing the layout,
+  // which writes rank_offset during this kernel) the CTA's own scan of it
+  const int32_t first_row = fin_mode ? (RT::kRegions && lane < W ? s_off[lane] : 0)
+                                     : region_first_row(rt, W, lane);
   // the receive row of (tt, lane), written back to the slot table (the warp
   // owns token tt's entries)
   auto finalize = [&](int s_loc, int64_t tt) -> int {
@@ -487,6 +490,36 @@ cudaError_t launch_dispatch_with_layout(const void* x, const int32_t* topk_idx, 
   return launch_dispatch(x, topk_idx, topk_w, T, H, k, W, slot, capacity_rows, quant, recv_x,
                          recv_scale, recv_topk_idx, recv_topk_w, recv_src, status, stream,
                          /*x_early=*/1);
+}
+
+// The same into per-rank regions: count kernel + a dispatch that finishes the
+// layout where that applies, else the whole layout and then the dispatch (no
+// one-launch kernel for regions).
+cudaError_t launch_dispatch_regions_with_layout(
+    const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T, int H, int k, int E,
+    int W, int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank, int32_t* rank_offset,
+    int32_t* slot, void* workspace, int quant, const RankRegions& regions, int32_t* status,
+    cudaStream_t stream) {
+  TmaShape sh;
+  if (finalize_applies(T, H, W, quant, &sh)) {
+    LayoutChunks ch;
+    cudaError_t e = launch_layout_count(topk_idx, T, k, E, W, workspace, slot, status, stream, &ch);
+    if (e != cudaSuccess) return e;
+    Finalize fin{ch.chunk_rank, ch.chunk_exp, ch.C, ch.shift, E, num_tokens_per_expert,
+                 num_tokens_per_rank, rank_offset, ch.claim};
+    if (quant == EP_QUANT_FP8_E4M3_B128)
+      return launch_dispatch_fp8(x, topk_idx, topk_w, T, H, k, W, slot, /*capacity_rows=*/0,
+                                 nullptr, nullptr, nullptr, nullptr, nullptr, status, stream,
+                                 /*x_early=*/1, fin, regions);
+    return launch_tma(x, topk_idx, topk_w, T, k, W, slot, /*capacity_rows=*/0, nullptr, nullptr,
+                      nullptr, nullptr, status, stream, /*x_early=*/1, sh, fin, regions);
+  }
+  cudaError_t e = launch_layout(topk_idx, T, k, E, W, num_tokens_per_expert, num_tokens_per_rank,
+                                rank_offset, slot, workspace, status, stream);
+  if (e != cudaSuccess) return e;
+  return launch_dispatch_rt(x, topk_idx, topk_w, T, H, k, W, slot, /*capacity_rows=*/0, quant,
+                            nullptr, nullptr, nullptr, nullptr, nullptr, status, stream,
+                            /*x_early=*/1, regions);
 }
 
 }  // namespace ep

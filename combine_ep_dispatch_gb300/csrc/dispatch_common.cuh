@@ -286,6 +286,13 @@ cudaError_t launch_dispatch_regions(const void* x, const int32_t* topk_idx, cons
                                     cudaStream_t stream);
 cudaError_t launch_combine_regions(const RankRegions& y_regions, const int32_t* slot, int64_t T,
                                    int H, int W, void* out, int32_t* status, cudaStream_t stream);
+// ep_dispatch_regions_with_layout: the layout, then (or finished by) the
+// dispatch into per-rank regions, in one call.
+cudaError_t launch_dispatch_regions_with_layout(
+    const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T, int H, int k, int E,
+    int W, int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank, int32_t* rank_offset,
+    int32_t* slot, void* workspace, int quant, const RankRegions& regions, int32_t* status,
+    cudaStream_t stream);
 
 template <typename K>
 inline int grid_for(K kernel, int64_t T, int threads) {

@@ -180,7 +180,6 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
   }
   load_region_view(rt, W, s_rv);
   pdl_wait();
-  const int32_t first_row = region_first_row(rt, W, lane);
   // With a Finalize the slot table holds in-chunk positions: every CTA scans
   // the chunk counts first; the warp taking a token's first segment writes
   // its receive rows back (other segments may read either form).
@@ -188,6 +187,10 @@ __global__ void __launch_bounds__(kDThreads, kFp8MinB)
   __shared__ int32_t s_tot[32], s_off[33];
   const bool fin_mode = fin.chunk_rank != nullptr;  // uniform over the grid
   if (fin_mode) build_chunk_base(fin, W, s_base, s_tot, s_off);
+  // each region's first global row: rank_offset, or (finishing the layout,
+  // which writes rank_offset during this kernel) the CTA's own scan of it
+  const int32_t first_row = fin_mode ? (RT::kRegions && lane < W ? s_off[lane] : 0)
+                                     : region_first_row(rt, W, lane);
   // plain loads: with a Finalize the table is also written during the kernel
   auto slot_entry = [&](int64_t tt) { return lane < W ? slot[tt * W + lane] : -1; };
   if (u < units) {

@@ -294,6 +294,27 @@ EP_API int ep_dispatch_regions(const void* x, const int32_t* topk_idx, const flo
                                int quant, int32_t* status, ep_stream_t stream);
 
 /*
+ * Layout and dispatch into per-rank regions in one call: ep_dispatch_layout
+ * followed by ep_dispatch_regions on the same stream, with their arguments,
+ * limits, results and errors (every layout output is written; region r gets
+ * the rows that ep_dispatch_regions would write).  As in
+ * ep_dispatch_with_layout, the dispatch loads its first rows of x while the
+ * layout kernels run (x must be complete in stream order before this call),
+ * and beyond 1024 tokens (bf16 rows of at least 1 KB, or FP8) it finishes the
+ * layout itself and its bulk-copy warps take tokens from a counter in the
+ * workspace, so the workspace serves one call at a time.  There is no
+ * one-launch form for regions.  Same passages as ep_dispatch_layout and
+ * ep_dispatch_regions.
+ */
+EP_API int ep_dispatch_regions_with_layout(const void* x, const int32_t* topk_idx,
+                                           const float* topk_w, int64_t T, int H, int k, int E,
+                                           int W, int32_t* num_tokens_per_expert,
+                                           int32_t* num_tokens_per_rank, int32_t* rank_offset,
+                                           int32_t* slot, void* workspace, size_t workspace_bytes,
+                                           const ep_rank_region_t* regions, int quant,
+                                           int32_t* status, ep_stream_t stream);
+
+/*
  * Combine from per-rank regions: ep_combine with rank r's expert outputs in an
  * allocation of their own.  The row of (t, r) is y_regions[r] row
  * slot[t][r] - rank_offset[r]; out[t] is the bf16 rounding of the fp32 sum of

@@ -7,7 +7,8 @@
  *   gpu mode (built with -DEP_CLIENT_GPU): a small batch through
  *     ep_dispatch_with_layout and ep_combine with identity experts (the
  *     combine reads the dispatched rows back), then the same rows through
- *     ep_dispatch_regions and ep_combine_regions with every rank's rows in a
+ *     ep_dispatch_regions (and ep_dispatch_regions_with_layout) and
+ *     ep_combine_regions with every rank's rows in a
  *     cudaMalloc of its own.  Every output row must then be d_t * x_t exactly,
  *     with d_t the number of distinct destination ranks of token t: small
  *     integer inputs make the fp32 sum and the bf16 rounding exact, so this
@@ -50,6 +51,10 @@ static int query_mode(void) {
   if (ep_combine_regions(NULL, NULL, NULL, NULL, 10, 256, 33, NULL, NULL, NULL) !=
       EP_ERR_INVALID_ARG)
     return fail("reject 33 ranks of regions");
+  if (ep_dispatch_regions_with_layout(NULL, NULL, NULL, 10, 256, 8, 64, 8, NULL, NULL, NULL, NULL,
+                                      NULL, 0, NULL, EP_QUANT_BF16, NULL,
+                                      NULL) != EP_ERR_INVALID_ARG)
+    return fail("reject the one-call regions dispatch without its arguments");
   printf("query mode ok\n");
   return 0;
 }
@@ -176,6 +181,26 @@ static int gpu_mode(void) {
     for (int64_t i = 1; i < n; ++i)
       if (src[i] <= src[i - 1]) return fail("region rows out of token order");
   }
+  /* layout and dispatch into the regions in one call: the same rows */
+  for (int r = 0; r < W; ++r)
+    if (yrows[r] > 0) CK(cudaMemset(regions[r].recv_x, 0, (size_t)yrows[r] * H * 2));
+  CK(cudaMemset(dslot, 0xff, T * W * 4));
+  CK(cudaMemset(dout, 0, sizeof out));
+  rc = ep_dispatch_regions_with_layout(dx, didx, dw, T, H, K, E, W, dne, dnr, doff, dslot, dws,
+                                       ws_bytes, regions, EP_QUANT_BF16, dst, NULL);
+  if (rc != EP_OK) return fail(ep_status_string(rc));
+  rc = ep_combine_regions(yreg, yrows, dslot, doff, T, H, W, dout, dst, NULL);
+  if (rc != EP_OK) return fail(ep_status_string(rc));
+  CK(cudaDeviceSynchronize());
+  CK(cudaMemcpy(out, dout, sizeof out, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(&status, dst, 4, cudaMemcpyDeviceToHost));
+  if (status != 0) return fail("status word (regions, one call)");
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h)
+      if (out[t * H + h] != bf16_of_int(d[t] * ((t * 7 + h * 3) % 17 - 8))) {
+        fprintf(stderr, "token %d column %d\n", t, h);
+        return fail("combine_regions(dispatch_regions_with_layout(x)) != d_t * x");
+      }
   printf("gpu mode ok: T=%d H=%d E=%d k=%d W=%d R=%d (one buffer and per-rank regions)\n", T, H, E,
          K, W, R);
   return 0;

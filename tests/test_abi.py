@@ -298,3 +298,31 @@ def test_combine_regions_rejects(lib, kw, code):
     rc = lib.ep_combine_regions(ptrs, rows, A, None if kw.get("off_null") else A, 100,
                                 kw.get("H", 256), W, A + kw.get("out_off", 0), None, None)
     assert rc == code
+
+
+@cpu_only
+@pytest.mark.parametrize("kw,code", [
+    (dict(W=0), _lib.EP_ERR_INVALID_ARG),
+    (dict(W=33), _lib.EP_ERR_INVALID_ARG),
+    (dict(E=60), _lib.EP_ERR_INVALID_ARG),                      # E not a multiple of W
+    (dict(table_null=True), _lib.EP_ERR_INVALID_ARG),
+    (dict(rows=-1), _lib.EP_ERR_INVALID_ARG),
+    (dict(region_off=8), _lib.EP_ERR_MISALIGNED),
+    (dict(quant=1, scale_null=True), _lib.EP_ERR_INVALID_ARG),
+    (dict(H=12), _lib.EP_ERR_UNSUPPORTED),
+    (dict(ws_bytes=16), _lib.EP_ERR_WORKSPACE),
+])
+def test_dispatch_regions_with_layout_rejects(lib, kw, code):
+    W = kw.get("W", 8)
+    n = max(W, 1)
+    table = (_lib.RankRegion * n)()
+    for r in range(n):
+        table[r] = _lib.RankRegion(A + 0x100000 * r + (kw.get("region_off", 0) if r == 3 else 0),
+                                   None if kw.get("scale_null") else A, A, A, A,
+                                   kw.get("rows", 100))
+    T, E, k = 100, kw.get("E", 64), 8
+    ws = kw.get("ws_bytes", ep.ep_layout_workspace_bytes(T, max(min(W, 32), 1), 64) + 4096)
+    rc = lib.ep_dispatch_regions_with_layout(
+        A, A, A, T, kw.get("H", 256), k, E, W, A, A, A, A, A, ws,
+        None if kw.get("table_null") else table, kw.get("quant", 0), None, None)
+    assert rc == code

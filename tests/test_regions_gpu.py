@@ -150,3 +150,61 @@ def test_regions_match_the_one_buffer_dispatch():
         assert torch.equal(regs[r]["recv_src"], dc.recv_src[off[r]:off[r + 1]]), r
     assert torch.equal(out.view(torch.int16), dc.out.view(torch.int16))
     assert int(dc.status.item()) == 0
+
+
+@pytest.mark.parametrize("name,T,short", [
+    ("dsv3", None, False),            # the dispatch finishes the layout (bulk-copy rows, claims)
+    ("dsv3_zipf_fp8", None, False),   # FP8, finishing the layout
+    ("qwen", 3000, False),
+    ("decode", None, False),          # no finishing below 1024 tokens: layout, then dispatch
+    ("tiny", None, False),            # register rows
+    ("dsv3", 2048, True),             # regions shorter than their ranks' rows
+])
+def test_regions_with_layout(name, T, short):
+    """ep_dispatch_regions_with_layout against the oracle: every layout output,
+    and region r bit for bit (rows, FP8 scales, metadata), twice in a row."""
+    inp = make_inputs(name, seed=63, T=T)
+    cfg = inp["cfg"]
+    quant = ep.EP_QUANT_FP8_E4M3_B128 if cfg.quant == "fp8" else ep.EP_QUANT_BF16
+    x, idx, w = inp["x"], inp["topk_idx"], inp["topk_w"]
+    Tn, H = x.shape
+    k = idx.shape[1]
+    lay = oracle.layout(idx, cfg.E, cfg.W)
+    off = lay["rank_offset"]
+    counts = np.diff(off)
+    cut = {0: 5, cfg.W - 1: int(counts[-1]) // 2} if short else None
+    regs = _regions(counts, H, k, quant, cut)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    ne = torch.full((cfg.E,), SENT_I32, **i32)
+    nr = torch.full((cfg.W,), SENT_I32, **i32)
+    ro = torch.full((cfg.W + 1,), SENT_I32, **i32)
+    sl = torch.full((Tn, cfg.W), SENT_I32, **i32)
+    ws = torch.zeros(ep.ep_layout_workspace_bytes(Tn, cfg.W, cfg.E), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, **i32)
+    xd, idd, wd = to_dev_bf16(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()
+    for _ in range(2):
+        ep.ep_dispatch_regions_with_layout(xd, idd, wd, cfg.E, ne, nr, ro, sl, ws, regs, quant, st)
+    torch.cuda.synchronize()
+    for key, got in (("num_tokens_per_expert", ne), ("num_tokens_per_rank", nr),
+                     ("rank_offset", ro), ("slot", sl)):
+        assert_rows_equal(got.cpu().numpy(), lay[key], key)
+    R = int(off[-1])
+    want = oracle.dispatch(x, idx, w, lay["slot"], R, quant)
+    over = any(int(counts[r]) > regs[r]["recv_x"].shape[0] for r in range(cfg.W))
+    assert int(st.item()) == (ep.EP_STATUS_CAPACITY if over else 0)
+    for r in range(cfg.W):
+        g = regs[r]
+        n = g["recv_x"].shape[0]
+        lo = int(off[r])
+        got_x = u16(g["recv_x"]) if quant == ep.EP_QUANT_BF16 else g["recv_x"].cpu().numpy()
+        assert_rows_equal(got_x, want["recv_x"][lo:lo + n], f"region {r} rows")
+        if quant != ep.EP_QUANT_BF16:
+            assert_rows_equal(g["recv_scale"].cpu().numpy().view(np.uint32),
+                              want["recv_scale"][lo:lo + n].view(np.uint32), f"region {r} scales")
+        assert_rows_equal(g["recv_topk_idx"].cpu().numpy(), want["recv_topk_idx"][lo:lo + n],
+                          f"region {r} ids")
+        assert_rows_equal(g["recv_topk_w"].cpu().numpy().view(np.uint32),
+                          want["recv_topk_w"][lo:lo + n].view(np.uint32), f"region {r} weights")
+        assert_rows_equal(g["recv_src"].cpu().numpy(), want["recv_src"][lo:lo + n],
+                          f"region {r} sources")

@@ -22,10 +22,11 @@
  *  - Kernels are launched with programmatic dependent launch: each one waits
  *    for the previous kernel on the stream to finish before it touches memory,
  *    so consecutive calls overlap only their launch latency.  The one
- *    exception is inside a single call: in ep_dispatch_with_layout and
- *    ep_dispatch_experts_with_layout the dispatch kernel loads its first rows
- *    of x while that call's own layout kernels run (x must be complete in
- *    stream order before the call, as for any input).
+ *    exception is inside a single call: in ep_dispatch_with_layout,
+ *    ep_dispatch_regions_with_layout and ep_dispatch_experts_with_layout the
+ *    dispatch kernel loads its first rows of x while that call's own layout
+ *    kernels run (x must be complete in stream order before the call, as for
+ *    any input).
  *
  * Notation: T tokens, H hidden size, E experts, k experts per token, W ranks,
  * Er = E / W experts per rank, rank(e) = e / Er, D(t) = the distinct ranks of

@@ -208,3 +208,63 @@ def test_regions_with_layout(name, T, short):
                           want["recv_topk_w"][lo:lo + n].view(np.uint32), f"region {r} weights")
         assert_rows_equal(g["recv_src"].cpu().numpy(), want["recv_src"][lo:lo + n],
                           f"region {r} sources")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_regions_with_layout_fuzz(seed):
+    """Seeded random shapes (ranks, experts, top-k, batch around the 1024-token
+    switch, row sizes, routing with invalid ids) through
+    ep_dispatch_regions_with_layout and ep_combine_regions, against the
+    oracle."""
+    rng = np.random.default_rng(7000 + seed)
+    W = int(rng.choice([1, 2, 3, 8, 16, 32]))
+    E = W * int(rng.integers(1, 17))
+    k = int(rng.integers(1, min(E, 9) + 1))
+    T = int(rng.choice([0, 1, 300, 1024, 1025, 2500]))
+    H = int(rng.choice([256, 1024, 2048, 7168]))
+    quant = int(rng.integers(0, 2))
+    idx = make_routing(rng, T, E, k, "zipf" if seed % 2 else "uniform") if T else \
+        np.zeros((0, k), np.int32)
+    if T:
+        idx[rng.random(idx.shape) < 0.02] = -1
+    x = make_bf16(rng, (T, H))
+    w = rng.standard_normal((T, k)).astype(np.float32)
+    lay = oracle.layout(idx, E, W)
+    off = lay["rank_offset"]
+    counts = np.diff(off)
+    regs = _regions(counts, H, k, quant)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    ne, nr = torch.zeros(E, **i32), torch.zeros(W, **i32)
+    ro, sl = torch.zeros(W + 1, **i32), torch.zeros((T, W), **i32)
+    ws = torch.zeros(max(ep.ep_layout_workspace_bytes(T, W, E), 16), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, **i32)
+    xd = to_dev_bf16(x) if T else torch.zeros((0, H), dtype=torch.bfloat16, device="cuda")
+    ep.ep_dispatch_regions_with_layout(xd, torch.from_numpy(idx).cuda(),
+                                       torch.from_numpy(w).cuda(), E, ne, nr, ro, sl, ws, regs,
+                                       quant, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == lay["status"]
+    for key, got in (("num_tokens_per_expert", ne), ("num_tokens_per_rank", nr),
+                     ("rank_offset", ro), ("slot", sl)):
+        assert_rows_equal(got.cpu().numpy(), lay[key], key)
+    R = int(off[-1])
+    want = oracle.dispatch(x, idx, w, lay["slot"], R, quant)
+    for r in range(W):
+        g = regs[r]
+        n = g["recv_x"].shape[0]
+        lo = int(off[r])
+        got_x = u16(g["recv_x"]) if quant == ep.EP_QUANT_BF16 else g["recv_x"].cpu().numpy()
+        assert_rows_equal(got_x, want["recv_x"][lo:lo + n], f"region {r} rows")
+        if quant != ep.EP_QUANT_BF16:
+            assert_rows_equal(g["recv_scale"].cpu().numpy().view(np.uint32),
+                              want["recv_scale"][lo:lo + n].view(np.uint32), f"region {r} scales")
+        assert_rows_equal(g["recv_src"].cpu().numpy(), want["recv_src"][lo:lo + n],
+                          f"region {r} sources")
+    if T and quant == ep.EP_QUANT_BF16:
+        out = torch.full((T, H), SENT_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        st.zero_()
+        ep.ep_combine_regions([g["recv_x"] for g in regs], sl, ro, out, st)
+        torch.cuda.synchronize()
+        assert_rows_equal(u16(out), oracle.combine(want["recv_x"][:R], lay["slot"])["out"],
+                          "combine of the regions")

@@ -492,14 +492,18 @@ cudaError_t launch_dispatch_with_layout(const void* x, const int32_t* topk_idx, 
                          /*x_early=*/1);
 }
 
-// The same into per-rank regions: count kernel + a dispatch that finishes the
-// layout where that applies, else the whole layout and then the dispatch (no
-// one-launch kernel for regions).
+// The same into per-rank regions, by the same paths: the one-launch kernel
+// for small bf16 batches, count kernel + a dispatch that finishes the layout
+// where that applies, else the whole layout and then the dispatch.
 cudaError_t launch_dispatch_regions_with_layout(
     const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T, int H, int k, int E,
     int W, int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank, int32_t* rank_offset,
     int32_t* slot, void* workspace, int quant, const RankRegions& regions, int32_t* status,
     cudaStream_t stream) {
+  if (prefer_fused(T, H, k, quant))
+    return launch_dispatch_fused_regions(x, topk_idx, topk_w, T, H, k, E, W, num_tokens_per_expert,
+                                         num_tokens_per_rank, rank_offset, slot, regions, status,
+                                         stream);
   TmaShape sh;
   if (finalize_applies(T, H, W, quant, &sh)) {
     LayoutChunks ch;

@@ -286,6 +286,12 @@ cudaError_t launch_dispatch_regions(const void* x, const int32_t* topk_idx, cons
                                     cudaStream_t stream);
 cudaError_t launch_combine_regions(const RankRegions& y_regions, const int32_t* slot, int64_t T,
                                    int H, int W, void* out, int32_t* status, cudaStream_t stream);
+// The one-launch layout + dispatch into per-rank regions (small batches).
+cudaError_t launch_dispatch_fused_regions(const void* x, const int32_t* topk_idx,
+                                          const float* topk_w, int64_t T, int H, int k, int E,
+                                          int W, int32_t* ne, int32_t* nr, int32_t* off,
+                                          int32_t* slot, const RankRegions& regions,
+                                          int32_t* status, cudaStream_t stream);
 // ep_dispatch_regions_with_layout: the layout, then (or finished by) the
 // dispatch into per-rank regions, in one call.
 cudaError_t launch_dispatch_regions_with_layout(

@@ -42,7 +42,7 @@ __device__ __forceinline__ void fused_load_row(const int32_t* __restrict__ row, 
   }
 }
 
-template <int KV, bool VEC>
+template <int KV, bool VEC, class RT>
 __global__ void __launch_bounds__(kFThreads, 1)
     dispatch_fused_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
                           const float* __restrict__ topk_w, int T, int H, int k, int E, int W,
@@ -51,8 +51,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
                           int32_t* __restrict__ rank_offset, int32_t* __restrict__ slot,
                           int64_t cap, uint8_t* __restrict__ recv_x,
                           int32_t* __restrict__ recv_topk_idx, float* __restrict__ recv_topk_w,
-                          int32_t* __restrict__ recv_src, int32_t* __restrict__ status) {
+                          int32_t* __restrict__ recv_src, int32_t* __restrict__ status, RT rt) {
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ typename RT::View s_rv;  // per-rank regions: the table
   __shared__ uint64_t s_bar[kFWarps];
   __shared__ int32_t s_cnt[kFBatches][kFWarps][32];  // rows per (batch, warp, rank)
   __shared__ int32_t s_off[33];
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   if (first)
     for (int e = tid; e < E; e += kFThreads) s_hist[e] = 0;
   __syncthreads();
+  load_region_view(rt, W, s_rv);
   pdl_wait();
 
   // ---------------- layout of the whole batch (every CTA)
@@ -165,38 +167,52 @@ __global__ void __launch_bounds__(kFThreads, 1)
   for (int l = warp; l < n_local; l += kFWarps) {
     const int64_t t = c + (int64_t)l * G;
     const int s = lane < W ? s_lslot[l][lane] : -1;
-    const bool keep = s >= 0 && (int64_t)s < cap;
-    cap_err |= __any_sync(kFull, s >= 0 && (int64_t)s >= cap);
+    // the row in its storage and that storage's capacity (per-rank regions:
+    // the row inside rank lane's region, from this kernel's own offsets)
+    int64_t srow = s, lim = cap;
+    if (RT::kRegions && s >= 0) {
+      srow = storage_row<RT>(s, s_off[lane]);
+      lim = storage_rows<RT>(lane, cap, s_rv);
+    }
+    const bool keep = s >= 0 && srow < lim;
+    cap_err |= __any_sync(kFull, s >= 0 && srow >= lim);
     const unsigned dmask = __ballot_sync(kFull, keep);
     Dests d;
     d.nd = __popc(dmask);
     const int r = nth_set_bit_of_lane(dmask, lane);
-    const int row = __shfl_sync(kFull, s, r & 31);
+    const int row = __shfl_sync(kFull, (int)srow, r & 31);
     d.my_row = r >= 0 ? row : -1;
+    d.my_rank = r;
     d.cap_err = false;
     if (tma) {
       if (lane == 0) {
         mbar_arrive_expect_tx(&s_bar[warp], row_bytes);
         bulk_load(buf, x + t * row_bytes, row_bytes, &s_bar[warp]);
       }
-      carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
+      carry_metadata<RT>(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane,
+                         &s_rv);
       const bool ok = mbar_wait_bounded(&s_bar[warp], uses & 1u);
       ++uses;
       if (!__all_sync(kFull, ok)) {
         timed_out = true;
         break;
       }
-      if (lane < d.nd) bulk_store(recv_x + (int64_t)d.my_row * row_bytes, buf, row_bytes);
+      if (lane < d.nd)
+        bulk_store(rows_base<RT>(s_rv, r & 31, recv_x) + (int64_t)d.my_row * row_bytes, buf,
+                   row_bytes);
       bulk_commit();
       bulk_wait_read<0>();  // the buffer is reused for the warp's next token
       __syncwarp();
     } else {
-      carry_metadata(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane);
+      carry_metadata<RT>(topk_idx, topk_w, t, k, d, recv_topk_idx, recv_topk_w, recv_src, lane,
+                         &s_rv);
       const uint4* src = reinterpret_cast<const uint4*>(x + t * row_bytes);
       const int n16 = (int)(row_bytes / 16);
       for (int q = 0; q < d.nd; ++q) {
         const int64_t dst_row = __shfl_sync(kFull, d.my_row, q);
-        uint4* dst = reinterpret_cast<uint4*>(recv_x + dst_row * row_bytes);
+        const int dst_rank = __shfl_sync(kFull, r, q);
+        uint4* dst = reinterpret_cast<uint4*>(rows_base<RT>(s_rv, dst_rank & 31, recv_x) +
+                                              dst_row * row_bytes);
         for (int cidx = lane; cidx < n16; cidx += 32) st_v4(dst + cidx, ld_stream_v4(src + cidx));
       }
     }
@@ -214,11 +230,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
   }
 }
 
-template <int KV, bool VEC>
+template <int KV, bool VEC, class RT>
 cudaError_t launch_fused(const void* x, const int32_t* topk_idx, const float* topk_w, int T,
                          int H, int k, int E, int W, int32_t* ne, int32_t* nr, int32_t* off,
                          int32_t* slot, int64_t cap, void* recv_x, int32_t* ridx, float* rw,
-                         int32_t* rsrc, int32_t* status, cudaStream_t stream) {
+                         int32_t* rsrc, int32_t* status, cudaStream_t stream, const RT& rt) {
   const uint32_t row_bytes = (uint32_t)H * 2u;
   const bool tma = row_bytes >= 1024 && row_bytes <= kFMaxTmaRow;
   const uint32_t row_pad = (row_bytes + 127u) & ~127u;
@@ -228,7 +244,7 @@ cudaError_t launch_fused(const void* x, const int32_t* topk_idx, const float* to
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 128 && !attr_set[dev]) {
     const int most = (int)((size_t)kFWarps * kFMaxTmaRow + sizeof(int32_t) * 8192);
-    cudaError_t e = cudaFuncSetAttribute(dispatch_fused_kernel<KV, VEC>,
+    cudaError_t e = cudaFuncSetAttribute(dispatch_fused_kernel<KV, VEC, RT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
@@ -238,30 +254,50 @@ cudaError_t launch_fused(const void* x, const int32_t* topk_idx, const float* to
   const int at_least = (T + kFMaxLocal - 1) / kFMaxLocal;  // a CTA owns at most kFMaxLocal tokens
   if (grid < at_least) grid = at_least;
   if (grid < 1) grid = 1;
-  return launch_pdl(dispatch_fused_kernel<KV, VEC>, dim3(grid), dim3(kFThreads), smem, stream,
+  return launch_pdl(dispatch_fused_kernel<KV, VEC, RT>, dim3(grid), dim3(kFThreads), smem, stream,
                     static_cast<const uint8_t*>(x), topk_idx, topk_w, T, H, k, E, W, E / W, ne, nr,
-                    off, slot, cap, static_cast<uint8_t*>(recv_x), ridx, rw, rsrc, status);
+                    off, slot, cap, static_cast<uint8_t*>(recv_x), ridx, rw, rsrc, status, rt);
 }
 
 }  // namespace
 
 int64_t fused_max_tokens() { return kFusedMaxT; }
 
+namespace {
+template <class RT>
+cudaError_t launch_fused_rt(const void* x, const int32_t* topk_idx, const float* topk_w, int64_t T,
+                            int H, int k, int E, int W, int32_t* ne, int32_t* nr, int32_t* off,
+                            int32_t* slot, int64_t cap, void* recv_x, int32_t* ridx, float* rw,
+                            int32_t* rsrc, int32_t* status, cudaStream_t stream, const RT& rt) {
+  const int Ti = (int)T;
+  const bool vec = (reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0;
+  if (k == 8 && vec)
+    return launch_fused<8, true>(x, topk_idx, topk_w, Ti, H, k, E, W, ne, nr, off, slot, cap,
+                                 recv_x, ridx, rw, rsrc, status, stream, rt);
+  if (k == 4 && vec)
+    return launch_fused<4, true>(x, topk_idx, topk_w, Ti, H, k, E, W, ne, nr, off, slot, cap,
+                                 recv_x, ridx, rw, rsrc, status, stream, rt);
+  return launch_fused<16, false>(x, topk_idx, topk_w, Ti, H, k, E, W, ne, nr, off, slot, cap,
+                                 recv_x, ridx, rw, rsrc, status, stream, rt);
+}
+}  // namespace
+
 cudaError_t launch_dispatch_fused(const void* x, const int32_t* topk_idx, const float* topk_w,
                                   int64_t T, int H, int k, int E, int W, int32_t* ne, int32_t* nr,
                                   int32_t* off, int32_t* slot, int64_t cap, void* recv_x,
                                   int32_t* ridx, float* rw, int32_t* rsrc, int32_t* status,
                                   cudaStream_t stream) {
-  const int Ti = (int)T;
-  const bool vec = (reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0;
-  if (k == 8 && vec)
-    return launch_fused<8, true>(x, topk_idx, topk_w, Ti, H, k, E, W, ne, nr, off, slot, cap,
-                                 recv_x, ridx, rw, rsrc, status, stream);
-  if (k == 4 && vec)
-    return launch_fused<4, true>(x, topk_idx, topk_w, Ti, H, k, E, W, ne, nr, off, slot, cap,
-                                 recv_x, ridx, rw, rsrc, status, stream);
-  return launch_fused<16, false>(x, topk_idx, topk_w, Ti, H, k, E, W, ne, nr, off, slot, cap,
-                                 recv_x, ridx, rw, rsrc, status, stream);
+  return launch_fused_rt(x, topk_idx, topk_w, T, H, k, E, W, ne, nr, off, slot, cap, recv_x, ridx,
+                         rw, rsrc, status, stream, OneBuffer{});
+}
+
+cudaError_t launch_dispatch_fused_regions(const void* x, const int32_t* topk_idx,
+                                          const float* topk_w, int64_t T, int H, int k, int E,
+                                          int W, int32_t* ne, int32_t* nr, int32_t* off,
+                                          int32_t* slot, const RankRegions& regions,
+                                          int32_t* status, cudaStream_t stream) {
+  return launch_fused_rt(x, topk_idx, topk_w, T, H, k, E, W, ne, nr, off, slot, /*cap=*/0,
+                         nullptr, nullptr, nullptr, nullptr, status, stream, regions);
 }
 
 }  // namespace ep

@@ -303,9 +303,9 @@ EP_API int ep_dispatch_regions(const void* x, const int32_t* topk_idx, const flo
  * layout kernels run (x must be complete in stream order before this call),
  * and beyond 1024 tokens (bf16 rows of at least 1 KB, or FP8) it finishes the
  * layout itself and its bulk-copy warps take tokens from a counter in the
- * workspace, so the workspace serves one call at a time.  There is no
- * one-launch form for regions.  Same passages as ep_dispatch_layout and
- * ep_dispatch_regions.
+ * workspace, so the workspace serves one call at a time; bf16 batches of up
+ * to 512 tokens take the one-launch kernel, as in ep_dispatch_with_layout.
+ * Same passages as ep_dispatch_layout and ep_dispatch_regions.
  */
 EP_API int ep_dispatch_regions_with_layout(const void* x, const int32_t* topk_idx,
                                            const float* topk_w, int64_t T, int H, int k, int E,

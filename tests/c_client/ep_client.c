@@ -8,11 +8,13 @@
  *     ep_dispatch_with_layout and ep_combine with identity experts (the
  *     combine reads the dispatched rows back), then the same rows through
  *     ep_dispatch_regions (and ep_dispatch_regions_with_layout) and
- *     ep_combine_regions with every rank's rows in a
- *     cudaMalloc of its own.  Every output row must then be d_t * x_t exactly,
- *     with d_t the number of distinct destination ranks of token t: small
- *     integer inputs make the fp32 sum and the bf16 rounding exact, so this
- *     closed form needs no reference implementation.
+ *     ep_combine_regions with every rank's rows in a cudaMalloc of its own.
+ *     Every output row must then be d_t * x_t exactly, with d_t the number
+ *     of distinct destination ranks of token t: small integer inputs make the
+ *     fp32 sum and the bf16 rounding exact, so this closed form needs no
+ *     reference implementation.  Then the expert-major path
+ *     (ep_dispatch_experts_with_layout, ep_combine_weighted with unit
+ *     weights), whose rows must be k * x_t.
  */
 #include <stdio.h>
 #include <stdlib.h>
@@ -72,6 +74,73 @@ static uint16_t bf16_of_int(int v) {
   do {                                                        \
     if ((call) != cudaSuccess) return fail(#call);            \
   } while (0)
+
+/* The expert-major path from C: ep_dispatch_experts_with_layout (one row per
+   (token, expert) pair, 2800 pairs: the chunked layout whose dispatch claims
+   tokens, bulk-copy rows of 1 KB) and ep_combine_weighted with unit weights,
+   so that every output row must be k * x_t exactly. */
+static int expert_major(void) {
+  enum { T = 700, H = 512, E = 32, K = 4 };
+  static int32_t idx[T * K];
+  static float ones[T * K];
+  static uint16_t x[T * H], out[T * H];
+  uint32_t lcg = 777u;
+  for (int t = 0; t < T; ++t) {
+    for (int j = 0; j < K; ++j) {
+      int e, dup;
+      do {
+        lcg = lcg * 1664525u + 1013904223u;
+        e = (int)((lcg >> 8) % E);
+        dup = 0;
+        for (int i = 0; i < j; ++i) dup |= idx[t * K + i] == e;
+      } while (dup);
+      idx[t * K + j] = e;
+      ones[t * K + j] = 1.0f;
+    }
+    for (int h = 0; h < H; ++h) x[t * H + h] = bf16_of_int((t * 5 + h) % 13 - 6);
+  }
+  const int64_t cap = (int64_t)T * K;
+  const size_t ws_bytes = ep_layout_experts_workspace_bytes(T, K, E);
+  void *dx, *dy, *dout, *dws;
+  int32_t *didx, *dne, *doff, *dslot, *dsrc, *dst;
+  float* dw;
+  CK(cudaMalloc((void**)&dx, sizeof x));
+  CK(cudaMalloc((void**)&didx, sizeof idx));
+  CK(cudaMalloc((void**)&dw, sizeof ones));
+  CK(cudaMalloc((void**)&dne, E * 4));
+  CK(cudaMalloc((void**)&doff, (E + 1) * 4));
+  CK(cudaMalloc((void**)&dslot, T * K * 4));
+  CK(cudaMalloc((void**)&dws, ws_bytes));
+  CK(cudaMalloc((void**)&dy, (size_t)cap * H * 2));
+  CK(cudaMalloc((void**)&dsrc, (size_t)cap * 4));
+  CK(cudaMalloc((void**)&dout, sizeof out));
+  CK(cudaMalloc((void**)&dst, 4));
+  CK(cudaMemset(dst, 0, 4));
+  CK(cudaMemcpy(dx, x, sizeof x, cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(didx, idx, sizeof idx, cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(dw, ones, sizeof ones, cudaMemcpyHostToDevice));
+  int rc = ep_dispatch_experts_with_layout(dx, didx, dw, T, H, K, E, dne, doff, dslot, dws,
+                                           ws_bytes, cap, EP_QUANT_BF16, dy, NULL, NULL, NULL,
+                                           dsrc, dst, NULL);
+  if (rc != EP_OK) return fail(ep_status_string(rc));
+  rc = ep_combine_weighted(dy, dslot, dw, T, H, K, cap, dout, dst, NULL);
+  if (rc != EP_OK) return fail(ep_status_string(rc));
+  CK(cudaDeviceSynchronize());
+  int32_t status = -1, off[E + 1];
+  CK(cudaMemcpy(out, dout, sizeof out, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(off, doff, sizeof off, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(&status, dst, 4, cudaMemcpyDeviceToHost));
+  if (status != 0) return fail("status word (expert-major)");
+  if (off[E] != T * K) return fail("expert_offset[E] != T * k");
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h)
+      if (out[t * H + h] != bf16_of_int(K * ((t * 5 + h) % 13 - 6))) {
+        fprintf(stderr, "token %d column %d\n", t, h);
+        return fail("weighted combine of the expert-major rows != k * x");
+      }
+  printf("gpu mode ok: expert-major T=%d H=%d E=%d k=%d\n", T, H, E, K);
+  return 0;
+}
 
 static int gpu_mode(void) {
   enum { T = 300, H = 256, E = 64, K = 4, W = 8 };
@@ -203,7 +272,7 @@ static int gpu_mode(void) {
       }
   printf("gpu mode ok: T=%d H=%d E=%d k=%d W=%d R=%d (one buffer and per-rank regions)\n", T, H, E,
          K, W, R);
-  return 0;
+  return expert_major();
 }
 #endif
 
